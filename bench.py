@@ -1,0 +1,480 @@
+"""Benchmark of the block-FP8 MoE layer forward on GB300 (decode shape).
+
+Workload: the decode configuration -- M tokens (default 32) of hidden size 7168, local
+intermediate size 256 (gate/up width 512), E = 256 experts, top-k 8, uniform random routing,
+E4M3 weights with 128x128 fp32 block scales, BF16 activations ~N(0, 1), fp32 dynamic
+activation scales.  Inputs are seeded and synthetic; weights are random (no checkpoint).
+
+One step = one whole layer forward (route preparation, input quantisation, gate/up GEMM,
+fused SiLU*mul + quantisation, down GEMM, moe_reduce) through moe_blockfp8_forward, replayed
+from a CUDA graph.  Eight routing batches rotate between steps and a 256 MiB buffer is written
+between timed steps (outside the events) so no step starts with its weights in L2.
+
+Prints one JSON line.  --impl reference times the CPU oracle instead (a bounded token sample
+per step, scaled to the layer latency).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer latency (us) & HBM GB/s (fraction of roofline) at decode M=1..256"
+DECODE = dict(H=7168, N=256, E=256, k=8)
+NROT = 8
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--M", type=int, default=32)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [s for s in sm if smax and s >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------------------------
+def active_bytes(ids_list, H, N, E):
+    """Algorithmic HBM bytes of one layer forward per routing batch: the active experts'
+    E4M3 weights and fp32 block scales, read once."""
+    per_expert_gu = 2 * N * H + (2 * N // 128) * (H // 128) * 4
+    per_expert_d = H * N + (H // 128) * (N // 128) * 4
+    out = []
+    for ids in ids_list:
+        a = len(np.unique(ids[(ids >= 0) & (ids < E)]))
+        out.append((a, a * per_expert_gu, a * per_expert_d))
+    return out
+
+
+def make_inputs(M, seed, dev):
+    import torch
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    xs, ids, ws = [], [], []
+    for r in range(NROT):
+        i, w = wl.routing_topk(M, DECODE["E"], DECODE["k"], seed=seed * 1000 + r, kind="uniform")
+        x = wl.bf16_normal((M, DECODE["H"]), 1.0, seed * 1000 + 500 + r)
+        xs.append(x.to(dev))
+        ids.append(torch.from_numpy(i).to(dev))
+        ws.append(torch.from_numpy(w).to(dev))
+    return xs, ids, ws
+
+
+def capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
+
+
+def make_event(external=False):
+    import torch
+    try:
+        return torch.cuda.Event(enable_timing=True, external=external)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
+def time_graph_steps(graphs, steps, warmup, flush, stream):
+    """Per-step device time (ms) of graph replays, L2 flushed between steps (outside events)."""
+    import torch
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            flush.zero_()
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        evs = [(make_event(), make_event()) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            graphs[i % len(graphs)].replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        times = [a.elapsed_time(b) for a, b in evs]
+    return times
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_fp8_mixture_moe_gb300 import ops, workloads as wl
+
+    H, N, E, k = DECODE["H"], DECODE["N"], DECODE["E"], DECODE["k"]
+    M = args.M
+    wgu_q, wgu_s = wl.quantized_weights(E, 2 * N, H, seed=args.seed * 7919 + 5, device=dev)
+    wd_q, wd_s = wl.quantized_weights(E, H, N, seed=args.seed * 7919 + 6, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def layer_graphs(M_):
+        xs, ids, ws = make_inputs(M_, args.seed, dev)
+        need = ops.moe_blockfp8_workspace_bytes(M_, k, E, E, H, N)
+        work = torch.empty(need, dtype=torch.uint8, device=dev)
+        outs = [torch.empty((M_, H), dtype=torch.bfloat16, device=dev) for _ in range(NROT)]
+        graphs = []
+        for r in range(NROT):
+            fn = (lambda r=r: ops.moe_blockfp8_forward(xs[r], ids[r], ws[r], E, None, wgu_q, wgu_s,
+                                                       wd_q, wd_s, out=outs[r], workspace=work,
+                                                       stream=stream))
+            graphs.append(capture(fn, stream))
+        return xs, ids, ws, outs, work, graphs
+
+    xs, ids, ws, outs, work, graphs = layer_graphs(M)
+    ids_host = [t.cpu().numpy() for t in ids]
+    act = active_bytes(ids_host, H, N, E)
+    bm, B_cap, splits = ops.moe_blockfp8_plan(M, k, E, E, H, N)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    step_ms = time_graph_steps(graphs, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    layer_bytes = [a[1] + a[2] for a in act]
+    mean_bytes = sum(layer_bytes[i % NROT] for i in range(args.steps)) / args.steps
+
+    # ---- the dominant kernel (gate/up GEMM) timed with events on its own stream -------------
+    gemm_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, wd_q, wd_s,
+                                  M, H, N, E, k, args.steps, args.warmup)
+    gu_bytes = []
+    for i, (a, gub, _) in enumerate(act):
+        kept = M * k
+        gu_bytes.append(gub + kept * (H + (H // 128) * 4) + kept * 2 * N * 2)
+    gu_mean_bytes = sum(gu_bytes) / len(gu_bytes)
+
+    # ---- end to end through the public API with host buffers --------------------------------
+    e2e_ms, h2d, d2h = time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, args.steps, args.warmup)
+    clocks = sampler.stop()
+
+    sweep = None
+    if not args.no_sweep:
+        sweep = {}
+        for Ms in (1, 4, 16, 32, 64, 128, 256):
+            _, ids_s, _, _, _, g_s = layer_graphs(Ms)
+            a_s = active_bytes([t.cpu().numpy() for t in ids_s], H, N, E)
+            t = time_graph_steps(g_s, 50, 5, flush, stream)
+            by = sum(a_s[i % NROT][1] + a_s[i % NROT][2] for i in range(50)) / 50
+            us = statistics.mean(t) * 1e3
+            sweep[str(Ms)] = {"us": round(us, 2), "us_median": round(statistics.median(t) * 1e3, 2),
+                              "active_experts": round(sum(a[0] for a in a_s) / NROT, 1),
+                              "GBps": round(by / (us * 1e-6) / 1e9, 1)}
+            del g_s
+
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    achieved = gu_mean_bytes / (statistics.mean(gemm_ms) * 1e-3) / 1e9
+    traffic = recorded_traffic()
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = cpu_baseline(M, ids_host[0], xs[0], wgu_q, wgu_s, wd_q, wd_s, H, N, E, k)
+
+    launches_per_step = (1 if M * k <= 2048 else 2) + 5
+    layer_us = ms_per_step * 1e3
+    line = {
+        "metric": METRIC, "value": round(layer_us, 3), "unit": "us", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded; random weights, uniform random routing)",
+        "config": {"workload": f"decode MoE layer M={M} H={H} N={N} E={E} top-k={k}, block-FP8 128x128",
+                   "M": M, "H": H, "N": N, "E": E, "topk": k, "block_m": bm, "gate_up_splits": splits,
+                   "l2": "256 MiB buffer written between timed steps (outside the events); 8 rotating routing batches",
+                   "timing": "CUDA graph replay per step, CUDA events per step", "parallelism": f"replicas x{world}"},
+        "layer_hbm": {"GBps": round(mean_bytes / (layer_us * 1e-6) / 1e9, 1),
+                      "frac": round(mean_bytes / (layer_us * 1e-6) / 1e9 / hbm_peak, 4),
+                      "active_bytes": int(mean_bytes), "peak": hbm_peak, "peak_source": peak_src,
+                      "us_median": round(statistics.median(step_ms) * 1e3, 2),
+                      "us_p10": round(float(np.percentile(step_ms, 10)) * 1e3, 2),
+                      "us_p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2)},
+        "roofline": {"bound": "hbm", "kernel": "k_grouped_gemm<16> (gate/up)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": int(gu_mean_bytes),
+                     "kernel_us": round(statistics.mean(gemm_ms) * 1e3, 2),
+                     "peak_source": peak_src},
+        "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "sweep_M": sweep,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, wd_q, wd_s, M, H, N,
+                        E, k, steps, warmup):
+    """The layer's stages launched one by one through the per-stage entry points, with events
+    around the gate/up GEMM only; returns its per-launch device times (ms)."""
+    import torch
+    bm, B_cap, splits = ops.moe_blockfp8_plan(M, k, E, E, H, N)
+    slots = B_cap * bm
+    gu = torch.empty((splits, slots, 2 * N), dtype=torch.float32, device=dev)
+    xq = torch.empty((slots, H), dtype=torch.uint8, device=dev)
+    xsc = torch.empty((slots, H // 128), dtype=torch.float32, device=dev)
+    routes = []
+    with torch.cuda.stream(stream):
+        for r in range(NROT):
+            route = ops.moe_route_prepare(ids[r], E, None, E, bm, stream=stream)
+            routes.append(route)
+        torch.cuda.synchronize()
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            r = i % NROT
+            route = routes[r]
+            ops.silu_mul_quant_fp8(0, xs[r], H, rows=M * k, row_map=route["route_slot"], row_div=k,
+                                   out_rows=slots, out_q=xq, out_s=xsc, stream=stream)
+            flush.zero_()
+            torch.cuda._sleep(2_000_000)  # keep the device busy while the host enqueues
+            e0, e1 = make_event(), make_event()
+            e0.record(stream)
+            ops.moe_blockfp8_grouped_gemm(0, xq, xsc, wgu_q, wgu_s, route, bm, out_dtype=ops.DTYPE_F32,
+                                          out_rows=slots, splits=splits, out=gu, stream=stream)
+            e1.record(stream)
+            if i >= warmup:
+                times.append((e0, e1))
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, steps, warmup):
+    """Per step: host->device copy of x, topk_ids, topk_w from pinned host buffers, the layer
+    (graph of moe_blockfp8_forward), device->host copy of the output; events around all of it."""
+    import torch
+    hx = [x.cpu().pin_memory() for x in xs]
+    hi = [t.cpu().pin_memory() for t in ids]
+    hw = [t.cpu().pin_memory() for t in ws]
+    ho = [o.cpu().pin_memory() for o in outs]
+    h2d = hx[0].numel() * 2 + hi[0].numel() * 4 + hw[0].numel() * 4
+    d2h = ho[0].numel() * 2
+    evs = []
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            r = i % NROT
+            flush.zero_()
+            e0, e1 = make_event(), make_event()
+            e0.record(stream)
+            xs[r].copy_(hx[r], non_blocking=True)
+            ids[r].copy_(hi[r], non_blocking=True)
+            ws[r].copy_(hw[r], non_blocking=True)
+            graphs[r].replay()
+            ho[r].copy_(outs[r], non_blocking=True)
+            e1.record(stream)
+            if i >= warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+    t = [a.elapsed_time(b) for a, b in evs]
+    return statistics.mean(t), h2d, d2h
+
+
+def recorded_traffic():
+    """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken on the
+    current kernel source (otherwise null)."""
+    path = os.path.join(ROOT, "profiles", "gate_up_gemm_decode_traffic.json")
+    try:
+        rec = json.load(open(path))
+        src = open(os.path.join(ROOT, "block_fp8_mixture_moe_gb300", "csrc", "grouped_gemm.cu"), "rb").read()
+        if rec.get("grouped_gemm_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return rec.get("dram_bytes_per_launch_full_size")
+    except Exception:
+        return None
+
+
+def cpu_baseline(M, ids0, x0, wgu_q, wgu_s, wd_q, wd_s, H, N, E, k, sample_tokens=4):
+    """The oracle's sparse layer on a 4-token sample of the first routing batch (weights of the
+    sample's experts copied to the host), timed on all host cores and scaled to M tokens."""
+    import torch
+    import oracle
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    toks = list(range(min(sample_tokens, M)))
+    used = np.unique(ids0[toks])
+    layer = dict(x=x0.view(torch.int16).cpu().numpy().view(np.uint16), topk_ids=ids0,
+                 topk_w=np.full(ids0.shape, 1.0 / k, np.float32), expert_map=None,
+                 wgu_q=wgu_q, wgu_s=wgu_s, wd_q=wd_q, wd_s=wd_s, E=E, M=M, H=H, N=N, k=k)
+    host = wl.layer_numpy(layer, experts=used)
+    threads = oracle.set_threads(0)
+    oracle.moe_forward(host, tokens=toks)  # warm (page-in)
+    runs = []
+    t_end = time.time() + 10.0
+    while time.time() < t_end or len(runs) < 3:
+        t0 = time.perf_counter()
+        oracle.moe_forward(host, tokens=toks)
+        runs.append(time.perf_counter() - t0)
+        if len(runs) >= 50:
+            break
+    per_layer_us = statistics.median(runs) * (M / len(toks)) * 1e6
+    return {"value": round(per_layer_us, 1), "unit": "us", "cores": threads, "kind": "oracle",
+            "sample": f"{len(toks)} of {M} tokens (their {len(used)} experts), median of {len(runs)} runs, scaled x{M / len(toks):g}"}
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------------------------
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    oracle.build()
+    H, N, E, k = DECODE["H"], DECODE["N"], DECODE["E"], DECODE["k"]
+    M = args.M
+    ids, w = wl.routing_topk(M, E, k, seed=args.seed * 1000, kind="uniform")
+    x = wl.bf16_normal((M, H), 1.0, args.seed * 1000 + 500).view(torch.int16).numpy().view(np.uint16)
+    # one token per step; only the experts of the sampled tokens need weights on the host
+    sample = list(range(min(M, 4)))
+    used = np.unique(ids[sample])
+    remap = {int(g): i for i, g in enumerate(used)}
+    ids_s = np.array([[remap.get(int(g), -1) for g in row] for row in ids], np.int32)
+    wgu_q, wgu_s = wl.quantized_weights(len(used), 2 * N, H, seed=5)
+    wd_q, wd_s = wl.quantized_weights(len(used), H, N, seed=6)
+    layer = dict(x=x, topk_ids=ids_s, topk_w=w, expert_map=None, wgu_q=wgu_q.numpy(),
+                 wgu_s=wgu_s.numpy(), wd_q=wd_q.numpy(), wd_s=wd_s.numpy(), E=len(used), M=M,
+                 H=H, N=N, k=k)
+    threads = oracle.set_threads(0)
+    for i in range(args.warmup):
+        oracle.moe_forward(layer, tokens=[sample[i % len(sample)]])
+    t = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.moe_forward(layer, tokens=[sample[i % len(sample)]])
+        t.append(time.perf_counter() - t0)
+    per_layer_us = statistics.mean(t) * M * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(per_layer_us, 1), "unit": "us",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.mean(t) * 1e3, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": f"decode MoE layer M={M} H={H} N={N} E={E} top-k={k}, block-FP8 128x128",
+                   "M": M, "H": H, "N": N, "E": E, "topk": k},
+        "cpu_baseline": {"value": round(per_layer_us, 1), "unit": "us", "kind": "oracle", "cores": threads,
+                         "sample": f"1 token per step (of {M}), scaled x{M}"},
+        "e2e": {"value": round(per_layer_us, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

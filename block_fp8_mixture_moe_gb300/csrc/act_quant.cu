@@ -1,0 +1,310 @@
+// act_quant.cu -- fused (optionally clamped) SiLU-and-mul + per-128-group dynamic E4M3
+// quantisation, and the input quantisation (identity activation) that feeds the W8A8 gate/up
+// GEMM.
+//
+// Method: vLLM PR #53875 "Fuse clamped MoE activation and UE8M0 FP8 block quantization",
+// section "Purpose" (clamp, BF16 SiLU and gated multiplication, dynamic E4M3 block
+// quantisation with optional UE8M0 scales, optional filtering of invalid or non-local rows);
+// lmdeploy PR #4956 "Perf/pytorch block fp8 moe decode", section "Fused SwiGLU and FP8
+// quantization" (no BF16 intermediate in memory; bitwise equal to the two-kernel path).
+//
+// Layout of the work: one half-warp (16 lanes) owns one 128-wide quant group; every lane loads
+// 8 BF16 gate values and 8 BF16 up values with one 16-byte load each (or 2x16-byte loads per
+// split for fp32 split-K partials), materialises the 8 BF16 activations in registers, and the
+// group amax is a 4-step xor-shuffle reduction inside the half-warp.  Each lane then stores its
+// 8 E4M3 codes as one 8-byte store (128 contiguous bytes per group) and lane 0 of the half-warp
+// stores the group scale.  A warp always processes a pair of groups, so both halves run the
+// same loop and the full-mask shuffles never see a divergent partner.
+//
+// Two launch shapes (the pages' two strategies): PER_GROUP -- one warp per group pair, no loop,
+// for launch-bound decode shapes without a filter; PERSISTENT -- a grid sized to the SM count
+// that strides over the group pairs, for filtered (expert-parallel) inputs and large outputs.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+struct AQArgs {
+    const void* in;
+    long long split_stride;  // elements between fp32 split partials
+    int in_rows;
+    int rows, N, G, W;
+    float L;
+    int fmt;
+    const int32_t* row_expert;
+    const int32_t* expert_map;
+    int E;
+    const int32_t* row_map;
+    int row_div;
+    int out_rows;
+    uint8_t* out_q;
+    float* out_s;
+    int in_splits;
+    int* status;
+};
+
+// Loads 8 consecutive inputs as fp32 values of their BF16 materialisation.
+template <bool F32IN>
+__device__ __forceinline__ void load8(const AQArgs& p, long long off, float* v) {
+    if (!F32IN) {
+        uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.in) + off));
+        v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+        v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+    } else {
+        // split-K partials: summed in split order in fp32, then rounded to BF16 once
+        const float* base = static_cast<const float*>(p.in) + off;
+        float4 a = __ldg(reinterpret_cast<const float4*>(base));
+        float4 b = __ldg(reinterpret_cast<const float4*>(base) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        for (int s = 1; s < p.in_splits; ++s) {
+            const float* q = base + s * p.split_stride;
+            float4 c = __ldg(reinterpret_cast<const float4*>(q));
+            float4 d = __ldg(reinterpret_cast<const float4*>(q) + 1);
+            v[0] = __fadd_rn(v[0], c.x); v[1] = __fadd_rn(v[1], c.y);
+            v[2] = __fadd_rn(v[2], c.z); v[3] = __fadd_rn(v[3], c.w);
+            v[4] = __fadd_rn(v[4], d.x); v[5] = __fadd_rn(v[5], d.y);
+            v[6] = __fadd_rn(v[6], d.z); v[7] = __fadd_rn(v[7], d.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = bf16_round_f32(v[i]);
+    }
+}
+
+// Decides whether work row `w` is produced, and its input and output rows.
+__device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, int* out_row) {
+    int src = w, dst = w;
+    if (p.row_expert) {
+        int id = __ldg(p.row_expert + w);
+        if (id < 0 || id >= p.E) return false;
+        if (p.expert_map && __ldg(p.expert_map + id) < 0) return false;
+    }
+    if (p.row_map) {
+        int m = __ldg(p.row_map + w);
+        if (m < 0) return false;
+        dst = m;
+        src = p.row_div > 0 ? w / p.row_div : m;
+    }
+    if (src >= p.in_rows || dst >= p.out_rows) {
+        if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+        return false;
+    }
+    *in_row = src;
+    *out_row = dst;
+    return true;
+}
+
+template <int ACT, bool F32IN>
+__device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int lane) {
+    const int half = lane >> 4, l = lane & 15;
+    const long long item = pair * 2 + half;
+    bool active = item < static_cast<long long>(p.rows) * p.G;
+    int row = 0, g = 0, in_row = 0;
+    if (active) {
+        const int w = static_cast<int>(item / p.G);
+        g = static_cast<int>(item - static_cast<long long>(w) * p.G);
+        active = row_source(p, w, &in_row, &row);
+    }
+    float a[8];
+    float amax = 0.0f;
+    if (active) {
+        const long long col = static_cast<long long>(g) * 128 + l * 8;
+        const long long rbase = static_cast<long long>(in_row) * p.W;
+        if (ACT == MOE_ACT_IDENTITY) {
+            load8<F32IN>(p, rbase + col, a);
+        } else {
+            float gv[8], uv[8];
+            load8<F32IN>(p, rbase + col, gv);
+            load8<F32IN>(p, rbase + p.N + col, uv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = silu_mul_bf16<ACT>(gv[i], uv[i], p.L);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(a[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    if (active) {
+        const float s = group_scale(amax, p.fmt);
+        const float inv = p.fmt == MOE_SCALE_UE8M0 ? pow2_reciprocal(s) : 0.0f;
+        uint32_t c0 = cvt_e4m3x2(quant_div(a[0], s, inv, p.fmt), quant_div(a[1], s, inv, p.fmt));
+        uint32_t c1 = cvt_e4m3x2(quant_div(a[2], s, inv, p.fmt), quant_div(a[3], s, inv, p.fmt));
+        uint32_t c2 = cvt_e4m3x2(quant_div(a[4], s, inv, p.fmt), quant_div(a[5], s, inv, p.fmt));
+        uint32_t c3 = cvt_e4m3x2(quant_div(a[6], s, inv, p.fmt), quant_div(a[7], s, inv, p.fmt));
+        uint2 packed = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+        const long long o = static_cast<long long>(row) * p.N + static_cast<long long>(g) * 128 + l * 8;
+        *reinterpret_cast<uint2*>(p.out_q + o) = packed;
+        if (l == 0) p.out_s[static_cast<long long>(row) * p.G + g] = s;
+    }
+}
+
+template <int ACT, bool F32IN, bool PERSISTENT>
+__global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int lane = threadIdx.x & 31;
+    const long long warps_per_block = blockDim.x >> 5;
+    const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
+    long long pair = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
+    if (!PERSISTENT) {
+        if (pair < pairs) quant_pair<ACT, F32IN>(p, pair, lane);
+        return;
+    }
+    const long long stride = static_cast<long long>(gridDim.x) * warps_per_block;
+    for (; pair < pairs; pair += stride) quant_pair<ACT, F32IN>(p, pair, lane);
+}
+
+// The unfused first half: BF16 SiLU*mul written to memory, 8 outputs per thread.
+template <int ACT>
+__global__ void __launch_bounds__(256) k_silu_and_mul(const uint16_t* in, int rows, int N,
+                                                      float L, uint16_t* out) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const long long chunks = static_cast<long long>(rows) * (N / 8);
+    for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < chunks;
+         c += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = c / (N / 8);
+        const long long col = (c - row * (N / 8)) * 8;
+        uint4 gw = __ldg(reinterpret_cast<const uint4*>(in + row * 2 * N + col));
+        uint4 uw = __ldg(reinterpret_cast<const uint4*>(in + row * 2 * N + N + col));
+        const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+        const uint32_t uu[4] = {uw.x, uw.y, uw.z, uw.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float a0 = silu_mul_bf16<ACT>(bf16_lo(gg[i]), bf16_lo(uu[i]), L);
+            float a1 = silu_mul_bf16<ACT>(bf16_hi(gg[i]), bf16_hi(uu[i]), L);
+            o[i] = (__float_as_uint(a0) >> 16) | (__float_as_uint(a1) & 0xFFFF0000u);
+        }
+        *reinterpret_cast<uint4*>(out + row * N + col) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <int ACT, bool F32IN>
+int launch_aq(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream) {
+    const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
+    if (pairs == 0) return MOE_OK;
+    const int threads = 256, wpb = threads / 32;
+    long long blocks = (pairs + wpb - 1) / wpb;
+    if (persistent) {
+        long long cap = static_cast<long long>(sm_count()) * 8;
+        if (blocks > cap) blocks = cap;
+    }
+    if (blocks > 0x7FFFFFFFLL) { set_error("act_quant: too many groups"); return MOE_ERR_ARG; }
+    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, pdl);
+    cudaError_t e = persistent ? cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, true>, p)
+                               : cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, false>, p);
+    if (e != cudaSuccess) {
+        set_error("act_quant launch: %s", cudaGetErrorString(e));
+        return MOE_ERR_LAUNCH;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_splits, int in_rows,
+                     int rows, int N, float clamp_limit, moe_scale_fmt fmt,
+                     const int32_t* row_expert, const int32_t* expert_map, int E,
+                     const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
+                     float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream) {
+    if (!in || !out_q || !out_s) { set_error("silu_mul_quant_fp8: null pointer"); return MOE_ERR_ARG; }
+    if (!aligned16(in) || !aligned16(out_q) || (reinterpret_cast<uintptr_t>(out_s) & 3u)) {
+        set_error("silu_mul_quant_fp8: in/out_q must be 16-byte aligned, out_s 4-byte aligned");
+        return MOE_ERR_ARG;
+    }
+    if (rows < 0 || in_rows < 0 || out_rows < 0 || N <= 0 || N % 128) {
+        set_error("silu_mul_quant_fp8: need rows, in_rows, out_rows >= 0 and N a positive multiple of 128 (N=%d)", N);
+        return MOE_ERR_ARG;
+    }
+    if (act != MOE_ACT_IDENTITY && act != MOE_ACT_SILU_MUL && act != MOE_ACT_SILU_MUL_GATE_UPPER) {
+        set_error("silu_mul_quant_fp8: unknown act %d", static_cast<int>(act));
+        return MOE_ERR_ARG;
+    }
+    if (fmt != MOE_SCALE_F32 && fmt != MOE_SCALE_UE8M0) { set_error("silu_mul_quant_fp8: bad fmt"); return MOE_ERR_ARG; }
+    if (in_dtype != MOE_DTYPE_BF16 && in_dtype != MOE_DTYPE_F32) { set_error("silu_mul_quant_fp8: bad in_dtype"); return MOE_ERR_ARG; }
+    if (in_splits < 1 || (in_dtype == MOE_DTYPE_BF16 && in_splits != 1)) {
+        set_error("silu_mul_quant_fp8: in_splits must be 1 for BF16 input and >= 1 for fp32");
+        return MOE_ERR_ARG;
+    }
+    if (!row_map && (rows > in_rows || rows > out_rows)) {
+        set_error("silu_mul_quant_fp8: rows exceeds in_rows or out_rows without a row map");
+        return MOE_ERR_ARG;
+    }
+    if (row_map && row_div < 0) { set_error("silu_mul_quant_fp8: row_div < 0"); return MOE_ERR_ARG; }
+    if (row_expert && E <= 0) { set_error("silu_mul_quant_fp8: row_expert needs E > 0"); return MOE_ERR_ARG; }
+    if (expert_map && !row_expert) { set_error("silu_mul_quant_fp8: expert_map needs row_expert"); return MOE_ERR_ARG; }
+    AQArgs p{};
+    p.in = in;
+    p.W = act == MOE_ACT_IDENTITY ? N : 2 * N;
+    p.split_stride = static_cast<long long>(in_rows) * p.W;
+    p.in_rows = in_rows;
+    p.in_splits = in_splits;
+    p.rows = rows;
+    p.N = N;
+    p.G = N / 128;
+    p.L = clamp_limit;
+    p.fmt = fmt;
+    p.row_expert = row_expert;
+    p.expert_map = expert_map;
+    p.E = E;
+    p.row_map = row_map;
+    p.row_div = row_div;
+    p.out_rows = out_rows;
+    p.out_q = out_q;
+    p.out_s = out_s;
+    p.status = device_status_ptr();
+    bool persistent;
+    if (strategy == MOE_QUANT_PER_GROUP) persistent = false;
+    else if (strategy == MOE_QUANT_PERSISTENT) persistent = true;
+    else persistent = row_expert || row_map || static_cast<long long>(rows) * N >= (1LL << 20);
+    const bool f32 = in_dtype == MOE_DTYPE_F32;
+    switch (act) {
+        case MOE_ACT_IDENTITY:
+            return f32 ? launch_aq<MOE_ACT_IDENTITY, true>(p, persistent, pdl, stream)
+                       : launch_aq<MOE_ACT_IDENTITY, false>(p, persistent, pdl, stream);
+        case MOE_ACT_SILU_MUL:
+            return f32 ? launch_aq<MOE_ACT_SILU_MUL, true>(p, persistent, pdl, stream)
+                       : launch_aq<MOE_ACT_SILU_MUL, false>(p, persistent, pdl, stream);
+        default:
+            return f32 ? launch_aq<MOE_ACT_SILU_MUL_GATE_UPPER, true>(p, persistent, pdl, stream)
+                       : launch_aq<MOE_ACT_SILU_MUL_GATE_UPPER, false>(p, persistent, pdl, stream);
+    }
+}
+
+}  // namespace moe
+
+extern "C" int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, float clamp_limit,
+                                 void* out, cudaStream_t stream) {
+    using namespace moe;
+    clear_error();
+    if (!device_is_sm103()) { set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    if (!in || !out || !aligned16(in) || !aligned16(out)) { set_error("silu_and_mul_bf16: null or misaligned pointer"); return MOE_ERR_ARG; }
+    if (rows < 0 || N <= 0 || N % 8) { set_error("silu_and_mul_bf16: bad shape"); return MOE_ERR_ARG; }
+    if (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SILU_MUL_GATE_UPPER) { set_error("silu_and_mul_bf16: act must be a SiLU*mul"); return MOE_ERR_ARG; }
+    const long long chunks = static_cast<long long>(rows) * (N / 8);
+    if (chunks == 0) return MOE_OK;
+    long long blocks = (chunks + 255) / 256;
+    long long cap = static_cast<long long>(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, false);
+    cudaError_t e = act == MOE_ACT_SILU_MUL
+        ? cudaLaunchKernelEx(&L.cfg, k_silu_and_mul<MOE_ACT_SILU_MUL>, static_cast<const uint16_t*>(in), rows, N, clamp_limit, static_cast<uint16_t*>(out))
+        : cudaLaunchKernelEx(&L.cfg, k_silu_and_mul<MOE_ACT_SILU_MUL_GATE_UPPER>, static_cast<const uint16_t*>(in), rows, N, clamp_limit, static_cast<uint16_t*>(out));
+    if (e != cudaSuccess) { set_error("silu_and_mul_bf16 launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    return MOE_OK;
+}
+
+extern "C" int silu_mul_quant_fp8(moe_act act, const void* in, moe_dtype in_dtype, int in_splits,
+                                  int in_rows, int rows, int N, float clamp_limit,
+                                  moe_scale_fmt fmt, const int32_t* row_expert,
+                                  const int32_t* expert_map, int E, const int32_t* row_map,
+                                  int row_div, int out_rows, uint8_t* out_q, float* out_s,
+                                  moe_quant_strategy strategy, cudaStream_t stream) {
+    moe::clear_error();
+    if (!moe::device_is_sm103()) { moe::set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    return moe::launch_act_quant(act, in, in_dtype, in_splits, in_rows, rows, N, clamp_limit, fmt,
+                                 row_expert, expert_map, E, row_map, row_div, out_rows, out_q,
+                                 out_s, strategy, false, stream);
+}

@@ -1,0 +1,292 @@
+// api.cu -- host side of libmoefp8: error text, the per-device status word, device checks, and
+// the whole-layer entry point that chains the stages on one stream.
+//
+// Layer order (lmdeploy PR #4956 "Perf/pytorch block fp8 moe decode", section "Fused SwiGLU
+// and FP8 quantization": gate/up GEMM -> fused SiLU-and-mul + quant -> down GEMM; lmdeploy PR
+// #4228 "Moe Reduce kernel": weighted top-k sum in its own kernel):
+//   1. moe_route_prepare            topk_ids -> expert-sorted slots, compact blocks, route_slot
+//   2. silu_mul_quant_fp8(IDENTITY) x rows gathered into slot order, per-128 E4M3 + scales
+//   3. grouped GEMM (GATE_UP)       fp32 split-K partials per slot
+//   4. silu_mul_quant_fp8(SILU_MUL) partials summed, BF16 materialised in registers, E4M3
+//   5. grouped GEMM (DOWN)          BF16 rows scattered back to route order
+//   6. moe_reduce                   weighted sum per token
+// Steps 2-6 are launched with programmatic dependent launch so each kernel's prologue overlaps
+// the previous kernel's tail; every kernel waits for its predecessor before reading its output.
+#include "common.cuh"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+namespace moe {
+
+namespace {
+thread_local char g_err[512] = {0};
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+int g_is_sm103[kMaxDevices] = {0};  // 0 unknown, 1 yes, 2 no
+int* g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_dev_mutex;
+
+__device__ int g_status_word;  // one per device that loads the library
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+void init_device(int d) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_is_sm103[d]) return;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, d) != cudaSuccess) { g_is_sm103[d] = 2; return; }
+    g_sm_count[d] = prop.multiProcessorCount;
+    g_is_sm103[d] = (prop.major == 10 && prop.minor == 3) ? 1 : 2;
+    void* p = nullptr;
+    if (g_is_sm103[d] == 1 && cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess)
+        g_status_ptr[d] = static_cast<int*>(p);
+}
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+}
+void clear_error() { g_err[0] = 0; }
+
+bool device_is_sm103() {
+    int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return false;
+    if (!g_is_sm103[d]) init_device(d);
+    return g_is_sm103[d] == 1;
+}
+
+int sm_count() {
+    int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return 1;
+    if (!g_is_sm103[d]) init_device(d);
+    return g_sm_count[d] > 0 ? g_sm_count[d] : 1;
+}
+
+int* device_status_ptr() {
+    int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return nullptr;
+    if (!g_is_sm103[d]) init_device(d);
+    return g_status_ptr[d];
+}
+
+bool ensure_smem(const void* func, int bytes) {
+    // cudaFuncSetAttribute once per (device, kernel, size), outside any stream capture
+    struct Entry { int dev; const void* f; int bytes; };
+    static Entry table[256];
+    static int n = 0;
+    int d = current_device();
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    for (int i = 0; i < n; ++i)
+        if (table[i].dev == d && table[i].f == func && table[i].bytes >= bytes) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return false;
+    for (int i = 0; i < n; ++i)
+        if (table[i].dev == d && table[i].f == func) { table[i].bytes = bytes; return true; }
+    if (n < 256) table[n++] = Entry{d, func, bytes};
+    return true;
+}
+
+// ---------------------------------------------------------------------------------------------
+// layer plan: block_m, split count and workspace layout
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+int forward_block_m(int M, int k, int E_local, int H, int N) {
+    (void)k; (void)E_local; (void)H; (void)N;
+    if (M <= 64) return 16;
+    if (M <= 256) return 32;
+    return 64;
+}
+
+// Expected number of blocks under uniform routing, used only to size the split-K of the
+// gate/up GEMM (any value is correct; the grid reads num_blocks on the device).
+double expected_blocks(int M, int k, int E, int E_local, int bm) {
+    const double p_pick = std::min(1.0, static_cast<double>(k) / std::max(1, E));
+    const double active = E_local * (1.0 - std::pow(1.0 - p_pick, M));
+    const double kept = static_cast<double>(M) * k * E_local / std::max(1, E);
+    return std::max(1.0, std::max(active, kept / bm));
+}
+
+// Split-K of the gate/up GEMM: the smallest split whose round-robin schedule is within a few
+// percent of the best achievable balance over the SMs.
+int gate_up_splits(int M, int k, int E, int E_local, int H, int N, int bm, int sms) {
+    const int KB = H / 128;
+    const double units1 = expected_blocks(M, k, E, E_local, bm) * (2 * N / 128);
+    int best = 1;
+    double best_cost = 1e300;
+    const int smax = std::min(KB, 32);
+    for (int s = 1; s <= smax; ++s) {
+        const double units = units1 * s;
+        const double waves = std::ceil(units / sms);
+        const double per_unit = std::ceil(static_cast<double>(KB) / s) + 0.5;  // + unit overhead
+        const double cost = waves * per_unit;
+        if (cost < best_cost * 0.97) { best_cost = cost; best = s; }
+    }
+    return best;
+}
+
+struct Plan {
+    int bm, B_cap, slots, R, splits;
+    size_t off_sorted, off_bexp, off_nb, off_cnt, off_off, off_rslot, off_rws, off_xq, off_xs,
+        off_gu, off_aq, off_as, off_z, total;
+};
+
+Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int sms) {
+    Plan P{};
+    P.bm = block_m > 0 ? block_m : forward_block_m(M, k, E_local, H, N);
+    P.R = M * k;
+    P.B_cap = (P.R + P.bm - 1) / P.bm + std::min(E_local, P.R);
+    P.slots = P.B_cap * P.bm;
+    P.splits = gate_up_splits(M, k, E, E_local, H, N, P.bm, sms);
+    size_t o = 0;
+    auto take = [&o](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
+    P.off_sorted = take(sizeof(int32_t) * P.slots);
+    P.off_bexp = take(sizeof(int32_t) * P.B_cap);
+    P.off_nb = take(sizeof(int32_t));
+    P.off_cnt = take(sizeof(int32_t) * E_local);
+    P.off_off = take(sizeof(int32_t) * (E_local + 1));
+    P.off_rslot = take(sizeof(int32_t) * P.R);
+    P.off_rws = take(route_workspace_bytes(P.R, E_local, P.bm));
+    P.off_xq = take(static_cast<size_t>(P.slots) * H);
+    P.off_xs = take(sizeof(float) * static_cast<size_t>(P.slots) * (H / 128));
+    P.off_gu = take(sizeof(float) * static_cast<size_t>(P.splits) * P.slots * 2 * N);
+    P.off_aq = take(static_cast<size_t>(P.slots) * N);
+    P.off_as = take(sizeof(float) * static_cast<size_t>(P.slots) * (N / 128));
+    P.off_z = take(sizeof(uint16_t) * static_cast<size_t>(P.R) * H);
+    P.total = o;
+    return P;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" const char* moe_last_error_string(void) { return g_err; }
+
+extern "C" int moe_device_supported(void) { return device_is_sm103() ? 1 : 0; }
+
+extern "C" int moe_get_device_status(int* status, int reset) {
+    clear_error();
+    if (!status) { set_error("moe_get_device_status: null status"); return MOE_ERR_ARG; }
+    *status = 0;
+    int* p = device_status_ptr();
+    if (!p) { set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    cudaError_t e = cudaMemcpy(status, p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && reset) e = cudaMemset(p, 0, sizeof(int));
+    if (e != cudaSuccess) { set_error("moe_get_device_status: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    return MOE_OK;
+}
+
+extern "C" int moe_forward_block_m(int M, int k, int E_local, int H, int N) {
+    return forward_block_m(M, k, E_local, H, N);
+}
+
+extern "C" int moe_blockfp8_plan(int M, int k, int E, int E_local, int H, int N, int block_m,
+                                 int* out_block_m, int* out_B_cap, int* out_splits) {
+    clear_error();
+    if (M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0 || H % 128 || N % 128 ||
+        (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)) {
+        set_error("moe_blockfp8_plan: bad sizes");
+        return MOE_ERR_ARG;
+    }
+    const Plan P = make_plan(M, k, E, E_local, H, N, block_m, sm_count());
+    if (out_block_m) *out_block_m = P.bm;
+    if (out_B_cap) *out_B_cap = P.B_cap;
+    if (out_splits) *out_splits = P.splits;
+    return MOE_OK;
+}
+
+extern "C" size_t moe_blockfp8_workspace_bytes(int M, int k, int E, int E_local, int H, int N,
+                                               int block_m) {
+    if (M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0) return 0;
+    return make_plan(M, k, E, E_local, H, N, block_m, sm_count()).total;
+}
+
+extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, const float* topk_w,
+                                    int M, int k, int E, const int32_t* expert_map, int E_local,
+                                    int H, int N, const uint8_t* wgu_q, const float* wgu_s,
+                                    const uint8_t* wd_q, const float* wd_s, moe_act act,
+                                    float clamp_limit, moe_scale_fmt act_fmt, int block_m,
+                                    void* out, void* workspace, size_t ws_bytes,
+                                    cudaStream_t stream) {
+    clear_error();
+    if (!device_is_sm103()) { set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    if (!wgu_q || !wgu_s || !wd_q || !wd_s || (M > 0 && (!x || !topk_ids || !topk_w || !out))) {
+        set_error("moe_blockfp8_forward: null pointer");
+        return MOE_ERR_ARG;
+    }
+    if (M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0 || H % 128 || N % 128) {
+        set_error("moe_blockfp8_forward: need M >= 0, k, E, E_local > 0 and H, N multiples of 128");
+        return MOE_ERR_ARG;
+    }
+    if (k > E) { set_error("moe_blockfp8_forward: k > E"); return MOE_ERR_ARG; }
+    if (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SILU_MUL_GATE_UPPER) {
+        set_error("moe_blockfp8_forward: act must be SILU_MUL or SILU_MUL_GATE_UPPER");
+        return MOE_ERR_ARG;
+    }
+    if (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) {
+        set_error("moe_blockfp8_forward: block_m must be 0 (auto), 16, 32, 64 or 128");
+        return MOE_ERR_ARG;
+    }
+    if (!expert_map && E_local != E) {
+        set_error("moe_blockfp8_forward: without an expert map E_local must equal E");
+        return MOE_ERR_EXPERT_SLICE;
+    }
+    if (static_cast<long long>(M) * k > (1LL << 24)) { set_error("moe_blockfp8_forward: too many routes"); return MOE_ERR_ARG; }
+    const Plan P = make_plan(M, k, E, E_local, H, N, block_m, sm_count());
+    if (!workspace || ws_bytes < P.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+        set_error("moe_blockfp8_forward: need %zu bytes of 256-byte aligned workspace (got %zu)", P.total, ws_bytes);
+        return MOE_ERR_WORKSPACE;
+    }
+    if (M == 0) return MOE_OK;
+    char* ws = static_cast<char*>(workspace);
+    int32_t* sorted_idx = reinterpret_cast<int32_t*>(ws + P.off_sorted);
+    int32_t* block_expert = reinterpret_cast<int32_t*>(ws + P.off_bexp);
+    int32_t* num_blocks = reinterpret_cast<int32_t*>(ws + P.off_nb);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws + P.off_cnt);
+    int32_t* offsets = reinterpret_cast<int32_t*>(ws + P.off_off);
+    int32_t* route_slot = reinterpret_cast<int32_t*>(ws + P.off_rslot);
+    uint8_t* xq = reinterpret_cast<uint8_t*>(ws + P.off_xq);
+    float* xs = reinterpret_cast<float*>(ws + P.off_xs);
+    float* gu = reinterpret_cast<float*>(ws + P.off_gu);
+    uint8_t* aq = reinterpret_cast<uint8_t*>(ws + P.off_aq);
+    float* as = reinterpret_cast<float*>(ws + P.off_as);
+    void* z = ws + P.off_z;
+    const size_t rws_bytes = P.off_xq - P.off_rws;
+
+    int rc = launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, P.bm, MOE_ROUTE_AUTO,
+                                  sorted_idx, block_expert, num_blocks, counts, offsets,
+                                  route_slot, ws + P.off_rws, rws_bytes, false, stream);
+    if (rc) return rc;
+    rc = launch_act_quant(MOE_ACT_IDENTITY, x, MOE_DTYPE_BF16, 1, M, P.R, H, INFINITY, act_fmt,
+                          nullptr, nullptr, 0, route_slot, k, P.slots, xq, xs,
+                          MOE_QUANT_PERSISTENT, true, stream);
+    if (rc) return rc;
+    rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
+                             sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
+                             MOE_DTYPE_F32, P.slots, P.splits, true, stream);
+    if (rc) return rc;
+    rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
+                          nullptr, nullptr, 0, route_slot, 0, P.slots, aq, as,
+                          MOE_QUANT_PERSISTENT, true, stream);
+    if (rc) return rc;
+    rc = launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, sorted_idx,
+                             block_expert, num_blocks, P.B_cap, P.bm, z, MOE_DTYPE_BF16, P.R, 1,
+                             true, stream);
+    if (rc) return rc;
+    return launch_moe_reduce(z, topk_w, topk_ids, expert_map, M, k, E, H, out, true, stream);
+}

@@ -1,0 +1,408 @@
+// grouped_gemm.cu -- block-FP8 grouped GEMM over the active expert blocks, on the fifth-
+// generation tensor cores (tcgen05, accumulators in tensor memory) with TMA-fed operands.
+//
+// Method: lmdeploy PR #4956 "Perf/pytorch block fp8 moe decode", section "Active-expert block
+// scheduling" (GEMM programs only for expert blocks that received tokens); lmdeploy PR #4857
+// "optimize compact blocked FP8 MoE and route preparation", section "Changes" (compact blocks;
+// transposed MMA for small block_m); vLLM PR #53875, "Purpose" (W8A8 block shape [128, 128]:
+// one fp32 scale per 128x128 weight block and per token per 128 activation columns).
+//
+// Orientation (transposed / swap-AB): the MMA's M side is 128 weight rows (output features) of
+// one expert and its N side is the block's block_m tokens, so a decode block with one or two
+// real tokens still runs full-height MMAs and the weight tile is the A operand.  One work unit
+// is (block b, 128-row output tile, K split); a persistent grid of one CTA per SM walks the
+// units round-robin.  num_blocks is read on the device, so no work exists for inactive experts.
+//
+// Per CTA (192 threads, one CTA per SM):
+//   warp 0  lane 0: TMA producer.  Per 128-wide K-block it loads the 128x128 E4M3 weight tile
+//                   (16 KB) and the block_m x 128 activation tile into one pipeline stage,
+//                   both with 128-byte swizzle, completion counted on the stage's mbarrier.
+//   warp 1  lane 0: MMA issuer.  Per K-block: 4 tcgen05.mma (K = 32 each) into a fresh fp32
+//                   accumulator buffer in tensor memory, then tcgen05.commit frees the smem
+//                   stage and signals the accumulator buffer.
+//   warps 2-5     : epilogue / scale promotion.  Per K-block each thread (one weight row) reads
+//                   its block_m partial sums with tcgen05.ld, frees the buffer, and accumulates
+//                   partial * a_s[token, kb] * w_s[expert, tile, kb] in fp32 registers; at the
+//                   end of the unit it writes BF16 or fp32 (split-K partials) outputs.
+// Block scales differ per K-block, so every K-block gets its own accumulator buffer; 4-8
+// buffers let the MMA run ahead of the promotion.  Every wait is bounded (see mbar_wait).
+#include "common.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+struct GemmArgs {
+    const float* a_s;
+    int a_rows, K, KB;
+    const float* w_s;
+    int E_local, N_out, NT;
+    const int32_t* sorted_idx;
+    const int32_t* block_expert;
+    const int32_t* num_blocks;
+    int B_cap;
+    void* out;
+    int out_f32, out_rows, splits, scatter;
+    int* status;
+};
+
+template <int BM>
+struct Cfg {
+    static constexpr int kWBytes = 128 * 128;
+    static constexpr int kABytes = BM * 128;
+    static constexpr int kStage = kWBytes + kABytes;  // multiple of 1024
+    static constexpr int kStages = BM <= 16 ? 10 : BM <= 32 ? 9 : BM <= 64 ? 8 : 6;
+    static constexpr int kBufs = BM <= 64 ? 8 : 4;     // tensor-memory accumulator buffers
+    static constexpr int kCols = kBufs * BM <= 32 ? 32 : kBufs * BM <= 64 ? 64
+                               : kBufs * BM <= 128 ? 128 : kBufs * BM <= 256 ? 256 : 512;
+    static constexpr int kBarBytes = 1024;
+    static constexpr int kSmem = kStages * kStage + kBarBytes + 1024;  // + alignment slack
+    static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
+    static_assert(kBufs * BM <= 512, "tensor memory holds 512 fp32 columns");
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+__device__ __forceinline__ void decode_unit(const GemmArgs& p, long long u, int& b, int& nt,
+                                            int& kb0, int& kb1) {
+    const int sp = static_cast<int>(u % p.splits);
+    const long long bt = u / p.splits;
+    nt = static_cast<int>(bt % p.NT);
+    b = static_cast<int>(bt / p.NT);
+    kb0 = static_cast<int>((static_cast<long long>(sp) * p.KB) / p.splits);
+    kb1 = static_cast<int>((static_cast<long long>(sp + 1) * p.KB) / p.splits);
+}
+
+__device__ __forceinline__ int unit_expert(const GemmArgs& p, int b) {
+    const int e = __ldg(p.block_expert + b);
+    return (e >= 0 && e < p.E_local) ? e : -1;
+}
+
+template <int BM>
+__global__ void __launch_bounds__(192, 1)
+    k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_a, GemmArgs p) {
+    using C = Cfg<BM>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* tfull = empty + C::kStages;
+    uint64_t* tempty = tfull + C::kBufs;
+    uint64_t* mma_done = tempty + C::kBufs;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
+        for (int i = 0; i < C::kBufs; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_a);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(tmem_slot, C::kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // everything below reads what earlier kernels on the stream wrote
+    grid_dep_wait();
+    grid_dep_launch();
+    int nblk = __ldg(p.num_blocks);
+    nblk = max(0, min(nblk, p.B_cap));
+    const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_a = l2_policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            long long issued = 0;
+            for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+                int b, nt, kb0, kb1;
+                decode_unit(p, u, b, nt, kb0, kb1);
+                const int e = unit_expert(p, b);
+                if (e < 0) continue;
+                const int wrow = e * p.N_out + nt * 128;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, p.status)) goto producer_done;
+                    uint8_t* st = smem + s * C::kStage;
+                    mbar_arrive_expect_tx(full + s, C::kStage);
+                    tma_load_2d(st, &tmap_w, full + s, kb * 128, wrow, pol_w);
+                    tma_load_2d(st + C::kWBytes, &tmap_a, full + s, kb * 128, b * BM, pol_a);
+                    ++issued;
+                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                }
+            }
+        producer_done:
+            if (*abort_flag) {
+                // never leave a TMA write in flight: wait for the last load of every stage
+                for (int i = 0; i < C::kStages; ++i) {
+                    if (issued <= i) break;
+                    const long long n_i = (issued - 1 - i) / C::kStages + 1;
+                    volatile int no_abort = 0;
+                    mbar_wait(full + i, static_cast<uint32_t>((n_i - 1) & 1), &no_abort, p.status);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f8_f32(128, BM);
+            int s = 0, tb = 0;
+            uint32_t ph = 0, tph = 0;
+            for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+                int b, nt, kb0, kb1;
+                decode_unit(p, u, b, nt, kb0, kb1);
+                if (unit_expert(p, b) < 0) continue;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(tempty + tb, tph ^ 1u, abort_flag, p.status)) goto mma_out;
+                    if (!mbar_wait(full + s, ph, abort_flag, p.status)) goto mma_out;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(tb * BM);
+                    const uint32_t wa = smem_u32(smem + s * C::kStage);
+                    const uint32_t aa = wa + C::kWBytes;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f8(d, smem_desc_sw128(wa + ks * 32), smem_desc_sw128(aa + ks * 32), idesc,
+                               ks > 0 ? 1u : 0u);
+                    mma_commit(empty + s);
+                    mma_commit(tfull + tb);
+                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                    if (++tb == C::kBufs) { tb = 0; tph ^= 1u; }
+                }
+            }
+        mma_out:
+            // all issued MMAs complete before tensor memory is released
+            mma_commit(mma_done);
+            volatile int no_abort = 0;
+            mbar_wait(mma_done, 0, &no_abort, p.status);
+        }
+    } else {
+        // epilogue: warp (2..5) & 3 selects the 32-lane quarter of tensor memory it may read
+        const int q = warp & 3;
+        const int r_in_tile = q * 32 + lane;
+        int tb = 0;
+        uint32_t tph = 0;
+        for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+            int b, nt, kb0, kb1;
+            decode_unit(p, u, b, nt, kb0, kb1);
+            const int e = unit_expert(p, b);
+            if (e < 0) continue;
+            float acc[BM];
+#pragma unroll
+            for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
+            const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                const float sw = __ldg(wsc + kb);
+                constexpr int kSa = BM < 32 ? 1 : BM / 32;
+                float sa[kSa];
+#pragma unroll
+                for (int i = 0; i < kSa; ++i) {
+                    const int j = i * 32 + lane;
+                    sa[i] = j < BM ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + kb) : 0.0f;
+                }
+                bool ok = mbar_wait(tfull + tb, tph, abort_flag, p.status);
+                if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < BM / 16; ++c) {
+                    float v[16];
+                    tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                  static_cast<uint32_t>(tb * BM + c * 16),
+                              v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int j = c * 16 + i;
+                        const float sj = __shfl_sync(0xFFFFFFFFu, sa[j / 32], j % 32);
+                        acc[j] = __fmaf_rn(v[i], __fmul_rn(sj, sw), acc[j]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(tempty + tb);
+                if (++tb == C::kBufs) { tb = 0; tph ^= 1u; }
+            }
+            {
+                const int n = nt * 128 + r_in_tile;
+                const int sp = static_cast<int>(u % p.splits);
+#pragma unroll
+                for (int j = 0; j < BM; ++j) {
+                    const int slot = b * BM + j;
+                    const int r = __ldg(p.sorted_idx + slot);
+                    if (r < 0) continue;
+                    const int row = p.scatter ? r : slot;
+                    if (row >= p.out_rows) {
+                        if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                        continue;
+                    }
+                    if (p.out_f32) {
+                        float* o = static_cast<float*>(p.out);
+                        o[(static_cast<long long>(sp) * p.out_rows + row) * p.N_out + n] = acc[j];
+                    } else {
+                        uint16_t* o = static_cast<uint16_t*>(p.out);
+                        o[static_cast<long long>(row) * p.N_out + n] =
+                            static_cast<uint16_t>(f32_to_bf16_bits(acc[j]));
+                    }
+                }
+            }
+        }
+    epi_done:;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, C::kCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// 2-D map over a row-major [rows, K] E4M3 matrix, box 128 columns x box_rows rows, 128-byte
+// swizzle (the layout the MMA descriptors expect).
+bool make_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BM>
+int launch_bm(const CUtensorMap& tw, const CUtensorMap& ta, const GemmArgs& p, long long max_units,
+              bool pdl, cudaStream_t stream) {
+    using C = Cfg<BM>;
+    if (!ensure_smem(reinterpret_cast<const void*>(k_grouped_gemm<BM>), C::kSmem)) {
+        set_error("grouped_gemm: shared-memory limit %d refused", C::kSmem);
+        return MOE_ERR_LAUNCH;
+    }
+    long long grid = std::min<long long>(sm_count(), max_units);
+    if (grid <= 0) return MOE_OK;
+    Launch L(dim3(static_cast<unsigned>(grid)), dim3(192), C::kSmem, stream, pdl);
+    cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_grouped_gemm<BM>, tw, ta, p);
+    if (e != cudaSuccess) { set_error("grouped_gemm launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    return MOE_OK;
+}
+
+}  // namespace
+
+int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows, int K,
+                        const uint8_t* w_q, const float* w_s, int E_local, int N_out,
+                        const int32_t* sorted_idx, const int32_t* block_expert,
+                        const int32_t* num_blocks, int B_cap, int block_m, void* out,
+                        moe_dtype out_dtype, int out_rows, int splits, bool pdl,
+                        cudaStream_t stream) {
+    if (proj != MOE_PROJ_GATE_UP && proj != MOE_PROJ_DOWN) { set_error("grouped_gemm: bad proj"); return MOE_ERR_ARG; }
+    if (!a_q || !a_s || !w_q || !w_s || !sorted_idx || !block_expert || !num_blocks || !out) {
+        set_error("grouped_gemm: null pointer");
+        return MOE_ERR_ARG;
+    }
+    if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(out) || !aligned16(a_s) || !aligned16(w_s)) {
+        set_error("grouped_gemm: pointers must be 16-byte aligned");
+        return MOE_ERR_ARG;
+    }
+    if (K <= 0 || K % 128 || N_out <= 0 || N_out % 128 || E_local <= 0 || B_cap < 0 || out_rows < 0) {
+        set_error("grouped_gemm: K and N_out must be positive multiples of 128 (K=%d N_out=%d)", K, N_out);
+        return MOE_ERR_ARG;
+    }
+    if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) {
+        set_error("grouped_gemm: block_m must be 16, 32, 64 or 128");
+        return MOE_ERR_ARG;
+    }
+    const int KB = K / 128;
+    if (out_dtype == MOE_DTYPE_BF16 ? splits != 1 : (splits < 1 || splits > KB)) {
+        set_error("grouped_gemm: splits must be 1 for BF16 output and in [1, K/128] for fp32");
+        return MOE_ERR_ARG;
+    }
+    if (static_cast<long long>(a_rows) < static_cast<long long>(B_cap) * block_m) {
+        set_error("grouped_gemm: a_rows (%d) < B_cap*block_m", a_rows);
+        return MOE_ERR_ARG;
+    }
+    if (proj == MOE_PROJ_GATE_UP && static_cast<long long>(out_rows) < static_cast<long long>(B_cap) * block_m) {
+        set_error("grouped_gemm: GATE_UP writes slot rows; out_rows must be >= B_cap*block_m");
+        return MOE_ERR_ARG;
+    }
+    if (B_cap == 0) return MOE_OK;
+    if (static_cast<long long>(E_local) * N_out > 0x7FFFFFFFLL) { set_error("grouped_gemm: E_local*N_out too large"); return MOE_ERR_ARG; }
+    CUtensorMap tw, ta;
+    if (!make_map(&tw, w_q, static_cast<long long>(E_local) * N_out, K, 128) ||
+        !make_map(&ta, a_q, a_rows, K, block_m)) {
+        set_error("grouped_gemm: tensor-map encode failed (driver entry point missing or bad layout)");
+        return MOE_ERR_LAUNCH;
+    }
+    GemmArgs p{};
+    p.a_s = a_s;
+    p.a_rows = a_rows;
+    p.K = K;
+    p.KB = KB;
+    p.w_s = w_s;
+    p.E_local = E_local;
+    p.N_out = N_out;
+    p.NT = N_out / 128;
+    p.sorted_idx = sorted_idx;
+    p.block_expert = block_expert;
+    p.num_blocks = num_blocks;
+    p.B_cap = B_cap;
+    p.out = out;
+    p.out_f32 = out_dtype == MOE_DTYPE_F32;
+    p.out_rows = out_rows;
+    p.splits = splits;
+    p.scatter = proj == MOE_PROJ_DOWN;
+    p.status = device_status_ptr();
+    const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
+    switch (block_m) {
+        case 16: return launch_bm<16>(tw, ta, p, max_units, pdl, stream);
+        case 32: return launch_bm<32>(tw, ta, p, max_units, pdl, stream);
+        case 64: return launch_bm<64>(tw, ta, p, max_units, pdl, stream);
+        default: return launch_bm<128>(tw, ta, p, max_units, pdl, stream);
+    }
+}
+
+}  // namespace moe
+
+extern "C" int moe_blockfp8_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s,
+                                         int a_rows, int K, const uint8_t* w_q, const float* w_s,
+                                         int E_local, int N_out, const int32_t* sorted_idx,
+                                         const int32_t* block_expert, const int32_t* num_blocks,
+                                         int B_cap, int block_m, void* out, moe_dtype out_dtype,
+                                         int out_rows, int splits, cudaStream_t stream) {
+    moe::clear_error();
+    if (!moe::device_is_sm103()) { moe::set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    return moe::launch_grouped_gemm(proj, a_q, a_s, a_rows, K, w_q, w_s, E_local, N_out, sorted_idx,
+                                    block_expert, num_blocks, B_cap, block_m, out, out_dtype,
+                                    out_rows, splits, false, stream);
+}

@@ -1,0 +1,449 @@
+// route_prepare.cu -- route preparation: stable counting sort of the top-k routes by local
+// expert, block_m-padded compact blocks for the experts that received routes.
+//
+// Method: lmdeploy PR #4857 "optimize compact blocked FP8 MoE and route preparation", section
+// "Changes": one CTA when routes and experts are at most 2,048 (few graph nodes), a scalable
+// parallel path otherwise; outputs are the sorted route indices and the compact blocks.  The
+// review on that page asks that the local-expert slice and block_m be checked before launch.
+//
+// Single CTA (1024 threads = 32 warps).  Every route's local expert goes to shared memory.
+// Warp w owns a contiguous chunk of routes and counts it into its own row of a per-warp
+// histogram [32][E_local] (uint16): 32 routes at a time, __match_any_sync groups lanes with the
+// same expert and the group's lowest lane adds the group size -- no atomics, so the result is
+// deterministic.  A column scan over the 32 rows turns the histogram into per-warp starting
+// ranks; a block scan over the block_m-padded expert totals gives each expert's first slot.
+// The scatter repeats the warp walk: slot = expert start + warp rank + rank inside the 32-route
+// group, so the order inside an expert is the route order (stable).
+//
+// Multi CTA.  Kernel 1: each CTA histograms one chunk of routes (shared-memory atomics; counts
+// only) into the workspace; the CTA that finishes last (atomic ticket, no waiting) scans the
+// chunk histograms per expert, scans the padded totals and writes counts, offsets, the block
+// table and the -1 pads.  Kernel 2: each CTA runs the single-CTA warp walk on its own chunk,
+// offset by its chunk prefix.  Neither kernel ever waits on another CTA.
+#include "common.cuh"
+
+#include <algorithm>
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kSingleWarps = 32;
+constexpr int kSingleMaxRoutes = 8192;
+constexpr int kSingleMaxExperts = 2048;
+constexpr int kMaxExperts = 4096;
+constexpr size_t kMultiHistBytes = 96 * 1024;  // per-warp histogram budget of a scatter CTA
+
+struct RouteArgs {
+    const int32_t* ids;
+    int R, E;
+    const int32_t* map;
+    int E_loc, bm, B_cap;
+    int32_t* sorted_idx;
+    int32_t* block_expert;
+    int32_t* num_blocks;
+    int32_t* count;
+    int32_t* offset;   // nullable
+    int32_t* route_slot;  // nullable: slot of each route, -1 when dropped
+    int* status;
+    // multi-CTA workspace
+    int32_t* ws_cnt;   // [nchunks][E_loc]: chunk histograms, then chunk prefixes
+    int32_t* ws_off;   // [E_loc + 1]: first slot of each expert
+    unsigned* ws_done; // ticket counter
+    int chunk, nchunks, warps;
+};
+
+__device__ __forceinline__ int local_of(const RouteArgs& p, int r) {
+    int id = __ldg(p.ids + r);
+    if (id < 0 || id >= p.E) return -1;
+    int e = p.map ? __ldg(p.map + id) : id;
+    if (e < -1 || e >= p.E_loc) {
+        if (p.status) atomicOr(p.status, MOE_DEV_BAD_EXPERT_MAP);
+        return -1;
+    }
+    return e;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// In-place exclusive scan of data[0..n) by the whole block; returns the total.  `tmp` holds at
+// least 33 ints.
+__device__ int block_exclusive_scan(int* data, int n, int* tmp) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + nt - 1) / nt;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += data[i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) tmp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nt >> 5;
+        int v = lane < nw ? tmp[lane] : 0;
+        int s = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int u = __shfl_up_sync(kFull, s, o);
+            if (lane >= o) s += u;
+        }
+        if (lane < nw) tmp[lane] = s - v;  // exclusive warp prefix
+        if (lane == 31) tmp[32] = s;       // total
+    }
+    __syncthreads();
+    int run = tmp[warp] + incl - local;
+    for (int i = lo; i < hi; ++i) {
+        int v = data[i];
+        data[i] = run;
+        run += v;
+    }
+    int total = tmp[32];
+    __syncthreads();
+    return total;
+}
+
+// Per-warp histogram of the routes [w*per_warp, min(n, (w+1)*per_warp)) of `loc`.
+__device__ __forceinline__ void warp_histogram(const int* loc, int n, int per_warp,
+                                               uint16_t* row) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int lo = w * per_warp, hi = min(n, lo + per_warp);
+    for (int base = lo; base < hi; base += 32) {
+        const int r = base + lane;
+        const int e = r < hi ? loc[r] : -1;
+        const unsigned m = __match_any_sync(kFull, e);
+        if (e >= 0 && lane == __ffs(m) - 1) row[e] = static_cast<uint16_t>(row[e] + __popc(m));
+        __syncwarp();
+    }
+}
+
+// Turns the per-warp histograms [nw][E_loc] into exclusive per-warp starting ranks; stores the
+// expert totals in `tot` when it is not null.
+__device__ __forceinline__ void column_scan(uint16_t* wcnt, int nw, int E_loc, int* tot) {
+    for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < nw; ++w) {
+            int c = wcnt[w * E_loc + e];
+            wcnt[w * E_loc + e] = static_cast<uint16_t>(run);
+            run += c;
+        }
+        if (tot) tot[e] = run;
+    }
+}
+
+// Stable scatter of this CTA's routes (local ids in `loc`, global route id = first + i).
+// slot = start[e] + chunk_base(e) + warp rank + rank in the 32-group.
+__device__ __forceinline__ void warp_scatter(const RouteArgs& p, const int* loc, int n, int first,
+                                             int per_warp, uint16_t* row, const int* start,
+                                             const int32_t* chunk_base) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int lo = w * per_warp, hi = min(n, lo + per_warp);
+    for (int base = lo; base < hi; base += 32) {
+        const int r = base + lane;
+        const int e = r < hi ? loc[r] : -1;
+        const unsigned m = __match_any_sync(kFull, e);
+        if (e >= 0) {
+            int slot = start[e] + row[e] + __popc(m & lanemask_lt());
+            if (chunk_base) slot += chunk_base[e];
+            p.sorted_idx[slot] = first + r;
+            if (p.route_slot) p.route_slot[first + r] = slot;
+        } else if (r < hi && p.route_slot) {
+            p.route_slot[first + r] = -1;
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(m) - 1) row[e] = static_cast<uint16_t>(row[e] + __popc(m));
+        __syncwarp();
+    }
+}
+
+// Writes counts, offsets, num_blocks, the block table and every -1 pad from the expert totals
+// `tot` and the padded starts `start` (start[E_loc] = padded total).
+__device__ void write_metadata(const RouteArgs& p, const int* tot, const int* start) {
+    const int nb = start[p.E_loc] / p.bm;
+    for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x) {
+        p.count[e] = tot[e];
+        if (p.offset) p.offset[e] = start[e];
+        for (int b = start[e] / p.bm; b < start[e + 1] / p.bm; ++b) p.block_expert[b] = e;
+        for (int s = start[e] + tot[e]; s < start[e + 1]; ++s) p.sorted_idx[s] = -1;
+    }
+    for (int b = nb + threadIdx.x; b < p.B_cap; b += blockDim.x) p.block_expert[b] = -1;
+    for (long long s = static_cast<long long>(nb) * p.bm + threadIdx.x;
+         s < static_cast<long long>(p.B_cap) * p.bm; s += blockDim.x)
+        p.sorted_idx[s] = -1;
+    if (threadIdx.x == 0) {
+        *p.num_blocks = nb;
+        if (p.offset) p.offset[p.E_loc] = start[p.E_loc];
+    }
+}
+
+// shared memory of the single-CTA kernel: loc[R] | start[E_loc+1] | tot[E_loc] | tmp[33] | wcnt
+size_t single_smem_bytes(int R, int E_loc) {
+    size_t ints = static_cast<size_t>(R) + (E_loc + 1) + E_loc + 33;
+    ints = (ints + 3) & ~static_cast<size_t>(3);
+    return ints * 4 + static_cast<size_t>(kSingleWarps) * E_loc * 2;
+}
+
+__global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
+    extern __shared__ __align__(16) int sm[];
+    int* loc = sm;
+    int* start = loc + p.R;
+    int* tot = start + p.E_loc + 1;
+    int* tmp = tot + p.E_loc;
+    size_t ints = static_cast<size_t>(p.R) + (p.E_loc + 1) + p.E_loc + 33;
+    ints = (ints + 3) & ~static_cast<size_t>(3);
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(sm + ints);
+    grid_dep_wait();
+    grid_dep_launch();
+    for (int r = threadIdx.x; r < p.R; r += blockDim.x) loc[r] = local_of(p, r);
+    for (int i = threadIdx.x; i < kSingleWarps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const int per_warp = (p.R + kSingleWarps - 1) / kSingleWarps;
+    uint16_t* row = wcnt + (threadIdx.x >> 5) * p.E_loc;
+    warp_histogram(loc, p.R, per_warp, row);
+    __syncthreads();
+    column_scan(wcnt, kSingleWarps, p.E_loc, tot);
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x)
+        start[e] = (tot[e] + p.bm - 1) / p.bm * p.bm;
+    __syncthreads();
+    const int total = block_exclusive_scan(start, p.E_loc, tmp);
+    if (threadIdx.x == 0) start[p.E_loc] = total;
+    __syncthreads();
+    write_metadata(p, tot, start);
+    warp_scatter(p, loc, p.R, 0, per_warp, row, start, nullptr);
+}
+
+// Multi-CTA kernel 1: chunk histograms; the last CTA to finish builds the metadata.
+__global__ void __launch_bounds__(1024) k_route_count(RouteArgs p) {
+    extern __shared__ __align__(16) int sm[];
+    int* hist = sm;                         // [E_loc]
+    int* start = hist + p.E_loc;            // [E_loc + 1]
+    int* tmp = start + p.E_loc + 1;         // [33]
+    __shared__ int is_last;
+    grid_dep_wait();
+    grid_dep_launch();
+    const int c = blockIdx.x;
+    const int lo = c * p.chunk, hi = min(p.R, lo + p.chunk);
+    for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    for (int r = lo + threadIdx.x; r < hi; r += blockDim.x) {
+        int e = local_of(p, r);
+        if (e >= 0) atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x)
+        p.ws_cnt[static_cast<long long>(c) * p.E_loc + e] = hist[e];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(p.ws_done, 1u) == static_cast<unsigned>(p.nchunks - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // per expert: exclusive prefix over chunks (in place) and the total
+    int* tot = hist;
+    for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x) {
+        int run = 0;
+        for (int cc = 0; cc < p.nchunks; ++cc) {
+            int32_t* q = p.ws_cnt + static_cast<long long>(cc) * p.E_loc + e;
+            int v = __ldcg(q);
+            *q = run;
+            run += v;
+        }
+        tot[e] = run;
+        start[e] = (run + p.bm - 1) / p.bm * p.bm;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan(start, p.E_loc, tmp);
+    if (threadIdx.x == 0) start[p.E_loc] = total;
+    __syncthreads();
+    for (int e = threadIdx.x; e <= p.E_loc; e += blockDim.x) p.ws_off[e] = start[e];
+    write_metadata(p, tot, start);
+    if (threadIdx.x == 0) *p.ws_done = 0u;  // ready for the next call
+}
+
+// Multi-CTA kernel 2: the stable warp walk over one chunk.
+__global__ void __launch_bounds__(1024) k_route_scatter(RouteArgs p) {
+    extern __shared__ __align__(16) int sm[];
+    int* loc = sm;                                        // [chunk]
+    int* start = loc + p.chunk;                           // [E_loc]
+    size_t ints = static_cast<size_t>(p.chunk) + p.E_loc;
+    ints = (ints + 3) & ~static_cast<size_t>(3);
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(sm + ints);  // [warps][E_loc]
+    grid_dep_wait();
+    grid_dep_launch();
+    const int c = blockIdx.x;
+    const int first = c * p.chunk;
+    const int n = min(p.R - first, p.chunk);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) loc[i] = local_of(p, first + i);
+    for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x) start[e] = __ldcg(p.ws_off + e);
+    for (int i = threadIdx.x; i < p.warps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    uint16_t* row = wcnt + (threadIdx.x >> 5) * p.E_loc;
+    warp_histogram(loc, n, 32, row);
+    __syncthreads();
+    column_scan(wcnt, p.warps, p.E_loc, nullptr);
+    __syncthreads();
+    warp_scatter(p, loc, n, first, 32, row, start, p.ws_cnt + static_cast<long long>(c) * p.E_loc);
+}
+
+int multi_warps(int E_loc) {
+    int w = static_cast<int>(kMultiHistBytes / (static_cast<size_t>(E_loc) * 2));
+    return std::max(1, std::min(32, w));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+bool route_single_cta(int R, int E_local, moe_route_path path) {
+    if (path == MOE_ROUTE_SINGLE_CTA) return true;
+    if (path == MOE_ROUTE_MULTI_CTA) return false;
+    return R <= 2048 && E_local <= 2048;
+}
+
+size_t route_workspace_bytes(int R, int E_local, int block_m) {
+    (void)block_m;
+    const int chunk = multi_warps(E_local) * 32;
+    const long long nchunks = std::max(1, (R + chunk - 1) / chunk);
+    return align256(static_cast<size_t>(nchunks) * E_local * 4) +
+           align256(static_cast<size_t>(E_local + 1) * 4) + 256;
+}
+
+int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int32_t* expert_map,
+                         int E_local, int block_m, moe_route_path path, int32_t* sorted_idx,
+                         int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
+                         int32_t* expert_offset, int32_t* route_slot, void* workspace,
+                         size_t ws_bytes, bool pdl, cudaStream_t stream) {
+    if (M < 0 || k <= 0 || E <= 0 || E_local <= 0) {
+        set_error("moe_route_prepare: need M >= 0, k > 0, E > 0, E_local > 0");
+        return MOE_ERR_ARG;
+    }
+    if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) {
+        set_error("moe_route_prepare: block_m must be 16, 32, 64 or 128 (got %d)", block_m);
+        return MOE_ERR_ARG;
+    }
+    if (!expert_map && E_local != E) {
+        set_error("moe_route_prepare: without an expert map E_local must equal E (%d vs %d)", E_local, E);
+        return MOE_ERR_EXPERT_SLICE;
+    }
+    if (E_local > kMaxExperts || (!expert_map ? false : E_local > E)) {
+        set_error("moe_route_prepare: E_local %d outside [1, min(E, %d)]", E_local, kMaxExperts);
+        return MOE_ERR_EXPERT_SLICE;
+    }
+    if (static_cast<long long>(M) * k > (1LL << 24)) { set_error("moe_route_prepare: too many routes"); return MOE_ERR_ARG; }
+    const int R = M * k;
+    if (!num_blocks || !expert_count || (R > 0 && (!topk_ids || !sorted_idx || !block_expert))) {
+        set_error("moe_route_prepare: null output or input pointer");
+        return MOE_ERR_ARG;
+    }
+    RouteArgs p{};
+    p.ids = topk_ids;
+    p.R = R;
+    p.E = E;
+    p.map = expert_map;
+    p.E_loc = E_local;
+    p.bm = block_m;
+    p.B_cap = (R + block_m - 1) / block_m + std::min(E_local, R);
+    p.sorted_idx = sorted_idx;
+    p.block_expert = block_expert;
+    p.num_blocks = num_blocks;
+    p.count = expert_count;
+    p.offset = expert_offset;
+    p.route_slot = route_slot;
+    p.status = device_status_ptr();
+    const bool single = route_single_cta(R, E_local, path) && R > 0;
+    if (single) {
+        if (R > kSingleMaxRoutes || E_local > kSingleMaxExperts) {
+            set_error("moe_route_prepare: the single-CTA path takes at most %d routes and %d experts",
+                      kSingleMaxRoutes, kSingleMaxExperts);
+            return MOE_ERR_ARG;
+        }
+        const size_t smem = single_smem_bytes(R, E_local);
+        if (!ensure_smem(reinterpret_cast<const void*>(k_route_single), static_cast<int>(smem))) {
+            set_error("route single: shared-memory limit %zu refused", smem);
+            return MOE_ERR_LAUNCH;
+        }
+        Launch L(dim3(1), dim3(1024), smem, stream, pdl);
+        cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_route_single, p);
+        if (e != cudaSuccess) { set_error("route single launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+        return MOE_OK;
+    }
+    if (R == 0) {
+        // nothing to sort: zero counts and offsets, no blocks (B_cap is 0)
+        cudaError_t e = cudaMemsetAsync(expert_count, 0, sizeof(int32_t) * E_local, stream);
+        if (e == cudaSuccess && expert_offset)
+            e = cudaMemsetAsync(expert_offset, 0, sizeof(int32_t) * (E_local + 1), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(num_blocks, 0, sizeof(int32_t), stream);
+        if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+        return MOE_OK;
+    }
+    const size_t need = route_workspace_bytes(R, E_local, block_m);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+        set_error("moe_route_prepare: multi-CTA path needs %zu bytes of 256-byte aligned workspace (got %zu)",
+                  need, ws_bytes);
+        return MOE_ERR_WORKSPACE;
+    }
+    p.warps = multi_warps(E_local);
+    p.chunk = p.warps * 32;
+    p.nchunks = (R + p.chunk - 1) / p.chunk;
+    char* ws = static_cast<char*>(workspace);
+    p.ws_cnt = reinterpret_cast<int32_t*>(ws);
+    ws += align256(static_cast<size_t>(p.nchunks) * E_local * 4);
+    p.ws_off = reinterpret_cast<int32_t*>(ws);
+    ws += align256(static_cast<size_t>(E_local + 1) * 4);
+    p.ws_done = reinterpret_cast<unsigned*>(ws);
+    cudaError_t e = cudaMemsetAsync(p.ws_done, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    const size_t smem1 = (static_cast<size_t>(E_local) * 2 + 1 + 33) * 4;
+    const size_t ints2 = ((static_cast<size_t>(p.chunk) + E_local) + 3) & ~static_cast<size_t>(3);
+    const size_t smem2 = ints2 * 4 + static_cast<size_t>(p.warps) * E_local * 2;
+    if (!ensure_smem(reinterpret_cast<const void*>(k_route_count), static_cast<int>(smem1)) ||
+        !ensure_smem(reinterpret_cast<const void*>(k_route_scatter), static_cast<int>(smem2))) {
+        set_error("route multi: shared-memory limit refused");
+        return MOE_ERR_LAUNCH;
+    }
+    {
+        Launch L(dim3(p.nchunks), dim3(1024), smem1, stream, false);
+        e = cudaLaunchKernelEx(&L.cfg, k_route_count, p);
+    }
+    if (e == cudaSuccess) {
+        Launch L(dim3(p.nchunks), dim3(p.warps * 32), smem2, stream, false);
+        e = cudaLaunchKernelEx(&L.cfg, k_route_scatter, p);
+    }
+    if (e != cudaSuccess) { set_error("route multi launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" int moe_block_capacity(int M, int k, int E_local, int block_m) {
+    if (M < 0 || k <= 0 || E_local <= 0 || block_m <= 0) return -1;
+    const long long R = static_cast<long long>(M) * k;
+    const long long cap = (R + block_m - 1) / block_m + std::min<long long>(E_local, R);
+    return cap > 0x7FFFFFFFLL ? -1 : static_cast<int>(cap);
+}
+
+extern "C" size_t moe_route_prepare_workspace_bytes(int M, int k, int E_local, int block_m) {
+    if (M < 0 || k <= 0 || E_local <= 0) return 0;
+    return moe::route_workspace_bytes(M * k, E_local, block_m);
+}
+
+extern "C" int moe_route_prepare(const int32_t* topk_ids, int M, int k, int E,
+                                 const int32_t* expert_map, int E_local, int block_m,
+                                 moe_route_path path, int32_t* sorted_idx, int32_t* block_expert,
+                                 int32_t* num_blocks, int32_t* expert_count,
+                                 int32_t* expert_offset, int32_t* route_slot, void* workspace,
+                                 size_t ws_bytes, cudaStream_t stream) {
+    moe::clear_error();
+    if (!moe::device_is_sm103()) { moe::set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    return moe::launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, block_m, path,
+                                     sorted_idx, block_expert, num_blocks, expert_count,
+                                     expert_offset, route_slot, workspace, ws_bytes, false, stream);
+}

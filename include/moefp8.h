@@ -1,0 +1,226 @@
+/*
+ * moefp8.h -- C ABI of libmoefp8.so: the block-FP8 mixture-of-experts layer forward on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller; the library keeps no pointer
+ *   after the call returns and allocates no device memory on these paths (scratch space is the
+ *   caller's `workspace`).
+ * - Every call only enqueues work on `stream` and never synchronises it.  Routing metadata that
+ *   the device produces (num_blocks, ...) stays on the device; the kernels read it there.
+ * - Layouts are row-major and dense.  BF16 tensors are passed as `void*` (IEEE bfloat16 bit
+ *   patterns), E4M3 tensors as `uint8_t*` (OCP e4m3fn codes).  Groups of 128 run along the
+ *   contiguous (last) dimension.
+ * - Return value: MOE_OK (0), or an error code with nothing enqueued.  A text explanation of the
+ *   last error on the calling thread is available from moe_last_error_string().
+ * - Errors that only the device can see (an expert map entry outside [-1, E_local), a bounded
+ *   wait that ran out) set bits in a per-device status word read by moe_get_device_status();
+ *   the affected items are skipped, never trapped.
+ *
+ * Names follow the pages that describe the method: lmdeploy PR #4956 "Perf/pytorch block fp8
+ * moe decode", lmdeploy PR #4857 "optimize compact blocked FP8 MoE and route preparation",
+ * vLLM PR #53875 "Fuse clamped MoE activation and UE8M0 FP8 block quantization" and lmdeploy
+ * PR #4228 "Moe Reduce kernel".
+ */
+#ifndef MOEFP8_H
+#define MOEFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOEFP8_API __attribute__((visibility("default")))
+#else
+#define MOEFP8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = 1,          /* null or misaligned pointer, bad size, unsupported shape      */
+    MOE_ERR_EXPERT_SLICE = 2, /* inconsistent local-expert slice (e.g. no map but E_local!=E) */
+    MOE_ERR_UNSUPPORTED = 3,  /* no sm_103 device current, or the driver lacks an entry point */
+    MOE_ERR_LAUNCH = 4,       /* a CUDA launch or tensor-map encode failed                   */
+    MOE_ERR_WORKSPACE = 5     /* workspace null, misaligned (256 B) or smaller than required  */
+} moe_status;
+
+typedef enum { MOE_SCALE_F32 = 0, MOE_SCALE_UE8M0 = 1 } moe_scale_fmt;
+
+/* IDENTITY: quantise the BF16 input as is (the MoE input hidden states).
+ * SILU_MUL: a = bf16(SiLU(gate) * up), gate = first N columns, up = last N columns; a finite
+ *           clamp_limit L clamps both halves to [-L, L] first.
+ * SILU_MUL_GATE_UPPER: as SILU_MUL but the gate is clamped from above only (gate <= L). */
+typedef enum { MOE_ACT_IDENTITY = 0, MOE_ACT_SILU_MUL = 1, MOE_ACT_SILU_MUL_GATE_UPPER = 2 } moe_act;
+
+typedef enum { MOE_PROJ_GATE_UP = 0, MOE_PROJ_DOWN = 1 } moe_proj;
+typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
+typedef enum { MOE_ROUTE_AUTO = 0, MOE_ROUTE_SINGLE_CTA = 1, MOE_ROUTE_MULTI_CTA = 2 } moe_route_path;
+typedef enum { MOE_QUANT_AUTO = 0, MOE_QUANT_PER_GROUP = 1, MOE_QUANT_PERSISTENT = 2 } moe_quant_strategy;
+
+/* device status bits */
+#define MOE_DEV_TIMEOUT 1
+#define MOE_DEV_BAD_EXPERT_MAP 2
+#define MOE_DEV_BAD_INDEX 4      /* a row index outside the input or output; the row is skipped */
+
+/* ------------------------------------------------------------------------------------------
+ * Route preparation (lmdeploy PR #4857, section "Changes": sorted indices and compact blocks;
+ * its review note asks that the local-expert slice and block_m be validated before launch).
+ *
+ * Routes are the M*k entries of topk_ids [M, k] (int32 global expert ids), numbered r = t*k + j.
+ * A route is dropped when its id is < 0 or >= E, or when expert_map (int32 [E], nullable) sends
+ * it to -1; expert_map maps a global id to a local expert in [0, E_local).  Without a map,
+ * E_local must equal E.
+ *
+ * Outputs (device, int32):
+ *   sorted_idx   [B_cap * block_m]  stable counting sort of the kept routes by local expert
+ *                                   (experts ascending, route id ascending inside an expert);
+ *                                   every expert's run is padded with -1 to a multiple of
+ *                                   block_m; slots past the last block are -1.  Slot
+ *                                   b*block_m + i is row i of block b.
+ *   block_expert [B_cap]            local expert of block b, -1 for b >= num_blocks.  Only
+ *                                   experts that received routes own blocks.
+ *   num_blocks   [1]                number of blocks.
+ *   expert_count [E_local]          kept routes per local expert.
+ *   expert_offset[E_local + 1]      exclusive scan of the padded counts (slot of each run);
+ *                                   nullable.
+ *   route_slot   [M * k]            inverse of sorted_idx: the slot of route r, -1 when the
+ *                                   route is dropped; nullable.
+ * B_cap = moe_block_capacity(M, k, E_local, block_m) = ceil(M*k/block_m) + min(E_local, M*k).
+ * block_m in {16, 32, 64, 128}.  path: AUTO takes the single-CTA sort when M*k <= 2048 and
+ * E_local <= 2048 and the multi-CTA count/scan/scatter otherwise; the others force a path
+ * (SINGLE_CTA needs M*k <= 8192 and E_local <= 2048).
+ * workspace: moe_route_prepare_workspace_bytes(...) bytes, 256-byte aligned (only the multi-CTA
+ * path uses it; the single-CTA path accepts a null workspace).  An expert_map entry outside [-1, E_local) drops that route and sets
+ * MOE_DEV_BAD_EXPERT_MAP.
+ * ------------------------------------------------------------------------------------------ */
+MOEFP8_API int moe_block_capacity(int M, int k, int E_local, int block_m);
+MOEFP8_API size_t moe_route_prepare_workspace_bytes(int M, int k, int E_local, int block_m);
+MOEFP8_API int moe_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int32_t* expert_map,
+                      int E_local, int block_m, moe_route_path path, int32_t* sorted_idx,
+                      int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
+                      int32_t* expert_offset, int32_t* route_slot, void* workspace,
+                      size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Block-FP8 grouped GEMM over the active expert blocks (lmdeploy PR #4956, section
+ * "Active-expert block scheduling"; lmdeploy PR #4857, transposed MMA for small block_m;
+ * vLLM PR #53875, "FP8 W8A8 block shape [128, 128]").
+ *
+ * For every block b < num_blocks (expert e = block_expert[b]) and every slot s of b whose
+ * route sorted_idx[s] >= 0:
+ *   y[s, n] = sum_kb ( sum_{i in kb} a_q[s, i] * w_q[e, n, i] ) * a_s[s, kb] * w_s[e, n/128, kb]
+ * accumulated in fp32.  Work is launched for real blocks only (num_blocks is read on the
+ * device); pad slots are neither read for output nor written.
+ *   a_q  [a_rows, K] E4M3, rows in SLOT order (a_rows >= B_cap*block_m); a_s [a_rows, K/128] f32.
+ *   w_q  [E_local, N_out, K] E4M3 (K contiguous); w_s [E_local, N_out/128, K/128] f32.
+ *   out  GATE_UP: row = slot s (out_rows >= B_cap*block_m);
+ *        DOWN:    row = route sorted_idx[s] (out_rows > every route id, normally M*k).
+ *   out_dtype BF16: out is [out_rows, N_out] bf16 (round to nearest even), splits must be 1.
+ *   out_dtype F32 : out is [splits, out_rows, N_out] f32; split p holds the partial sum over
+ *                   K-blocks [p*KB/splits, (p+1)*KB/splits) (KB = K/128), 1 <= splits <= KB.
+ * K and N_out multiples of 128; block_m in {16, 32, 64, 128}; every pointer 16-byte aligned.
+ * ------------------------------------------------------------------------------------------ */
+MOEFP8_API int moe_blockfp8_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows,
+                              int K, const uint8_t* w_q, const float* w_s, int E_local, int N_out,
+                              const int32_t* sorted_idx, const int32_t* block_expert,
+                              const int32_t* num_blocks, int B_cap, int block_m, void* out,
+                              moe_dtype out_dtype, int out_rows, int splits, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Fused (optionally clamped) SiLU-and-mul with per-128-group dynamic E4M3 quantisation
+ * (vLLM PR #53875, section "Purpose"; lmdeploy PR #4956, "Fused SwiGLU and FP8 quantization").
+ *
+ * Per work row i and group g of 128 columns: the activation a (see moe_act) is materialised in
+ * BF16 in registers only; s = max(amax|a|, 1e-10) / 448 (IEEE fp32 division), rounded up to a
+ * power of two for MOE_SCALE_UE8M0; q = e4m3_rn_satfinite(a / s) (IEEE division).
+ *   in  BF16 [in_rows, W] (in_dtype BF16, in_splits 1) or F32 [in_splits, in_rows, W]
+ *       (in_dtype F32: split partial sums, added in split order in fp32 and rounded to BF16
+ *       first); W = N for IDENTITY, 2N otherwise.
+ *   out_q [out_rows, N] E4M3; out_s [out_rows, N/128] f32.
+ * Rows: work row i in [0, rows) reads input row i and writes output row i, unless row_map
+ *   (nullable int32 [rows]) is given: then m = row_map[i] < 0 skips the row, the output row is
+ *   m and the input row is i / row_div (row_div >= 1) or m (row_div == 0).  This is how the
+ *   layer gathers token rows into expert-sorted slot order (row_map = route_slot, row_div = k).
+ * Expert filter (nullable row_expert [rows] int32 global ids): a work row whose id is < 0,
+ *   >= E, or sent to -1 by expert_map (nullable, [E]) is skipped.
+ * Skipped rows leave out_q / out_s as they were.  An input or output row index past in_rows or
+ * out_rows skips the row and sets MOE_DEV_BAD_INDEX.  clamp_limit: +inf for none.
+ * strategy: PER_GROUP launches one warp per pair of quant groups with no loop (launch-bound
+ * decode without a filter), PERSISTENT a grid-stride kernel sized to the SM count; AUTO picks
+ * PER_GROUP when there is no filter or map and rows*N < 2^20.
+ * N multiple of 128; in and out_q 16-byte aligned.
+ * ------------------------------------------------------------------------------------------ */
+MOEFP8_API int silu_mul_quant_fp8(moe_act act, const void* in, moe_dtype in_dtype, int in_splits,
+                       int in_rows, int rows, int N, float clamp_limit, moe_scale_fmt fmt,
+                       const int32_t* row_expert, const int32_t* expert_map, int E,
+                       const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
+                       float* out_s, moe_quant_strategy strategy, cudaStream_t stream);
+
+/* The unfused first half of the two-kernel path (lmdeploy PR #4956, "Motivation"): writes the
+ * BF16 SiLU*mul result out [rows, N] from in [rows, 2N].  act must not be IDENTITY.  Used as
+ * the separate-kernel arm that the fused kernel is compared with. */
+MOEFP8_API int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, float clamp_limit, void* out,
+                      cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * moe_reduce (lmdeploy PR #4228 "Moe Reduce kernel"): weighted top-k sum back to one row per
+ * token, out[t, h] = bf16( sum_j w[t, j] * z[t*k + j, h] ) over the kept routes in j order,
+ * fp32 accumulation with one fused multiply-add per term.  Dropped routes (id < 0, >= E, or
+ * mapped to -1) contribute nothing and their z rows are never read.
+ *   z [M*k, H] bf16 (route order); topk_w [M, k] f32; topk_ids [M, k] int32;
+ *   expert_map nullable [E]; out [M, H] bf16.  H multiple of 8; pointers 16-byte aligned.
+ * ------------------------------------------------------------------------------------------ */
+MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
+               const int32_t* expert_map, int M, int k, int E, int H, void* out,
+               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * The whole layer: route preparation -> input quantisation (gathered into slot order) ->
+ * gate/up grouped GEMM -> fused SiLU*mul + quantisation -> down grouped GEMM -> moe_reduce.
+ *   x [M, H] bf16; topk_ids / topk_w [M, k]; expert_map nullable [E] (E_local local experts);
+ *   wgu_q [E_local, 2N, H] E4M3 + wgu_s [E_local, 2N/128, H/128] f32 (gate rows 0..N-1, up
+ *   rows N..2N-1); wd_q [E_local, H, N] E4M3 + wd_s [E_local, H/128, N/128] f32;
+ *   act SILU_MUL or SILU_MUL_GATE_UPPER; clamp_limit (+inf = none); act_fmt for the dynamic
+ *   activation scales (input and intermediate); block_m 0 = chosen from the shape.
+ *   out [M, H] bf16.  workspace: moe_blockfp8_workspace_bytes(...) bytes, 256-byte aligned.
+ * H and N multiples of 128.  All stages run on `stream` with no host synchronisation, so the
+ * call can be captured in a CUDA graph.
+ * ------------------------------------------------------------------------------------------ */
+MOEFP8_API size_t moe_blockfp8_workspace_bytes(int M, int k, int E, int E_local, int H, int N, int block_m);
+MOEFP8_API int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, const float* topk_w, int M,
+                         int k, int E, const int32_t* expert_map, int E_local, int H, int N,
+                         const uint8_t* wgu_q, const float* wgu_s, const uint8_t* wd_q,
+                         const float* wd_s, moe_act act, float clamp_limit,
+                         moe_scale_fmt act_fmt, int block_m, void* out, void* workspace,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/* block_m the forward uses when called with block_m = 0. */
+MOEFP8_API int moe_forward_block_m(int M, int k, int E_local, int H, int N);
+
+/* The launch plan moe_blockfp8_forward uses for these sizes: block_m, B_cap (blocks of
+ * capacity) and the split-K count of the gate/up GEMM (its fp32 partials are summed by the
+ * fused activation kernel).  Host only; returns MOE_OK or MOE_ERR_ARG. */
+MOEFP8_API int moe_blockfp8_plan(int M, int k, int E, int E_local, int H, int N, int block_m,
+                                 int* out_block_m, int* out_B_cap, int* out_splits);
+
+/* ------------------------------------------------------------------------------------------
+ * Diagnostics.
+ * ------------------------------------------------------------------------------------------ */
+/* Text of the last error on this thread ("" if none).  The pointer stays valid until the next
+ * call on this thread. */
+MOEFP8_API const char* moe_last_error_string(void);
+/* Reads (synchronously) the status word of the current device into *status; reset != 0 clears
+ * it afterwards.  Returns MOE_OK or MOE_ERR_LAUNCH. */
+MOEFP8_API int moe_get_device_status(int* status, int reset);
+/* 1 if the current device is an sm_103 GPU the library was built for, else 0. */
+MOEFP8_API int moe_device_supported(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOEFP8_H */

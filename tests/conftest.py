@@ -18,3 +18,6 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+from tests.gpu_util import ops  # noqa: E402,F401  (session fixture for the GPU tests)

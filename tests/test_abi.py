@@ -1,0 +1,84 @@
+"""The C-ABI library builds for sm_103a, loads, and exports exactly the entry points that
+include/moefp8.h declares (no compute calls: this runs without a GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moefp8.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"^MOEFP8_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from block_fp8_mixture_moe_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_five_entry_points():
+    names = set(_declared())
+    for n in ("moe_route_prepare", "moe_blockfp8_grouped_gemm", "silu_mul_quant_fp8",
+              "moe_reduce", "moe_blockfp8_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert set(_declared()) <= exported
+    # nothing of the internal C++ namespace leaks into the ABI
+    assert not [s for s in exported if s.startswith("_ZN3moe")]
+
+
+def test_binding_signatures_cover_the_header(lib_path):
+    from block_fp8_mixture_moe_gb300 import ops
+    assert set(ops.SIGNATURES) == set(_declared())
+    text = open(HEADER).read()
+    for name, (_, args) in ops.SIGNATURES.items():
+        m = re.search(r"^MOEFP8_API[^;(]*\b" + name + r"\s*\(([^;]*?)\);", text, flags=re.S | re.M)
+        assert m, name
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(params) == len(args), (name, len(params), len(args))
+    ops.load(lib_path)
+
+
+def test_library_is_built_for_sm103a(lib_path):
+    out = subprocess.run(["cuobjdump", "--list-elf", lib_path], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_pure_host_helpers(lib_path):
+    from block_fp8_mixture_moe_gb300 import ops
+    L = ops.load(lib_path)
+    import oracle
+    for (M, k, E_loc, bm) in [(1, 8, 256, 16), (32, 8, 256, 16), (512, 8, 512, 64), (0, 8, 16, 16), (7, 3, 5, 128)]:
+        assert L.moe_block_capacity(M, k, E_loc, bm) == oracle.block_capacity(M * k, E_loc, bm)
+    assert L.moe_block_capacity(-1, 8, 16, 16) == -1
+    assert L.moe_blockfp8_workspace_bytes(32, 8, 256, 256, 7168, 256, 0) > 0
+    assert L.moe_forward_block_m(1, 8, 256, 7168, 256) in (16, 32, 64, 128)
+
+
+def test_calls_without_a_gpu_fail_cleanly(lib_path):
+    """On a machine without an sm_103 device every launch entry point refuses with
+    MOE_ERR_UNSUPPORTED and launches nothing."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from block_fp8_mixture_moe_gb300 import ops
+    L = ops.load(lib_path)
+    assert L.moe_device_supported() == 0
+    rc = L.moe_reduce(None, None, None, None, 1, 1, 1, 8, None, None)
+    assert rc == ops.MOE_ERR_UNSUPPORTED
+    assert L.moe_last_error_string()

@@ -1,0 +1,128 @@
+"""Whole-layer GPU parity: moe_blockfp8_forward against the CPU oracle, BF16 outputs within
+|err| <= 2e-2 + 1e-2*|ref|, on the pages' workload shapes (seeded synthetic inputs).
+
+Full-size decode (H=7168, N=256, E=256, k=8, M=1..32) is compared on every output; the prefill
+shape (M=512, H=4096, N=768, E=512, Zipf routing) on a token sample that includes the tokens of
+the most loaded expert (each token's output depends only on its own routes, so a sampled
+oracle row is exactly the full-run row)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_fp8_mixture_moe_gb300 import workloads as wl
+from tests.gpu_util import assert_bf16_close, bf16_host, bf16_to_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+INF = float("inf")
+
+
+def _run(ops, L, act=1, clamp=INF, fmt=0, block_m=0):
+    emap = L["expert_map"]
+    out = ops.moe_blockfp8_forward(
+        bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"]), L["E"],
+        None if emap is None else to_dev(emap), L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"],
+        act=act, clamp_limit=clamp, act_fmt=fmt, block_m=block_m)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    return bf16_host(out)
+
+
+def _host(L, tokens=None):
+    ids = L["topk_ids"] if tokens is None else L["topk_ids"][tokens]
+    emap = L["expert_map"]
+    loc = ids[(ids >= 0) & (ids < L["E"])]
+    if emap is not None:
+        loc = emap[loc]
+    return wl.layer_numpy(L, experts=loc[loc >= 0])
+
+
+@pytest.mark.parametrize("act,clamp,fmt", [(1, INF, 0), (1, INF, 1), (1, 7.0, 1), (2, 1.0, 0)])
+@pytest.mark.parametrize("block_m", [0, 16, 32, 64, 128])
+def test_tiny_layer(ops, act, clamp, fmt, block_m):
+    L = wl.make_layer(**wl.CONFIGS["tiny"], seed=0, device="cuda")
+    got = _run(ops, L, act, clamp, fmt, block_m)
+    ref = oracle.moe_forward(_host(L), act=act, clamp_limit=clamp, fmt=fmt)
+    assert_bf16_close(got, ref, "tiny")
+
+
+@pytest.mark.parametrize("M", wl.DECODE_M)
+def test_decode_full_size(ops, M):
+    cfg = dict(wl.CONFIGS["decode"], M=M)
+    L = wl.make_layer(**cfg, seed=1, device="cuda")
+    got = _run(ops, L)
+    ref = oracle.moe_forward(_host(L))
+    assert_bf16_close(got, ref, f"decode M={M}")
+
+
+@pytest.mark.parametrize("T", [1, 10, 100])
+def test_expert_parallel_slice(ops, T):
+    """k=6 of E=256 with 32 local experts through an expert map; non-local routes are dropped
+    in every stage and add nothing to the output."""
+    cfg = dict(wl.CONFIGS["ep"], M=T)
+    L = wl.make_layer(**cfg, seed=2, device="cuda")
+    got = _run(ops, L, clamp=7.0, fmt=1)
+    ref = oracle.moe_forward(_host(L), clamp_limit=7.0, fmt=1)
+    assert_bf16_close(got, ref, f"ep T={T}")
+
+
+def test_prefill_zipf_sampled(ops):
+    cfg = wl.CONFIGS["prefill"]
+    L = wl.make_layer(**cfg, seed=3, device="cuda")
+    got = _run(ops, L)
+    ids = L["topk_ids"]
+    hot = np.bincount(ids.reshape(-1), minlength=cfg["E"]).argmax()
+    hot_tokens = np.nonzero((ids == hot).any(axis=1))[0]
+    r = np.random.default_rng(0)
+    toks = np.unique(np.concatenate([hot_tokens[:8], r.choice(cfg["M"], 16, replace=False), [0, cfg["M"] - 1]]))
+    ref = oracle.moe_forward(_host(L, toks), tokens=toks)
+    assert_bf16_close(got[toks], ref[toks], "prefill sample")
+
+
+def test_invalid_routes_and_empty(ops):
+    L = wl.make_layer(M=9, H=256, N=128, E=12, k=3, seed=4, device="cuda", invalid_frac=0.3)
+    got = _run(ops, L)
+    ref = oracle.moe_forward(_host(L))
+    assert_bf16_close(got, ref, "invalid routes")
+    # every route dropped: the output is exactly zero
+    L2 = dict(L)
+    L2["topk_ids"] = np.full_like(L["topk_ids"], -1)
+    assert (f32 := oracle.bf16_to_f32(_run(ops, L2))).max() == 0 and f32.min() == 0
+    # no tokens at all
+    L3 = dict(L)
+    L3["x"] = L["x"][:0]
+    L3["topk_ids"] = L["topk_ids"][:0]
+    L3["topk_w"] = L["topk_w"][:0]
+    emap = None
+    out = ops.moe_blockfp8_forward(
+        torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"),
+        torch.empty((0, 3), dtype=torch.int32, device="cuda"),
+        torch.empty((0, 3), dtype=torch.float32, device="cuda"), 12, emap,
+        L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"])
+    assert out.shape == (0, 256)
+
+
+def test_forward_is_deterministic_and_graph_capturable(ops):
+    cfg = dict(wl.CONFIGS["decode"], M=4)
+    L = wl.make_layer(**cfg, seed=5, device="cuda")
+    x, ids, w = bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"])
+    M, H = x.shape
+    need = ops.moe_blockfp8_workspace_bytes(M, 8, 256, 256, H, 256)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    args = (x, ids, w, 256, None, L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"])
+    ops.moe_blockfp8_forward(*args, out=out, workspace=ws)
+    first = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        ops.moe_blockfp8_forward(*args, out=out, workspace=ws, stream=s)  # warm up on s
+        torch.cuda.synchronize()
+        out.zero_()
+        with torch.cuda.graph(g, stream=s):
+            ops.moe_blockfp8_forward(*args, out=out, workspace=ws, stream=s)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, first)

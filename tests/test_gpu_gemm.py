@@ -1,0 +1,134 @@
+"""GPU parity of moe_blockfp8_grouped_gemm (tcgen05 kernel) against the oracle's per-route
+block-scaled GEMM, within |err| <= 2e-2 + 1e-2*|ref| (fp32 accumulation in a different order
+than the oracle's exact K-block sums).
+
+Method: lmdeploy PR #4956 "Perf/pytorch block fp8 moe decode" ("Active-expert block
+scheduling") and lmdeploy PR #4857 ("Changes": compact blocks, transposed MMA); W8A8 block
+shape [128, 128] (vLLM PR #53875, "Purpose")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_fp8_mixture_moe_gb300 import workloads as wl
+from tests.gpu_util import assert_bf16_close, bf16_host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(ops, M, k, E, E_loc, bm, K, N_out, kind="uniform", seed=0, inv=0.0):
+    ids, _ = wl.routing_topk(M, E, k, seed=seed, kind=kind)
+    if inv:
+        r = np.random.default_rng(seed)
+        ids = np.where(r.random(ids.shape) < inv, -1, ids).astype(np.int32)
+    emap = None if E_loc == E else wl.expert_map_random(E, E_loc, seed=seed + 1)
+    route = ops.moe_route_prepare(to_dev(ids), E, None if emap is None else to_dev(emap), E_loc, bm)
+    ref_route = oracle.route_prepare(ids, E, emap, E_loc, bm)
+    slots = route["B_cap"] * bm
+    # activations in slot order: realistic per-128 quantised rows; pad slots hold NaN codes so
+    # any leak of a pad column into a real output shows up
+    x = wl.act_rows(max(slots, 1), K, 1.0, seed=seed + 2)[:slots]
+    aq, a_s = oracle.act_quant(0, x, K)
+    si = ref_route["sorted_idx"]
+    aq[si < 0] = 0x7F
+    a_s[si < 0] = np.nan
+    wq, ws = wl.quantized_weights(E_loc, N_out, K, seed=seed + 3, device="cuda")
+    return route, ref_route, aq, a_s, wq, ws
+
+
+def _oracle_rows(ref_route, aq, a_s, wq_h, ws_h, bm):
+    si = ref_route["sorted_idx"]
+    valid = np.nonzero(si >= 0)[0].astype(np.int32)
+    rexp = ref_route["block_expert"][valid // bm].astype(np.int32)
+    out = oracle.route_gemm(aq, a_s, wq_h, ws_h, valid, rexp)
+    return valid, out
+
+
+@pytest.mark.parametrize("proj", [0, 1])
+@pytest.mark.parametrize("M,k,E,E_loc,bm,K,N_out,kind", [
+    (1, 8, 256, 256, 16, 7168, 512, "uniform"),     # decode gate/up, one token
+    (32, 8, 256, 256, 16, 1024, 512, "uniform"),
+    (32, 8, 256, 256, 16, 256, 1024, "uniform"),    # decode-like down (K = N = 256)
+    (100, 6, 256, 32, 32, 2048, 512, "uniform"),    # expert-parallel slice
+    (64, 8, 512, 512, 64, 1024, 384, "zipf"),       # skewed routing, block_m 64
+    (300, 2, 4, 4, 128, 512, 256, "uniform"),       # many tokens per expert, block_m 128
+    (5, 3, 7, 7, 16, 128, 128, "uniform"),          # one K-block, one tile
+])
+def test_gemm_bf16_vs_oracle(ops, proj, M, k, E, E_loc, bm, K, N_out, kind):
+    route, rr, aq, a_s, wq, ws = _setup(ops, M, k, E, E_loc, bm, K, N_out, kind, seed=M + K)
+    slots = route["B_cap"] * bm
+    R = M * k
+    out_rows = slots if proj == 0 else R
+    sentinel = torch.full((out_rows, N_out), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = ops.moe_blockfp8_grouped_gemm(proj, to_dev(aq), to_dev(a_s), wq, ws, route, bm,
+                                        out_dtype=ops.DTYPE_BF16, out_rows=out_rows, out=sentinel)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    wq_h, ws_h = wq.cpu().numpy(), ws.cpu().numpy()
+    valid, ref = _oracle_rows(rr, aq, a_s, wq_h, ws_h, bm)
+    got = bf16_host(out)
+    rows = valid if proj == 0 else rr["sorted_idx"][valid]
+    assert_bf16_close(got[rows], ref, f"proj {proj}")
+    # rows that no route writes keep the sentinel
+    untouched = np.setdiff1d(np.arange(out_rows), rows)
+    assert (got[untouched] == bf16_host(torch.tensor([-7.0], dtype=torch.bfloat16))[0]).all()
+
+
+@pytest.mark.parametrize("splits", [1, 3, 7, 56])
+def test_gemm_fp32_split_partials(ops, splits):
+    """Split p covers K-blocks [p*KB/S, (p+1)*KB/S): each partial equals the oracle GEMM over
+    that slice of K, and the partials sum to the full product."""
+    M, k, E, bm, K, N_out = 4, 8, 64, 16, 7168, 256
+    route, rr, aq, a_s, wq, ws = _setup(ops, M, k, E, E, bm, K, N_out, seed=splits)
+    slots = route["B_cap"] * bm
+    out = ops.moe_blockfp8_grouped_gemm(0, to_dev(aq), to_dev(a_s), wq, ws, route, bm,
+                                        out_dtype=ops.DTYPE_F32, out_rows=slots, splits=splits)
+    torch.cuda.synchronize()
+    P = out.cpu().numpy()
+    wq_h, ws_h = wq.cpu().numpy(), ws.cpu().numpy()
+    si = rr["sorted_idx"]
+    valid = np.nonzero(si >= 0)[0].astype(np.int32)
+    rexp = rr["block_expert"][valid // bm].astype(np.int32)
+    KB = K // 128
+    for p in range(splits):
+        kb0, kb1 = p * KB // splits, (p + 1) * KB // splits
+        sl = slice(kb0 * 128, kb1 * 128)
+        ref = oracle.route_gemm(np.ascontiguousarray(aq[:, sl]), np.ascontiguousarray(a_s[:, kb0:kb1]),
+                                np.ascontiguousarray(wq_h[:, :, sl]), np.ascontiguousarray(ws_h[:, :, kb0:kb1]),
+                                valid, rexp)
+        got = oracle.bf16_round(P[p][valid])
+        assert_bf16_close(got, ref, f"split {p}")
+    full = oracle.route_gemm(aq, a_s, wq_h, ws_h, valid, rexp)
+    assert_bf16_close(oracle.bf16_round(P.sum(axis=0)[valid]), full, "sum of partials")
+
+
+def test_gemm_no_active_blocks(ops):
+    """Every route dropped: no blocks, nothing is written."""
+    M, k, E, bm, K, N_out = 8, 4, 16, 16, 256, 128
+    ids = np.full((M, k), -1, np.int32)
+    route = ops.moe_route_prepare(to_dev(ids), E, None, E, bm)
+    slots = route["B_cap"] * bm
+    aq = torch.zeros((slots, K), dtype=torch.uint8, device="cuda")
+    a_s = torch.ones((slots, K // 128), dtype=torch.float32, device="cuda")
+    wq, ws = wl.quantized_weights(E, N_out, K, seed=1, device="cuda")
+    out = torch.full((slots, N_out), 3.0, dtype=torch.bfloat16, device="cuda")
+    ops.moe_blockfp8_grouped_gemm(0, aq, a_s, wq, ws, route, bm, out=out, out_rows=slots)
+    torch.cuda.synchronize()
+    assert route["num_blocks"].item() == 0
+    assert (out == 3.0).all()
+
+
+def test_gemm_rejects_bad_arguments(ops):
+    M, k, E, bm = 2, 2, 4, 16
+    route = ops.moe_route_prepare(to_dev(np.zeros((M, k), np.int32)), E, None, E, bm)
+    slots = route["B_cap"] * bm
+    aq = torch.zeros((slots, 200), dtype=torch.uint8, device="cuda")  # K not a multiple of 128
+    a_s = torch.ones((slots, 2), dtype=torch.float32, device="cuda")
+    wq = torch.zeros((E, 128, 200), dtype=torch.uint8, device="cuda")
+    ws = torch.ones((E, 1, 2), dtype=torch.float32, device="cuda")
+    with pytest.raises(ops.MoeError):
+        ops.moe_blockfp8_grouped_gemm(0, aq, a_s, wq, ws, route, bm)
+    aq = torch.zeros((slots, 256), dtype=torch.uint8, device="cuda")
+    wq = torch.zeros((E, 128, 256), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ops.MoeError):  # BF16 output with splits > 1
+        ops.moe_blockfp8_grouped_gemm(0, aq, a_s, wq, ws, route, bm, splits=2)
