@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--M", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -276,7 +277,7 @@ def run_ours(args):
     traffic = recorded_traffic()
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(M, ids_host[0], xs[0], wgu_q, wgu_s, wd_q, wd_s, H, N, E, k)
 
     launches_per_step = (1 if M * k <= 2048 else 2) + 5
