@@ -23,6 +23,7 @@
 #include "common.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace moe {
 namespace {
@@ -446,4 +447,139 @@ extern "C" int moe_route_prepare(const int32_t* topk_ids, int M, int k, int E,
     return moe::launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, block_m, path,
                                      sorted_idx, block_expert, num_blocks, expert_count,
                                      expert_offset, route_slot, workspace, ws_bytes, false, stream);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant of the multi-CTA route preparation.
+//
+// For callers that cannot allocate device memory or hand the library a workspace: the chunk
+// histograms, the per-expert slot offsets and the ticket counter live in one file-scope device
+// array instead of the caller's workspace.  Every GPU that loads the library keeps this array
+// (266,752 bytes) until the process exits.  Limits: at most kNoAllocMaxRoutes routes (M*k) and
+// kNoAllocMaxExperts local experts; larger calls are rejected before anything is enqueued.
+// ---------------------------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxRoutes = 65536;
+constexpr int kNoAllocMaxExperts = 1024;
+constexpr int kNoAllocChunk = 1024;  // 32 warps x 32 routes: the scatter CTA size for <= 1536 experts
+constexpr int kNoAllocChunks = kNoAllocMaxRoutes / kNoAllocChunk;
+constexpr size_t kNoAllocCntInts = static_cast<size_t>(kNoAllocChunks) * kNoAllocMaxExperts;
+constexpr size_t kNoAllocOffInts = 1088;  // >= kNoAllocMaxExperts + 1, keeps 256-byte alignment
+constexpr size_t kNoAllocInts = kNoAllocCntInts + kNoAllocOffInts + 64;
+
+static __device__ __align__(256) int32_t g_route_noalloc_scratch[kNoAllocInts];
+
+int32_t* g_noalloc_ptr[64] = {nullptr};
+std::mutex g_noalloc_mutex;
+
+// Device address of the scratch array on the current device, looked up once per device.
+int32_t* noalloc_scratch() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[d]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_route_noalloc_scratch);
+        if (e != cudaSuccess) {
+            set_error("moe_route_prepare_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        g_noalloc_ptr[d] = static_cast<int32_t*>(p);
+    }
+    return g_noalloc_ptr[d];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, int E,
+                                         const int32_t* expert_map, int E_local, int block_m,
+                                         int32_t* sorted_idx, int32_t* block_expert,
+                                         int32_t* num_blocks, int32_t* expert_count,
+                                         int32_t* expert_offset, int32_t* route_slot,
+                                         cudaStream_t stream) {
+    using namespace moe;
+    clear_error();
+    if (!device_is_sm103()) { set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    if (M < 0 || k <= 0 || E <= 0 || E_local <= 0) {
+        set_error("moe_route_prepare_noalloc: need M >= 0, k > 0, E > 0, E_local > 0");
+        return MOE_ERR_ARG;
+    }
+    if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) {
+        set_error("moe_route_prepare_noalloc: block_m must be 16, 32, 64 or 128 (got %d)", block_m);
+        return MOE_ERR_ARG;
+    }
+    if (!expert_map && E_local != E) {
+        set_error("moe_route_prepare_noalloc: without an expert map E_local must equal E (%d vs %d)", E_local, E);
+        return MOE_ERR_EXPERT_SLICE;
+    }
+    if (expert_map && E_local > E) {
+        set_error("moe_route_prepare_noalloc: E_local %d > E %d", E_local, E);
+        return MOE_ERR_EXPERT_SLICE;
+    }
+    const long long R = static_cast<long long>(M) * k;
+    if (R > kNoAllocMaxRoutes || E_local > kNoAllocMaxExperts) {
+        set_error("moe_route_prepare_noalloc: at most %d routes (M*k) and %d local experts fit its "
+                  "fixed scratch (got %lld routes, %d experts); use moe_route_prepare with a workspace",
+                  kNoAllocMaxRoutes, kNoAllocMaxExperts, R, E_local);
+        return MOE_ERR_ARG;
+    }
+    if (!num_blocks || !expert_count || (R > 0 && (!topk_ids || !sorted_idx || !block_expert))) {
+        set_error("moe_route_prepare_noalloc: null output or input pointer");
+        return MOE_ERR_ARG;
+    }
+    if (R == 0) {
+        cudaError_t e = cudaMemsetAsync(expert_count, 0, sizeof(int32_t) * E_local, stream);
+        if (e == cudaSuccess && expert_offset)
+            e = cudaMemsetAsync(expert_offset, 0, sizeof(int32_t) * (E_local + 1), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(num_blocks, 0, sizeof(int32_t), stream);
+        if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+        return MOE_OK;
+    }
+    int32_t* scratch = noalloc_scratch();
+    if (!scratch) return MOE_ERR_LAUNCH;
+    RouteArgs p{};
+    p.ids = topk_ids;
+    p.R = static_cast<int>(R);
+    p.E = E;
+    p.map = expert_map;
+    p.E_loc = E_local;
+    p.bm = block_m;
+    p.B_cap = static_cast<int>((R + block_m - 1) / block_m + std::min<long long>(E_local, R));
+    p.sorted_idx = sorted_idx;
+    p.block_expert = block_expert;
+    p.num_blocks = num_blocks;
+    p.count = expert_count;
+    p.offset = expert_offset;
+    p.route_slot = route_slot;
+    p.status = device_status_ptr();
+    p.warps = kNoAllocChunk / 32;
+    p.chunk = kNoAllocChunk;
+    p.nchunks = static_cast<int>((R + kNoAllocChunk - 1) / kNoAllocChunk);
+    p.ws_cnt = scratch;                                       // [nchunks][E_local]
+    p.ws_off = scratch + kNoAllocCntInts;                     // [E_local + 1]
+    p.ws_done = reinterpret_cast<unsigned*>(scratch + kNoAllocCntInts + kNoAllocOffInts);
+    // the ticket counter must start at zero (the array keeps the previous call's contents)
+    cudaError_t e = cudaMemsetAsync(p.ws_done, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    const size_t smem1 = (static_cast<size_t>(E_local) * 2 + 1 + 33) * 4;
+    const size_t ints2 = ((static_cast<size_t>(p.chunk) + E_local) + 3) & ~static_cast<size_t>(3);
+    const size_t smem2 = ints2 * 4 + static_cast<size_t>(p.warps) * E_local * 2;
+    if (!ensure_smem(reinterpret_cast<const void*>(k_route_count), static_cast<int>(smem1)) ||
+        !ensure_smem(reinterpret_cast<const void*>(k_route_scatter), static_cast<int>(smem2))) {
+        set_error("moe_route_prepare_noalloc: shared-memory limit refused");
+        return MOE_ERR_LAUNCH;
+    }
+    {
+        Launch L(dim3(p.nchunks), dim3(1024), smem1, stream, false);
+        e = cudaLaunchKernelEx(&L.cfg, k_route_count, p);
+    }
+    if (e == cudaSuccess) {
+        Launch L(dim3(p.nchunks), dim3(p.warps * 32), smem2, stream, false);
+        e = cudaLaunchKernelEx(&L.cfg, k_route_scatter, p);
+    }
+    if (e != cudaSuccess) { set_error("moe_route_prepare_noalloc launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    return MOE_OK;
 }

@@ -32,6 +32,7 @@ SIGNATURES = {
     "moe_block_capacity": (_I, [_I, _I, _I, _I]),
     "moe_route_prepare_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "moe_route_prepare": (_I, [_P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_route_prepare_noalloc": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_blockfp8_grouped_gemm": (_I, [_I, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I, _P,
                                        _I, _I, _I, _P]),
     "silu_mul_quant_fp8": (_I, [_I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _I, _P, _I, _I, _P, _P,
@@ -135,6 +136,37 @@ def moe_route_prepare(topk_ids, E, expert_map, E_local, block_m, path=ROUTE_AUTO
     _check(rc, "moe_route_prepare")
     out["B_cap"] = B_cap
     out["_ws"] = ws
+    return out
+
+
+def moe_route_prepare_noalloc(topk_ids, E, expert_map, E_local, block_m, stream=None):
+    """Route preparation that allocates nothing inside the library: its scratch is a fixed
+    array in the library (for callers that cannot provide device memory).  The output tensors
+    below are allocated here by torch only because this is the Python binding; C callers pass
+    their own.  Same outputs as moe_route_prepare."""
+    L = load()
+    ids = _i32(topk_ids)
+    M, k = ids.shape
+    dev = ids.device
+    B_cap = L.moe_block_capacity(M, k, E_local, block_m)
+    if B_cap < 0:
+        raise MoeError("moe_block_capacity: bad arguments")
+    out = dict(
+        sorted_idx=torch.empty(max(1, B_cap * block_m), dtype=torch.int32, device=dev)[: B_cap * block_m],
+        block_expert=torch.empty(max(1, B_cap), dtype=torch.int32, device=dev)[:B_cap],
+        num_blocks=torch.empty(1, dtype=torch.int32, device=dev),
+        expert_count=torch.empty(E_local, dtype=torch.int32, device=dev),
+        expert_offset=torch.empty(E_local + 1, dtype=torch.int32, device=dev),
+        route_slot=torch.empty(max(1, M * k), dtype=torch.int32, device=dev)[: M * k],
+    )
+    em = _i32(expert_map)
+    rc = L.moe_route_prepare_noalloc(_ptr(ids), M, k, E, _ptr(em), E_local, block_m,
+                                     _ptr(out["sorted_idx"]), _ptr(out["block_expert"]),
+                                     _ptr(out["num_blocks"]), _ptr(out["expert_count"]),
+                                     _ptr(out["expert_offset"]), _ptr(out["route_slot"]),
+                                     _stream(stream))
+    _check(rc, "moe_route_prepare_noalloc")
+    out["B_cap"] = B_cap
     return out
 
 

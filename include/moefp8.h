@@ -106,6 +106,32 @@ MOEFP8_API int moe_route_prepare(const int32_t* topk_ids, int M, int k, int E, c
                       int32_t* expert_offset, int32_t* route_slot, void* workspace,
                       size_t ws_bytes, cudaStream_t stream);
 
+/* Allocation-free route preparation (no counterpart in the pages; added for callers that
+ * cannot allocate).  Some callers have no way to obtain device memory for a workspace: a host
+ * that owns every byte of device memory and gives this library neither an allocator nor a
+ * workspace, or code that must not allocate at all because allocation would synchronise the
+ * device or is forbidden where it runs.  This variant of the multi-CTA route preparation keeps
+ * its scratch (per-chunk expert histograms, per-expert slot offsets, a ticket counter) in a
+ * fixed array inside the library instead: 266,752 bytes of device memory on every GPU that
+ * loads the library, held until the process exits.  It allocates nothing and calls no
+ * allocating routine.
+ *   Arguments and outputs are those of moe_route_prepare (always the multi-CTA path), without
+ *   the workspace.  Limits: M*k <= 65536 routes and E_local <= 1024; larger sizes return
+ *   MOE_ERR_ARG with nothing enqueued.
+ *   Set-up: the first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress while that device is current; make that first call before any stream
+ *   capture.
+ *   Sharing: every call on a device uses the same array and leaves its contents behind (the
+ *   ticket counter is cleared on the stream at the start of each call).  Calls whose execution
+ *   overlaps on the GPU -- on different streams, or from different threads -- race on the array
+ *   and give wrong results; serialise them. */
+MOEFP8_API int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, int E,
+                                         const int32_t* expert_map, int E_local, int block_m,
+                                         int32_t* sorted_idx, int32_t* block_expert,
+                                         int32_t* num_blocks, int32_t* expert_count,
+                                         int32_t* expert_offset, int32_t* route_slot,
+                                         cudaStream_t stream);
+
 /* ------------------------------------------------------------------------------------------
  * Block-FP8 grouped GEMM over the active expert blocks (lmdeploy PR #4956, section
  * "Active-expert block scheduling"; lmdeploy PR #4857, transposed MMA for small block_m;
