@@ -13,17 +13,24 @@
 // is (block b, 128-row output tile, K split); a persistent grid of one CTA per SM walks the
 // units round-robin.  num_blocks is read on the device, so no work exists for inactive experts.
 //
-// Per CTA (192 threads, one CTA per SM):
+// Per CTA (224 threads, one CTA per SM):
+//   warp 6        : metadata.  Walks this CTA's units ahead of everyone else and writes, per
+//                   chunk of up to CK K-blocks of a unit, a descriptor into a shared-memory
+//                   ring: expert, block, tile, K range, the block's output rows, and the token
+//                   and weight-block scales of those K-blocks.  All dependent global loads of
+//                   the kernel happen here, off the critical path.
 //   warp 0  lane 0: TMA producer.  Per 128-wide K-block it loads the 128x128 E4M3 weight tile
 //                   (16 KB) and the block_m x 128 activation tile into one pipeline stage,
 //                   both with 128-byte swizzle, completion counted on the stage's mbarrier.
 //   warp 1  lane 0: MMA issuer.  Per K-block: 4 tcgen05.mma (K = 32 each) into a fresh fp32
 //                   accumulator buffer in tensor memory, then tcgen05.commit frees the smem
 //                   stage and signals the accumulator buffer.
-//   warps 2-5     : epilogue / scale promotion.  Per K-block each thread (one weight row) reads
-//                   its block_m partial sums with tcgen05.ld, frees the buffer, and accumulates
-//                   partial * a_s[token, kb] * w_s[expert, tile, kb] in fp32 registers; at the
-//                   end of the unit it writes BF16 or fp32 (split-K partials) outputs.
+//   warps 2-5     : epilogue / scale promotion.  Each thread owns one weight row; per K-block
+//                   it reads its block_m partial sums (tcgen05.ld, two buffers per wait when
+//                   block_m = 16), frees the buffer, and accumulates
+//                   partial * a_s[token, kb] * w_s[expert, tile, kb] in fp32 registers with the
+//                   scales read from the descriptor; at the end of the unit it writes BF16 or
+//                   fp32 (split-K partials) outputs to the rows the descriptor lists.
 // Block scales differ per K-block, so every K-block gets its own accumulator buffer; 4-8
 // buffers let the MMA run ahead of the promotion.  Every wait is bounded (see mbar_wait).
 #include "common.cuh"
@@ -59,16 +66,45 @@ struct Cfg {
     static constexpr int kBufs = BM <= 64 ? 8 : 4;     // tensor-memory accumulator buffers
     static constexpr int kCols = kBufs * BM <= 32 ? 32 : kBufs * BM <= 64 ? 64
                                : kBufs * BM <= 128 ? 128 : kBufs * BM <= 256 ? 256 : 512;
+    // descriptor ring
+    static constexpr int kCK = 2048 / BM;              // K-blocks per descriptor chunk
+    static constexpr int kRing = 3;
+    static constexpr int kDescHdr = 8;                 // ints: e, b, nt, sp, kb0, nck, flags, -
+    static constexpr int kDescInts = kDescHdr + BM + kCK + kCK * BM;  // hdr, rows, sw, sa
+    static constexpr int kDescBytes = ((kDescInts * 4) + 15) / 16 * 16;
     static constexpr int kBarBytes = 1024;
-    static constexpr int kSmem = kStages * kStage + kBarBytes + 1024;  // + alignment slack
+    static constexpr int kSmem = kStages * kStage + kRing * kDescBytes + kBarBytes + 1024;
+    static constexpr int kThreads = 224;
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kBufs * BM <= 512, "tensor memory holds 512 fp32 columns");
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
+// descriptor flags
+constexpr int kFirst = 1, kLast = 2, kEnd = 4;
+
+struct Desc {
+    int* hdr;
+    int* rows;
+    float* sw;
+    float* sa;  // [kCK][BM]
+};
+
+template <int BM>
+__device__ __forceinline__ Desc desc_at(uint8_t* ring, int slot) {
+    using C = Cfg<BM>;
+    int* base = reinterpret_cast<int*>(ring + slot * C::kDescBytes);
+    Desc d;
+    d.hdr = base;
+    d.rows = base + C::kDescHdr;
+    d.sw = reinterpret_cast<float*>(d.rows + BM);
+    d.sa = d.sw + C::kCK;
+    return d;
+}
+
 __device__ __forceinline__ void decode_unit(const GemmArgs& p, long long u, int& b, int& nt,
-                                            int& kb0, int& kb1) {
-    const int sp = static_cast<int>(u % p.splits);
+                                            int& sp, int& kb0, int& kb1) {
+    sp = static_cast<int>(u % p.splits);
     const long long bt = u / p.splits;
     nt = static_cast<int>(bt % p.NT);
     b = static_cast<int>(bt / p.NT);
@@ -76,24 +112,22 @@ __device__ __forceinline__ void decode_unit(const GemmArgs& p, long long u, int&
     kb1 = static_cast<int>((static_cast<long long>(sp + 1) * p.KB) / p.splits);
 }
 
-__device__ __forceinline__ int unit_expert(const GemmArgs& p, int b) {
-    const int e = __ldg(p.block_expert + b);
-    return (e >= 0 && e < p.E_local) ? e : -1;
-}
-
 template <int BM>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_a, GemmArgs p) {
     using C = Cfg<BM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+    uint8_t* ring = smem + C::kStages * C::kStage;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kRing * C::kDescBytes);
     uint64_t* empty = full + C::kStages;
     uint64_t* tfull = empty + C::kStages;
     uint64_t* tempty = tfull + C::kBufs;
-    uint64_t* mma_done = tempty + C::kBufs;
+    uint64_t* dfull = tempty + C::kBufs;
+    uint64_t* dempty = dfull + C::kRing;
+    uint64_t* mma_done = dempty + C::kRing;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -101,6 +135,7 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
         for (int i = 0; i < C::kBufs; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
+        for (int i = 0; i < C::kRing; ++i) { mbar_init(dfull + i, 32); mbar_init(dempty + i, 130); }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -122,25 +157,79 @@ __global__ void __launch_bounds__(192, 1)
     // everything below reads what earlier kernels on the stream wrote
     grid_dep_wait();
     grid_dep_launch();
-    int nblk = __ldg(p.num_blocks);
-    nblk = max(0, min(nblk, p.B_cap));
-    const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
 
-    if (warp == 0) {
+    if (warp == 6) {
+        // ---------------- metadata warp ----------------
+        int nblk = __ldg(p.num_blocks);
+        nblk = max(0, min(nblk, p.B_cap));
+        const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
+        int slot = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            int b, nt, sp, kb0, kb1;
+            decode_unit(p, u, b, nt, sp, kb0, kb1);
+            const int e_raw = __ldg(p.block_expert + b);
+            const int e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
+            if (e < 0) continue;  // not a block of a local expert: no work anywhere
+            for (int c0 = kb0; c0 < kb1; c0 += C::kCK) {
+                const int nck = min(C::kCK, kb1 - c0);
+                ok = mbar_wait(dempty + slot, ph ^ 1u, abort_flag, p.status);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                Desc d = desc_at<BM>(ring, slot);
+                if (lane == 0) {
+                    d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt; d.hdr[3] = sp; d.hdr[4] = c0;
+                    d.hdr[5] = nck;
+                    d.hdr[6] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
+                }
+                for (int j = lane; j < BM; j += 32) {
+                    const int slot_j = b * BM + j;
+                    const int r = __ldg(p.sorted_idx + slot_j);
+                    int row = r < 0 ? -1 : (p.scatter ? r : slot_j);
+                    if (row >= p.out_rows) {
+                        if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                        row = -1;
+                    }
+                    d.rows[j] = row;
+                }
+                const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB + c0;
+                for (int kk = lane; kk < nck; kk += 32) d.sw[kk] = __ldg(wsc + kk);
+                for (int i = lane; i < nck * BM; i += 32) {
+                    const int kk = i / BM, j = i - kk * BM;
+                    d.sa[i] = __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk);
+                }
+                mbar_arrive(dfull + slot);
+                if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
+            }
+        }
+        if (ok) {
+            // end marker
+            ok = mbar_wait(dempty + slot, ph ^ 1u, abort_flag, p.status);
+            if (__all_sync(0xFFFFFFFFu, ok)) {
+                if (lane == 0) desc_at<BM>(ring, slot).hdr[6] = kEnd;
+                mbar_arrive(dfull + slot);
+            }
+        }
+    } else if (warp == 0) {
+        // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_a = l2_policy_evict_last();
-            int s = 0;
-            uint32_t ph = 0;
+            int s = 0, slot = 0;
+            uint32_t ph = 0, dph = 0;
             long long issued = 0;
-            for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-                int b, nt, kb0, kb1;
-                decode_unit(p, u, b, nt, kb0, kb1);
-                const int e = unit_expert(p, b);
-                if (e < 0) continue;
+            for (;;) {
+                if (!mbar_wait(dfull + slot, dph, abort_flag, p.status)) break;
+                const Desc d = desc_at<BM>(ring, slot);
+                const int flags = d.hdr[6];
+                if (flags & kEnd) break;
+                const int e = d.hdr[0], b = d.hdr[1], nt = d.hdr[2], c0 = d.hdr[4], nck = d.hdr[5];
+                mbar_arrive(dempty + slot);
+                if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
                 const int wrow = e * p.N_out + nt * 128;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, p.status)) goto producer_done;
+                bool ok = true;
+                for (int kb = c0; kb < c0 + nck; ++kb) {
+                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t* st = smem + s * C::kStage;
                     mbar_arrive_expect_tx(full + s, C::kStage);
                     tma_load_2d(st, &tmap_w, full + s, kb * 128, wrow, pol_w);
@@ -148,8 +237,8 @@ __global__ void __launch_bounds__(192, 1)
                     ++issued;
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
+                if (!ok) break;
             }
-        producer_done:
             if (*abort_flag) {
                 // never leave a TMA write in flight: wait for the last load of every stage
                 for (int i = 0; i < C::kStages; ++i) {
@@ -161,94 +250,134 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f8_f32(128, BM);
-            int s = 0, tb = 0;
-            uint32_t ph = 0, tph = 0;
-            for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-                int b, nt, kb0, kb1;
-                decode_unit(p, u, b, nt, kb0, kb1);
-                if (unit_expert(p, b) < 0) continue;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(tempty + tb, tph ^ 1u, abort_flag, p.status)) goto mma_out;
-                    if (!mbar_wait(full + s, ph, abort_flag, p.status)) goto mma_out;
+            int s = 0, tb = 0, slot = 0;
+            uint32_t ph = 0, tph = 0, dph = 0;
+            for (;;) {
+                if (!mbar_wait(dfull + slot, dph, abort_flag, p.status)) break;
+                const Desc d = desc_at<BM>(ring, slot);
+                const int flags = d.hdr[6];
+                if (flags & kEnd) break;
+                const int nck = d.hdr[5];
+                mbar_arrive(dempty + slot);
+                if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
+                bool ok = true;
+                for (int kk = 0; kk < nck; ++kk) {
+                    if (!mbar_wait(tempty + tb, tph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (!mbar_wait(full + s, ph, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(tb * BM);
+                    const uint32_t dt = tmem_base + static_cast<uint32_t>(tb * BM);
                     const uint32_t wa = smem_u32(smem + s * C::kStage);
                     const uint32_t aa = wa + C::kWBytes;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f8(d, smem_desc_sw128(wa + ks * 32), smem_desc_sw128(aa + ks * 32), idesc,
+                        mma_f8(dt, smem_desc_sw128(wa + ks * 32), smem_desc_sw128(aa + ks * 32), idesc,
                                ks > 0 ? 1u : 0u);
                     mma_commit(empty + s);
                     mma_commit(tfull + tb);
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
                     if (++tb == C::kBufs) { tb = 0; tph ^= 1u; }
                 }
+                if (!ok) break;
             }
-        mma_out:
             // all issued MMAs complete before tensor memory is released
             mma_commit(mma_done);
             volatile int no_abort = 0;
             mbar_wait(mma_done, 0, &no_abort, p.status);
         }
     } else {
-        // epilogue: warp (2..5) & 3 selects the 32-lane quarter of tensor memory it may read
+        // ---------------- epilogue (warps 2..5) ----------------
+        // warp & 3 selects the 32-lane quarter of tensor memory this warp may read
         const int q = warp & 3;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         const int r_in_tile = q * 32 + lane;
-        int tb = 0;
-        uint32_t tph = 0;
-        for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-            int b, nt, kb0, kb1;
-            decode_unit(p, u, b, nt, kb0, kb1);
-            const int e = unit_expert(p, b);
-            if (e < 0) continue;
-            float acc[BM];
+        int tb = 0, slot = 0;
+        uint32_t tph = 0, dph = 0;
+        float acc[BM];
 #pragma unroll
-            for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
-            const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                const float sw = __ldg(wsc + kb);
-                constexpr int kSa = BM < 32 ? 1 : BM / 32;
-                float sa[kSa];
+        for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
+        for (;;) {
+            bool ok = mbar_wait(dfull + slot, dph, abort_flag, p.status);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            const Desc d = desc_at<BM>(ring, slot);
+            const int flags = d.hdr[6];
+            if (flags & kEnd) break;
+            const int nck = d.hdr[5];
+            if (flags & kFirst) {
 #pragma unroll
-                for (int i = 0; i < kSa; ++i) {
-                    const int j = i * 32 + lane;
-                    sa[i] = j < BM ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + kb) : 0.0f;
+                for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
+            }
+            int kk = 0;
+            if (BM == 16) {
+                // two K-blocks per tensor-memory wait
+                for (; kk + 1 < nck; kk += 2) {
+                    const int tb1 = tb + 1 == C::kBufs ? 0 : tb + 1;
+                    const uint32_t tph1 = tb + 1 == C::kBufs ? (tph ^ 1u) : tph;
+                    ok = mbar_wait(tfull + tb, tph, abort_flag, p.status) &&
+                         mbar_wait(tfull + tb1, tph1, abort_flag, p.status);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
+                    tc_fence_after();
+                    float v[32];
+                    tmem_ld16x2(lane_base + static_cast<uint32_t>(tb * BM),
+                                lane_base + static_cast<uint32_t>(tb1 * BM), v);
+                    tc_fence_before();
+                    mbar_arrive(tempty + tb);
+                    mbar_arrive(tempty + tb1);
+                    const float sw0 = d.sw[kk], sw1 = d.sw[kk + 1];
+                    const float4* sa0 = reinterpret_cast<const float4*>(d.sa + kk * BM);
+                    const float4* sa1 = reinterpret_cast<const float4*>(d.sa + (kk + 1) * BM);
+#pragma unroll
+                    for (int j4 = 0; j4 < BM / 4; ++j4) {
+                        const float4 a0 = sa0[j4], a1 = sa1[j4];
+                        const float s0[4] = {a0.x, a0.y, a0.z, a0.w};
+                        const float s1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int j = j4 * 4 + i;
+                            acc[j] = __fmaf_rn(v[j], __fmul_rn(s0[i], sw0), acc[j]);
+                            acc[j] = __fmaf_rn(v[16 + j], __fmul_rn(s1[i], sw1), acc[j]);
+                        }
+                    }
+                    tb = tb1 + 1 == C::kBufs ? 0 : tb1 + 1;
+                    tph = tb1 + 1 == C::kBufs ? (tph1 ^ 1u) : tph1;
                 }
-                bool ok = mbar_wait(tfull + tb, tph, abort_flag, p.status);
+            }
+            for (; kk < nck; ++kk) {
+                ok = mbar_wait(tfull + tb, tph, abort_flag, p.status);
                 if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < BM / 16; ++c) {
+                const float sw = d.sw[kk];
+                const float* sa = d.sa + kk * BM;
+                if (BM == 16) {
                     float v[16];
-                    tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                  static_cast<uint32_t>(tb * BM + c * 16),
-                              v);
+                    tmem_ld16(lane_base + static_cast<uint32_t>(tb * BM), v);
+                    tc_fence_before();
+                    mbar_arrive(tempty + tb);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = c * 16 + i;
-                        const float sj = __shfl_sync(0xFFFFFFFFu, sa[j / 32], j % 32);
-                        acc[j] = __fmaf_rn(v[i], __fmul_rn(sj, sw), acc[j]);
+                    for (int j = 0; j < 16; ++j) acc[j] = __fmaf_rn(v[j], __fmul_rn(sa[j], sw), acc[j]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BM / 32; ++c) {
+                        float v[32];
+                        tmem_ld32(lane_base + static_cast<uint32_t>(tb * BM + c * 32), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            acc[c * 32 + i] = __fmaf_rn(v[i], __fmul_rn(sa[c * 32 + i], sw), acc[c * 32 + i]);
                     }
+                    tc_fence_before();
+                    mbar_arrive(tempty + tb);
                 }
-                tc_fence_before();
-                mbar_arrive(tempty + tb);
                 if (++tb == C::kBufs) { tb = 0; tph ^= 1u; }
             }
-            {
-                const int n = nt * 128 + r_in_tile;
-                const int sp = static_cast<int>(u % p.splits);
+            if (flags & kLast) {
+                const int n = d.hdr[2] * 128 + r_in_tile;
+                const int sp = d.hdr[3];
 #pragma unroll
                 for (int j = 0; j < BM; ++j) {
-                    const int slot = b * BM + j;
-                    const int r = __ldg(p.sorted_idx + slot);
-                    if (r < 0) continue;
-                    const int row = p.scatter ? r : slot;
-                    if (row >= p.out_rows) {
-                        if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
-                        continue;
-                    }
+                    const int row = d.rows[j];
+                    if (row < 0) continue;
                     if (p.out_f32) {
                         float* o = static_cast<float*>(p.out);
                         o[(static_cast<long long>(sp) * p.out_rows + row) * p.N_out + n] = acc[j];
@@ -259,6 +388,8 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            mbar_arrive(dempty + slot);
+            if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
         }
     epi_done:;
     }
@@ -312,7 +443,7 @@ int launch_bm(const CUtensorMap& tw, const CUtensorMap& ta, const GemmArgs& p, l
     }
     long long grid = std::min<long long>(sm_count(), max_units);
     if (grid <= 0) return MOE_OK;
-    Launch L(dim3(static_cast<unsigned>(grid)), dim3(192), C::kSmem, stream, pdl);
+    Launch L(dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmem, stream, pdl);
     cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_grouped_gemm<BM>, tw, ta, p);
     if (e != cudaSuccess) { set_error("grouped_gemm launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     return MOE_OK;

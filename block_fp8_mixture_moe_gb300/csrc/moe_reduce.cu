@@ -9,49 +9,64 @@
 //
 // One thread produces 8 consecutive outputs of one token: per kept route one 16-byte load of 8
 // BF16 values (a warp reads 512 contiguous bytes), 8 FMAs, and one 16-byte store at the end.
-// HBM traffic is the kept routes' rows once plus the output once.
+// HBM traffic is the kept routes' rows once plus the output once.  top-k is at most 16.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-__global__ void __launch_bounds__(256) k_moe_reduce(const uint16_t* __restrict__ z,
+constexpr int kMaxTopk = 16;
+
+// One CTA per (token, 1024-column slice): the token's top-k ids, weights and keep flags are
+// read once into shared memory; each thread then issues all its route loads back to back
+// before the fused multiply-adds, so the loads overlap instead of running one after another.
+__global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__ z,
                                                     const float* __restrict__ w,
                                                     const int32_t* __restrict__ ids,
                                                     const int32_t* __restrict__ map, int M, int k,
                                                     int E, int H, uint16_t* __restrict__ out) {
+    __shared__ float s_w[kMaxTopk];
+    __shared__ int s_keep[kMaxTopk];
     grid_dep_wait();
     grid_dep_launch();
-    const int cpt = H / 8;  // 8-wide chunks per token
-    const long long total = static_cast<long long>(M) * cpt;
-    for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < total;
-         c += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(c / cpt);
-        const int col = static_cast<int>(c - static_cast<long long>(t) * cpt) * 8;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int id = __ldg(ids + static_cast<long long>(t) * k + j);
-            if (id < 0 || id >= E) continue;
-            if (map && __ldg(map + id) < 0) continue;
-            const float wj = __ldg(w + static_cast<long long>(t) * k + j);
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                z + (static_cast<long long>(t) * k + j) * H + col));
-            acc[0] = __fmaf_rn(wj, bf16_lo(v.x), acc[0]);
-            acc[1] = __fmaf_rn(wj, bf16_hi(v.x), acc[1]);
-            acc[2] = __fmaf_rn(wj, bf16_lo(v.y), acc[2]);
-            acc[3] = __fmaf_rn(wj, bf16_hi(v.y), acc[3]);
-            acc[4] = __fmaf_rn(wj, bf16_lo(v.z), acc[4]);
-            acc[5] = __fmaf_rn(wj, bf16_hi(v.z), acc[5]);
-            acc[6] = __fmaf_rn(wj, bf16_lo(v.w), acc[6]);
-            acc[7] = __fmaf_rn(wj, bf16_hi(v.w), acc[7]);
-        }
-        uint4 o;
-        o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
-        o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
-        o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
-        o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
-        *reinterpret_cast<uint4*>(out + static_cast<long long>(t) * H + col) = o;
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) {
+        const int j = threadIdx.x;
+        const int id = __ldg(ids + static_cast<long long>(t) * k + j);
+        bool keep = id >= 0 && id < E;
+        if (keep && map) keep = __ldg(map + id) >= 0;
+        s_keep[j] = keep ? 1 : 0;
+        s_w[j] = __ldg(w + static_cast<long long>(t) * k + j);
     }
+    __syncthreads();
+    const int col = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
+    if (col >= H) return;
+    uint4 v[kMaxTopk];
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j)
+        if (j < k && s_keep[j])
+            v[j] = __ldg(reinterpret_cast<const uint4*>(z + (static_cast<long long>(t) * k + j) * H + col));
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) {
+        if (j < k && s_keep[j]) {
+            const float wj = s_w[j];
+            acc[0] = __fmaf_rn(wj, bf16_lo(v[j].x), acc[0]);
+            acc[1] = __fmaf_rn(wj, bf16_hi(v[j].x), acc[1]);
+            acc[2] = __fmaf_rn(wj, bf16_lo(v[j].y), acc[2]);
+            acc[3] = __fmaf_rn(wj, bf16_hi(v[j].y), acc[3]);
+            acc[4] = __fmaf_rn(wj, bf16_lo(v[j].z), acc[4]);
+            acc[5] = __fmaf_rn(wj, bf16_hi(v[j].z), acc[5]);
+            acc[6] = __fmaf_rn(wj, bf16_lo(v[j].w), acc[6]);
+            acc[7] = __fmaf_rn(wj, bf16_hi(v[j].w), acc[7]);
+        }
+    }
+    uint4 o;
+    o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
+    o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
+    o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
+    o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
+    *reinterpret_cast<uint4*>(out + static_cast<long long>(t) * H + col) = o;
 }
 
 }  // namespace
@@ -64,10 +79,9 @@ int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_id
     if (total == 0) return MOE_OK;
     if (!z || !topk_w || !topk_ids || !out) { set_error("moe_reduce: null pointer"); return MOE_ERR_ARG; }
     if (!aligned16(z) || !aligned16(out)) { set_error("moe_reduce: z and out must be 16-byte aligned"); return MOE_ERR_ARG; }
-    long long blocks = (total + 255) / 256;
-    const long long cap = static_cast<long long>(sm_count()) * 8;
-    if (blocks > cap) blocks = cap;
-    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl);
+    if (k > kMaxTopk) { set_error("moe_reduce: top-k above %d is not supported", kMaxTopk); return MOE_ERR_ARG; }
+    const int slices = (H / 8 + 127) / 128;
+    Launch L(dim3(static_cast<unsigned>(M), static_cast<unsigned>(slices)), dim3(128), 0, stream, pdl);
     cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_moe_reduce, static_cast<const uint16_t*>(z),
                                        topk_w, topk_ids, expert_map, M, k, E, H,
                                        static_cast<uint16_t*>(out));

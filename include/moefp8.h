@@ -199,7 +199,8 @@ MOEFP8_API int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, f
  * fp32 accumulation with one fused multiply-add per term.  Dropped routes (id < 0, >= E, or
  * mapped to -1) contribute nothing and their z rows are never read.
  *   z [M*k, H] bf16 (route order); topk_w [M, k] f32; topk_ids [M, k] int32;
- *   expert_map nullable [E]; out [M, H] bf16.  H multiple of 8; pointers 16-byte aligned.
+ *   expert_map nullable [E]; out [M, H] bf16.  H multiple of 8, k <= 16; pointers 16-byte
+ *   aligned.
  * ------------------------------------------------------------------------------------------ */
 MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
                const int32_t* expert_map, int M, int k, int E, int H, void* out,
