@@ -219,7 +219,8 @@ extern "C" size_t moe_blockfp8_workspace_bytes(int M, int k, int E, int E_local,
 extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, const float* topk_w,
                                     int M, int k, int E, const int32_t* expert_map, int E_local,
                                     int H, int N, const uint8_t* wgu_q, const float* wgu_s,
-                                    const uint8_t* wd_q, const float* wd_s, moe_act act,
+                                    const uint8_t* wd_q, const float* wd_s,
+                                    moe_weight_layout w_layout, moe_act act,
                                     float clamp_limit, moe_scale_fmt act_fmt, int block_m,
                                     void* out, void* workspace, size_t ws_bytes,
                                     cudaStream_t stream) {
@@ -277,14 +278,15 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                           MOE_QUANT_PERSISTENT, true, stream);
     if (rc) return rc;
     rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
-                             sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
+                             w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
                              MOE_DTYPE_F32, P.slots, P.splits, true, stream);
     if (rc) return rc;
     rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
                           nullptr, nullptr, 0, route_slot, 0, P.slots, aq, as,
                           MOE_QUANT_PERSISTENT, true, stream);
     if (rc) return rc;
-    rc = launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, sorted_idx,
+    rc = launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, w_layout,
+                             sorted_idx,
                              block_expert, num_blocks, P.B_cap, P.bm, z, MOE_DTYPE_BF16, P.R, 1,
                              true, stream);
     if (rc) return rc;

@@ -47,7 +47,7 @@ size_t route_workspace_bytes(int R, int E_local, int block_m);
 bool route_single_cta(int R, int E_local, moe_route_path path);
 int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows, int K,
                         const uint8_t* w_q, const float* w_s, int E_local, int N_out,
-                        const int32_t* sorted_idx, const int32_t* block_expert,
+                        moe_weight_layout w_layout, const int32_t* sorted_idx, const int32_t* block_expert,
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
                         cudaStream_t stream);

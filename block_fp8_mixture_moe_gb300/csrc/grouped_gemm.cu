@@ -54,6 +54,7 @@ struct GemmArgs {
     int B_cap;
     void* out;
     int out_f32, out_rows, splits, scatter;
+    int w_tiled;
     int* status;
 };
 
@@ -166,40 +167,75 @@ __global__ void __launch_bounds__(224, 1)
         int slot = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (long long u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            int b, nt, sp, kb0, kb1;
-            decode_unit(p, u, b, nt, sp, kb0, kb1);
-            const int e_raw = __ldg(p.block_expert + b);
-            const int e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
-            if (e < 0) continue;  // not a block of a local expert: no work anywhere
-            for (int c0 = kb0; c0 < kb1; c0 += C::kCK) {
-                const int nck = min(C::kCK, kb1 - c0);
-                ok = mbar_wait(dempty + slot, ph ^ 1u, abort_flag, p.status);
-                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                Desc d = desc_at<BM>(ring, slot);
-                if (lane == 0) {
-                    d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt; d.hdr[3] = sp; d.hdr[4] = c0;
-                    d.hdr[5] = nck;
-                    d.hdr[6] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
+        long long u = blockIdx.x;
+        while (u < units && ok) {
+            // the experts of this CTA's next 32 units in one round trip (lane l: unit u + l*grid)
+            int e_lane = -1;
+            {
+                const long long ul = u + static_cast<long long>(lane) * gridDim.x;
+                if (ul < units) {
+                    int b_l, nt_l, sp_l, k0_l, k1_l;
+                    decode_unit(p, ul, b_l, nt_l, sp_l, k0_l, k1_l);
+                    const int e_raw = __ldg(p.block_expert + b_l);
+                    e_lane = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
                 }
-                for (int j = lane; j < BM; j += 32) {
-                    const int slot_j = b * BM + j;
-                    const int r = __ldg(p.sorted_idx + slot_j);
-                    int row = r < 0 ? -1 : (p.scatter ? r : slot_j);
-                    if (row >= p.out_rows) {
-                        if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
-                        row = -1;
+            }
+            for (int i = 0; i < 32 && u < units && ok; ++i, u += gridDim.x) {
+                const int e = __shfl_sync(0xFFFFFFFFu, e_lane, i);
+                if (e < 0) continue;  // not a block of a local expert: no work anywhere
+                int b, nt, sp, kb0, kb1;
+                decode_unit(p, u, b, nt, sp, kb0, kb1);
+                for (int c0 = kb0; c0 < kb1; c0 += C::kCK) {
+                    const int nck = min(C::kCK, kb1 - c0);
+                    // the loads do not depend on the ring slot: issue them before waiting on it
+                    int rows[(BM + 31) / 32];
+#pragma unroll
+                    for (int t = 0; t < (BM + 31) / 32; ++t) {
+                        const int j = t * 32 + lane;
+                        int row = -1;
+                        if (j < BM) {
+                            const int slot_j = b * BM + j;
+                            const int r = __ldg(p.sorted_idx + slot_j);
+                            row = r < 0 ? -1 : (p.scatter ? r : slot_j);
+                            if (row >= p.out_rows) {
+                                if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                                row = -1;
+                            }
+                        }
+                        rows[t] = row;
                     }
-                    d.rows[j] = row;
+                    const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB + c0;
+                    ok = mbar_wait(dempty + slot, ph ^ 1u, abort_flag, p.status);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    Desc d = desc_at<BM>(ring, slot);
+                    if (lane == 0) {
+                        d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt; d.hdr[3] = sp; d.hdr[4] = c0;
+                        d.hdr[5] = nck;
+                        d.hdr[6] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
+                    }
+#pragma unroll
+                    for (int t = 0; t < (BM + 31) / 32; ++t)
+                        if (t * 32 + lane < BM) d.rows[t * 32 + lane] = rows[t];
+                    for (int kk = lane; kk < nck; kk += 32) d.sw[kk] = __ldg(wsc + kk);
+                    // token scales, 8 loads in flight per lane
+                    const int n_sa = nck * BM;
+                    for (int i0 = 0; i0 < n_sa; i0 += 256) {
+                        float v[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int i = i0 + q * 32 + lane;
+                            const int kk = i / BM, j = i - kk * BM;
+                            v[q] = i < n_sa ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk) : 0.0f;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int i = i0 + q * 32 + lane;
+                            if (i < n_sa) d.sa[i] = v[q];
+                        }
+                    }
+                    mbar_arrive(dfull + slot);
+                    if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
                 }
-                const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB + c0;
-                for (int kk = lane; kk < nck; kk += 32) d.sw[kk] = __ldg(wsc + kk);
-                for (int i = lane; i < nck * BM; i += 32) {
-                    const int kk = i / BM, j = i - kk * BM;
-                    d.sa[i] = __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk);
-                }
-                mbar_arrive(dfull + slot);
-                if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
             }
         }
         if (ok) {
@@ -226,13 +262,19 @@ __global__ void __launch_bounds__(224, 1)
                 const int e = d.hdr[0], b = d.hdr[1], nt = d.hdr[2], c0 = d.hdr[4], nck = d.hdr[5];
                 mbar_arrive(dempty + slot);
                 if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
-                const int wrow = e * p.N_out + nt * 128;
+                // row-major weights: box (kb*128, e*N_out + nt*128); tiled weights: every
+                // 128x128 tile is one contiguous 16 KB run at row ((e*NT + nt)*KB + kb)*128
+                const long long wrow = p.w_tiled ? (static_cast<long long>(e) * p.NT + nt) * p.KB * 128
+                                                 : static_cast<long long>(e) * p.N_out + nt * 128;
                 bool ok = true;
                 for (int kb = c0; kb < c0 + nck; ++kb) {
                     if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t* st = smem + s * C::kStage;
                     mbar_arrive_expect_tx(full + s, C::kStage);
-                    tma_load_2d(st, &tmap_w, full + s, kb * 128, wrow, pol_w);
+                    if (p.w_tiled)
+                        tma_load_2d(st, &tmap_w, full + s, 0, static_cast<int>(wrow + kb * 128), pol_w);
+                    else
+                        tma_load_2d(st, &tmap_w, full + s, kb * 128, static_cast<int>(wrow), pol_w);
                     tma_load_2d(st + C::kWBytes, &tmap_a, full + s, kb * 128, b * BM, pol_a);
                     ++issued;
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
@@ -453,7 +495,7 @@ int launch_bm(const CUtensorMap& tw, const CUtensorMap& ta, const GemmArgs& p, l
 
 int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows, int K,
                         const uint8_t* w_q, const float* w_s, int E_local, int N_out,
-                        const int32_t* sorted_idx, const int32_t* block_expert,
+                        moe_weight_layout w_layout, const int32_t* sorted_idx, const int32_t* block_expert,
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
                         cudaStream_t stream) {
@@ -488,9 +530,16 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
         return MOE_ERR_ARG;
     }
     if (B_cap == 0) return MOE_OK;
-    if (static_cast<long long>(E_local) * N_out > 0x7FFFFFFFLL) { set_error("grouped_gemm: E_local*N_out too large"); return MOE_ERR_ARG; }
+    if (w_layout != MOE_WEIGHTS_ROW_MAJOR && w_layout != MOE_WEIGHTS_TILED) {
+        set_error("grouped_gemm: unknown weight layout");
+        return MOE_ERR_ARG;
+    }
+    const bool tiled = w_layout == MOE_WEIGHTS_TILED;
+    const long long w_rows = tiled ? static_cast<long long>(E_local) * N_out * (K / 128)
+                                   : static_cast<long long>(E_local) * N_out;
+    if (w_rows > 0x7FFFFFFFLL) { set_error("grouped_gemm: weight tensor too large"); return MOE_ERR_ARG; }
     CUtensorMap tw, ta;
-    if (!make_map(&tw, w_q, static_cast<long long>(E_local) * N_out, K, 128) ||
+    if (!make_map(&tw, w_q, w_rows, tiled ? 128 : K, 128) ||
         !make_map(&ta, a_q, a_rows, K, block_m)) {
         set_error("grouped_gemm: tensor-map encode failed (driver entry point missing or bad layout)");
         return MOE_ERR_LAUNCH;
@@ -513,6 +562,7 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
     p.out_rows = out_rows;
     p.splits = splits;
     p.scatter = proj == MOE_PROJ_DOWN;
+    p.w_tiled = tiled ? 1 : 0;
     p.status = device_status_ptr();
     const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
     switch (block_m) {
@@ -527,13 +577,59 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
 
 extern "C" int moe_blockfp8_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s,
                                          int a_rows, int K, const uint8_t* w_q, const float* w_s,
-                                         int E_local, int N_out, const int32_t* sorted_idx,
+                                         int E_local, int N_out, moe_weight_layout w_layout,
+                                         const int32_t* sorted_idx,
                                          const int32_t* block_expert, const int32_t* num_blocks,
                                          int B_cap, int block_m, void* out, moe_dtype out_dtype,
                                          int out_rows, int splits, cudaStream_t stream) {
     moe::clear_error();
     if (!moe::device_is_sm103()) { moe::set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
-    return moe::launch_grouped_gemm(proj, a_q, a_s, a_rows, K, w_q, w_s, E_local, N_out, sorted_idx,
+    return moe::launch_grouped_gemm(proj, a_q, a_s, a_rows, K, w_q, w_s, E_local, N_out, w_layout,
+                                    sorted_idx,
                                     block_expert, num_blocks, B_cap, block_m, out, out_dtype,
                                     out_rows, splits, false, stream);
+}
+
+namespace moe {
+namespace {
+// 16 bytes per thread: tiled[e][nt][kb][r][c] = src[e][nt*128 + r][kb*128 + c]
+__global__ void __launch_bounds__(256) k_pack_weights(const uint4* __restrict__ src, int E, int N_out,
+                                                      int K, uint4* __restrict__ dst) {
+    const int NT = N_out / 128, KB = K / 128;
+    const long long total = static_cast<long long>(E) * N_out * K / 16;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        long long t = i;
+        const int c16 = static_cast<int>(t % 8); t /= 8;
+        const int r = static_cast<int>(t % 128); t /= 128;
+        const int kb = static_cast<int>(t % KB); t /= KB;
+        const int nt = static_cast<int>(t % NT); t /= NT;
+        const long long e = t;
+        const long long from = ((e * N_out + nt * 128 + r) * K + kb * 128) / 16 + c16;
+        dst[i] = __ldg(src + from);
+    }
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_blockfp8_pack_weights(const uint8_t* w_q, int E_local, int N_out, int K,
+                                         uint8_t* w_tiled, cudaStream_t stream) {
+    using namespace moe;
+    clear_error();
+    if (!device_is_sm103()) { set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
+    if (!w_q || !w_tiled || !aligned16(w_q) || !aligned16(w_tiled)) {
+        set_error("moe_blockfp8_pack_weights: null or misaligned pointer");
+        return MOE_ERR_ARG;
+    }
+    if (E_local <= 0 || N_out <= 0 || K <= 0 || N_out % 128 || K % 128) {
+        set_error("moe_blockfp8_pack_weights: N_out and K must be positive multiples of 128");
+        return MOE_ERR_ARG;
+    }
+    const long long total = static_cast<long long>(E_local) * N_out * K / 16;
+    long long blocks = std::min<long long>((total + 255) / 256, static_cast<long long>(sm_count()) * 16);
+    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, false);
+    cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_pack_weights, reinterpret_cast<const uint4*>(w_q),
+                                       E_local, N_out, K, reinterpret_cast<uint4*>(w_tiled));
+    if (e != cudaSuccess) { set_error("moe_blockfp8_pack_weights launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    return MOE_OK;
 }

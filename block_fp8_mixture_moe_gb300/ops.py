@@ -25,6 +25,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 ROUTE_AUTO, ROUTE_SINGLE_CTA, ROUTE_MULTI_CTA = 0, 1, 2
 QUANT_AUTO, QUANT_PER_GROUP, QUANT_PERSISTENT = 0, 1, 2
 DEV_TIMEOUT, DEV_BAD_EXPERT_MAP, DEV_BAD_INDEX = 1, 2, 4
+WEIGHTS_ROW_MAJOR, WEIGHTS_TILED = 0, 1
 
 # every entry point of include/moefp8.h with its ctypes signature
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -33,15 +34,16 @@ SIGNATURES = {
     "moe_route_prepare_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "moe_route_prepare": (_I, [_P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_route_prepare_noalloc": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
-    "moe_blockfp8_grouped_gemm": (_I, [_I, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I, _P,
-                                       _I, _I, _I, _P]),
+    "moe_blockfp8_grouped_gemm": (_I, [_I, _P, _P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I,
+                                       _P, _I, _I, _I, _P]),
+    "moe_blockfp8_pack_weights": (_I, [_P, _I, _I, _I, _P, _P]),
     "silu_mul_quant_fp8": (_I, [_I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _I, _P, _I, _I, _P, _P,
                                 _I, _P]),
     "silu_and_mul_bf16": (_I, [_I, _P, _I, _I, _F, _P, _P]),
     "moe_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_blockfp8_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
-    "moe_blockfp8_forward": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _F,
-                                  _I, _I, _P, _P, _Z, _P]),
+    "moe_blockfp8_forward": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I,
+                                  _F, _I, _I, _P, _P, _Z, _P]),
     "moe_forward_block_m": (_I, [_I, _I, _I, _I, _I]),
     "moe_blockfp8_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
                                ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
@@ -209,12 +211,34 @@ def silu_and_mul_bf16(act, inp, N, clamp_limit=float("inf"), stream=None):
     return out
 
 
+def moe_blockfp8_pack_weights(w_q, stream=None):
+    """Row-major E4M3 weights [E, N_out, K] -> the tiled layout (every 128x128 block one
+    contiguous 16 KB run).  Returns a uint8 tensor of shape [E, N_out/128, K/128, 128, 128]."""
+    L = load()
+    E, N_out, K = w_q.shape
+    out = torch.empty((E, N_out // 128, K // 128, 128, 128), dtype=torch.uint8, device=w_q.device)
+    _check(L.moe_blockfp8_pack_weights(_ptr(w_q), E, N_out, K, _ptr(out), _stream(stream)),
+           "moe_blockfp8_pack_weights")
+    return out
+
+
+def _weight_dims(w_q):
+    """(E_local, N_out, K, layout) of a row-major [E, N_out, K] or tiled [E, NT, KB, 128, 128]
+    weight tensor."""
+    if w_q.dim() == 5:
+        E, NT, KB = w_q.shape[:3]
+        return E, NT * 128, KB * 128, WEIGHTS_TILED
+    E, N_out, K = w_q.shape
+    return E, N_out, K, WEIGHTS_ROW_MAJOR
+
+
 def moe_blockfp8_grouped_gemm(proj, a_q, a_s, w_q, w_s, route, block_m, out_dtype=DTYPE_BF16,
                               out_rows=None, splits=1, out=None, stream=None):
-    """route: the dict returned by moe_route_prepare.  Returns the output tensor."""
+    """route: the dict returned by moe_route_prepare.  w_q row-major [E, N_out, K] or tiled
+    [E, N_out/128, K/128, 128, 128].  Returns the output tensor."""
     L = load()
     a_rows, K = a_q.shape
-    E_local, N_out = w_q.shape[0], w_q.shape[1]
+    E_local, N_out, _, layout = _weight_dims(w_q)
     B_cap = route["B_cap"]
     if out_rows is None:
         out_rows = B_cap * block_m
@@ -224,7 +248,7 @@ def moe_blockfp8_grouped_gemm(proj, a_q, a_s, w_q, w_s, route, block_m, out_dtyp
         else:
             out = torch.zeros((out_rows, N_out), dtype=torch.bfloat16, device=a_q.device)
     rc = L.moe_blockfp8_grouped_gemm(proj, _ptr(a_q), _ptr(a_s), a_rows, K, _ptr(w_q), _ptr(w_s),
-                                     E_local, N_out, _ptr(route["sorted_idx"]),
+                                     E_local, N_out, layout, _ptr(route["sorted_idx"]),
                                      _ptr(route["block_expert"]), _ptr(route["num_blocks"]), B_cap,
                                      block_m, _ptr(out), out_dtype, out_rows, splits,
                                      _stream(stream))
@@ -269,15 +293,16 @@ def moe_blockfp8_forward(x, topk_ids, topk_w, E, expert_map, wgu_q, wgu_s, wd_q,
     assert expert_map is None or expert_map.dtype == torch.int32
     M, H = x.shape
     k = topk_ids.shape[1]
-    E_local = wgu_q.shape[0]
-    N = wd_q.shape[2]
+    E_local, _, _, layout = _weight_dims(wgu_q)
+    _, H_d, N, layout_d = _weight_dims(wd_q)
+    assert layout == layout_d and H_d == H, "both weight tensors must use the same layout"
     need = L.moe_blockfp8_workspace_bytes(M, k, E, E_local, H, N, block_m)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     if out is None:
         out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     rc = L.moe_blockfp8_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), M, k, E, _ptr(expert_map),
-                                E_local, H, N, _ptr(wgu_q), _ptr(wgu_s), _ptr(wd_q), _ptr(wd_s), act,
+                                E_local, H, N, _ptr(wgu_q), _ptr(wgu_s), _ptr(wd_q), _ptr(wd_s), layout, act,
                                 float(clamp_limit), act_fmt, block_m, _ptr(out), _ptr(workspace),
                                 workspace.numel(), _stream(stream))
     _check(rc, "moe_blockfp8_forward")

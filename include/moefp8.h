@@ -61,6 +61,10 @@ typedef enum { MOE_PROJ_GATE_UP = 0, MOE_PROJ_DOWN = 1 } moe_proj;
 typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
 typedef enum { MOE_ROUTE_AUTO = 0, MOE_ROUTE_SINGLE_CTA = 1, MOE_ROUTE_MULTI_CTA = 2 } moe_route_path;
 typedef enum { MOE_QUANT_AUTO = 0, MOE_QUANT_PER_GROUP = 1, MOE_QUANT_PERSISTENT = 2 } moe_quant_strategy;
+/* ROW_MAJOR: [E_local, N_out, K] (K contiguous).  TILED: the same weights regrouped so that
+ * every 128x128 block is one contiguous 16 KB run, ordered [E_local][N_out/128][K/128][128][128]
+ * (see moe_blockfp8_pack_weights); the block scales keep their layout. */
+typedef enum { MOE_WEIGHTS_ROW_MAJOR = 0, MOE_WEIGHTS_TILED = 1 } moe_weight_layout;
 
 /* device status bits */
 #define MOE_DEV_TIMEOUT 1
@@ -143,7 +147,8 @@ MOEFP8_API int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, 
  * accumulated in fp32.  Work is launched for real blocks only (num_blocks is read on the
  * device); pad slots are neither read for output nor written.
  *   a_q  [a_rows, K] E4M3, rows in SLOT order (a_rows >= B_cap*block_m); a_s [a_rows, K/128] f32.
- *   w_q  [E_local, N_out, K] E4M3 (K contiguous); w_s [E_local, N_out/128, K/128] f32.
+ *   w_q  [E_local, N_out, K] E4M3 (K contiguous) for MOE_WEIGHTS_ROW_MAJOR, or the tiled
+ *        regrouping of it for MOE_WEIGHTS_TILED; w_s [E_local, N_out/128, K/128] f32.
  *   out  GATE_UP: row = slot s (out_rows >= B_cap*block_m);
  *        DOWN:    row = route sorted_idx[s] (out_rows > every route id, normally M*k).
  *   out_dtype BF16: out is [out_rows, N_out] bf16 (round to nearest even), splits must be 1.
@@ -153,9 +158,18 @@ MOEFP8_API int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, 
  * ------------------------------------------------------------------------------------------ */
 MOEFP8_API int moe_blockfp8_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows,
                               int K, const uint8_t* w_q, const float* w_s, int E_local, int N_out,
-                              const int32_t* sorted_idx, const int32_t* block_expert,
+                              moe_weight_layout w_layout, const int32_t* sorted_idx,
+                              const int32_t* block_expert,
                               const int32_t* num_blocks, int B_cap, int block_m, void* out,
                               moe_dtype out_dtype, int out_rows, int splits, cudaStream_t stream);
+
+/* Weight regrouping for MOE_WEIGHTS_TILED (done once when the weights are loaded; not part of
+ * the per-forward path): w_tiled[e][nt][kb][r][c] = w_q[e][nt*128 + r][kb*128 + c].  A tiled
+ * weight tile is one contiguous 16 KB read for the GEMM's TMA instead of 128 rows of 128 bytes
+ * that lie K bytes apart.  N_out and K multiples of 128; both pointers 16-byte aligned; the
+ * buffers must not overlap. */
+MOEFP8_API int moe_blockfp8_pack_weights(const uint8_t* w_q, int E_local, int N_out, int K,
+                                         uint8_t* w_tiled, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Fused (optionally clamped) SiLU-and-mul with per-128-group dynamic E4M3 quantisation
@@ -211,7 +225,8 @@ MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* top
  * gate/up grouped GEMM -> fused SiLU*mul + quantisation -> down grouped GEMM -> moe_reduce.
  *   x [M, H] bf16; topk_ids / topk_w [M, k]; expert_map nullable [E] (E_local local experts);
  *   wgu_q [E_local, 2N, H] E4M3 + wgu_s [E_local, 2N/128, H/128] f32 (gate rows 0..N-1, up
- *   rows N..2N-1); wd_q [E_local, H, N] E4M3 + wd_s [E_local, H/128, N/128] f32;
+ *   rows N..2N-1); wd_q [E_local, H, N] E4M3 + wd_s [E_local, H/128, N/128] f32; both weight
+ *   tensors in w_layout (row-major, or tiled by moe_blockfp8_pack_weights);
  *   act SILU_MUL or SILU_MUL_GATE_UPPER; clamp_limit (+inf = none); act_fmt for the dynamic
  *   activation scales (input and intermediate); block_m 0 = chosen from the shape.
  *   out [M, H] bf16.  workspace: moe_blockfp8_workspace_bytes(...) bytes, 256-byte aligned.
@@ -222,7 +237,8 @@ MOEFP8_API size_t moe_blockfp8_workspace_bytes(int M, int k, int E, int E_local,
 MOEFP8_API int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, const float* topk_w, int M,
                          int k, int E, const int32_t* expert_map, int E_local, int H, int N,
                          const uint8_t* wgu_q, const float* wgu_s, const uint8_t* wd_q,
-                         const float* wd_s, moe_act act, float clamp_limit,
+                         const float* wd_s, moe_weight_layout w_layout, moe_act act,
+                         float clamp_limit,
                          moe_scale_fmt act_fmt, int block_m, void* out, void* workspace,
                          size_t ws_bytes, cudaStream_t stream);
 

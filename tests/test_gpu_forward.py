@@ -17,11 +17,14 @@ pytestmark = pytest.mark.gpu
 INF = float("inf")
 
 
-def _run(ops, L, act=1, clamp=INF, fmt=0, block_m=0):
+def _run(ops, L, act=1, clamp=INF, fmt=0, block_m=0, tiled=False):
     emap = L["expert_map"]
+    wgu, wd = L["wgu_q"], L["wd_q"]
+    if tiled:
+        wgu, wd = ops.moe_blockfp8_pack_weights(wgu), ops.moe_blockfp8_pack_weights(wd)
     out = ops.moe_blockfp8_forward(
         bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"]), L["E"],
-        None if emap is None else to_dev(emap), L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"],
+        None if emap is None else to_dev(emap), wgu, L["wgu_s"], wd, L["wd_s"],
         act=act, clamp_limit=clamp, act_fmt=fmt, block_m=block_m)
     torch.cuda.synchronize()
     assert ops.device_status() == 0
@@ -37,11 +40,12 @@ def _host(L, tokens=None):
     return wl.layer_numpy(L, experts=loc[loc >= 0])
 
 
+@pytest.mark.parametrize("tiled", [False, True])
 @pytest.mark.parametrize("act,clamp,fmt", [(1, INF, 0), (1, INF, 1), (1, 7.0, 1), (2, 1.0, 0)])
 @pytest.mark.parametrize("block_m", [0, 16, 32, 64, 128])
-def test_tiny_layer(ops, act, clamp, fmt, block_m):
+def test_tiny_layer(ops, act, clamp, fmt, block_m, tiled):
     L = wl.make_layer(**wl.CONFIGS["tiny"], seed=0, device="cuda")
-    got = _run(ops, L, act, clamp, fmt, block_m)
+    got = _run(ops, L, act, clamp, fmt, block_m, tiled)
     ref = oracle.moe_forward(_host(L), act=act, clamp_limit=clamp, fmt=fmt)
     assert_bf16_close(got, ref, "tiny")
 
@@ -50,7 +54,7 @@ def test_tiny_layer(ops, act, clamp, fmt, block_m):
 def test_decode_full_size(ops, M):
     cfg = dict(wl.CONFIGS["decode"], M=M)
     L = wl.make_layer(**cfg, seed=1, device="cuda")
-    got = _run(ops, L)
+    got = _run(ops, L, tiled=(M % 2 == 0))
     ref = oracle.moe_forward(_host(L))
     assert_bf16_close(got, ref, f"decode M={M}")
 
@@ -69,7 +73,7 @@ def test_expert_parallel_slice(ops, T):
 def test_prefill_zipf_sampled(ops):
     cfg = wl.CONFIGS["prefill"]
     L = wl.make_layer(**cfg, seed=3, device="cuda")
-    got = _run(ops, L)
+    got = _run(ops, L, tiled=True)
     ids = L["topk_ids"]
     hot = np.bincount(ids.reshape(-1), minlength=cfg["E"]).argmax()
     hot_tokens = np.nonzero((ids == hot).any(axis=1))[0]

@@ -44,6 +44,7 @@ def _oracle_rows(ref_route, aq, a_s, wq_h, ws_h, bm):
     return valid, out
 
 
+@pytest.mark.parametrize("tiled", [False, True])
 @pytest.mark.parametrize("proj", [0, 1])
 @pytest.mark.parametrize("M,k,E,E_loc,bm,K,N_out,kind", [
     (1, 8, 256, 256, 16, 7168, 512, "uniform"),     # decode gate/up, one token
@@ -54,13 +55,14 @@ def _oracle_rows(ref_route, aq, a_s, wq_h, ws_h, bm):
     (300, 2, 4, 4, 128, 512, 256, "uniform"),       # many tokens per expert, block_m 128
     (5, 3, 7, 7, 16, 128, 128, "uniform"),          # one K-block, one tile
 ])
-def test_gemm_bf16_vs_oracle(ops, proj, M, k, E, E_loc, bm, K, N_out, kind):
+def test_gemm_bf16_vs_oracle(ops, proj, M, k, E, E_loc, bm, K, N_out, kind, tiled):
     route, rr, aq, a_s, wq, ws = _setup(ops, M, k, E, E_loc, bm, K, N_out, kind, seed=M + K)
     slots = route["B_cap"] * bm
     R = M * k
     out_rows = slots if proj == 0 else R
     sentinel = torch.full((out_rows, N_out), -7.0, dtype=torch.bfloat16, device="cuda")
-    out = ops.moe_blockfp8_grouped_gemm(proj, to_dev(aq), to_dev(a_s), wq, ws, route, bm,
+    w_used = ops.moe_blockfp8_pack_weights(wq) if tiled else wq
+    out = ops.moe_blockfp8_grouped_gemm(proj, to_dev(aq), to_dev(a_s), w_used, ws, route, bm,
                                         out_dtype=ops.DTYPE_BF16, out_rows=out_rows, out=sentinel)
     torch.cuda.synchronize()
     assert ops.device_status() == 0
@@ -132,3 +134,13 @@ def test_gemm_rejects_bad_arguments(ops):
     wq = torch.zeros((E, 128, 256), dtype=torch.uint8, device="cuda")
     with pytest.raises(ops.MoeError):  # BF16 output with splits > 1
         ops.moe_blockfp8_grouped_gemm(0, aq, a_s, wq, ws, route, bm, splits=2)
+
+
+def test_pack_weights_is_the_tile_regrouping(ops):
+    """tiled[e, nt, kb, r, c] == w[e, nt*128 + r, kb*128 + c] (a pure data movement, checked
+    against torch's view/permute of the same bytes)."""
+    wq, _ = wl.quantized_weights(3, 384, 640, seed=4, device="cuda")
+    t = ops.moe_blockfp8_pack_weights(wq)
+    torch.cuda.synchronize()
+    ref = wq.view(3, 3, 128, 5, 128).permute(0, 1, 3, 2, 4).contiguous()
+    assert torch.equal(t, ref)
