@@ -226,6 +226,13 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, vo
     }
 }
 
+// Inline fast path: one try_wait, then the bounded slow path.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait(bar, parity, abort, status);
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -60,15 +60,17 @@ struct GemmArgs {
 
 template <int BM>
 struct Cfg {
-    static constexpr int kWBytes = 128 * 128;
-    static constexpr int kABytes = BM * 128;
-    static constexpr int kStage = kWBytes + kABytes;  // multiple of 1024
-    static constexpr int kStages = BM <= 16 ? 10 : BM <= 32 ? 9 : BM <= 64 ? 8 : 6;
-    static constexpr int kBufs = BM <= 64 ? 8 : 4;     // tensor-memory accumulator buffers
-    static constexpr int kCols = kBufs * BM <= 32 ? 32 : kBufs * BM <= 64 ? 64
-                               : kBufs * BM <= 128 ? 128 : kBufs * BM <= 256 ? 256 : 512;
+    static constexpr int kWBytes = 128 * 128;          // one 128x128 E4M3 weight tile
+    static constexpr int kABytes = BM * 128;           // one block_m x 128 activation tile
+    static constexpr int kKps = 2;                     // K-blocks per pipeline stage
+    static constexpr int kStage = kKps * (kWBytes + kABytes);  // multiple of 1024
+    static constexpr int kStages = BM <= 16 ? 5 : BM <= 64 ? 4 : 3;
+    static constexpr int kTSlots = BM <= 64 ? 4 : 2;   // tensor-memory slots of kKps accumulators
+    static constexpr int kSlotCols = kKps * BM;
+    static constexpr int kCols = kTSlots * kSlotCols <= 32 ? 32 : kTSlots * kSlotCols <= 64 ? 64
+                               : kTSlots * kSlotCols <= 128 ? 128 : kTSlots * kSlotCols <= 256 ? 256 : 512;
     // descriptor ring
-    static constexpr int kCK = 2048 / BM;              // K-blocks per descriptor chunk
+    static constexpr int kCK = 2048 / BM;              // K-blocks per descriptor chunk (even)
     static constexpr int kRing = 3;
     static constexpr int kDescHdr = 8;                 // ints: e, b, nt, sp, kb0, nck, flags, -
     static constexpr int kDescInts = kDescHdr + BM + kCK + kCK * BM;  // hdr, rows, sw, sa
@@ -77,7 +79,8 @@ struct Cfg {
     static constexpr int kSmem = kStages * kStage + kRing * kDescBytes + kBarBytes + 1024;
     static constexpr int kThreads = 224;
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
-    static_assert(kBufs * BM <= 512, "tensor memory holds 512 fp32 columns");
+    static_assert(kTSlots * kSlotCols <= 512, "tensor memory holds 512 fp32 columns");
+    static_assert(kCK % kKps == 0, "chunks hold whole stages");
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -125,8 +128,8 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kRing * C::kDescBytes);
     uint64_t* empty = full + C::kStages;
     uint64_t* tfull = empty + C::kStages;
-    uint64_t* tempty = tfull + C::kBufs;
-    uint64_t* dfull = tempty + C::kBufs;
+    uint64_t* tempty = tfull + C::kTSlots;
+    uint64_t* dfull = tempty + C::kTSlots;
     uint64_t* dempty = dfull + C::kRing;
     uint64_t* mma_done = dempty + C::kRing;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(224, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
-        for (int i = 0; i < C::kBufs; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
+        for (int i = 0; i < C::kTSlots; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
         for (int i = 0; i < C::kRing; ++i) { mbar_init(dfull + i, 32); mbar_init(dempty + i, 130); }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(224, 1)
                         rows[t] = row;
                     }
                     const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB + c0;
-                    ok = mbar_wait(dempty + slot, ph ^ 1u, abort_flag, p.status);
+                    ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                     Desc d = desc_at<BM>(ring, slot);
                     if (lane == 0) {
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(224, 1)
             uint32_t ph = 0, dph = 0;
             long long issued = 0;
             for (;;) {
-                if (!mbar_wait(dfull + slot, dph, abort_flag, p.status)) break;
+                if (!mbar_wait_fast(dfull + slot, dph, abort_flag, p.status)) break;
                 const Desc d = desc_at<BM>(ring, slot);
                 const int flags = d.hdr[6];
                 if (flags & kEnd) break;
@@ -267,15 +270,22 @@ __global__ void __launch_bounds__(224, 1)
                 const long long wrow = p.w_tiled ? (static_cast<long long>(e) * p.NT + nt) * p.KB * 128
                                                  : static_cast<long long>(e) * p.N_out + nt * 128;
                 bool ok = true;
-                for (int kb = c0; kb < c0 + nck; ++kb) {
-                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                for (int kb = c0; kb < c0 + nck; kb += C::kKps) {
+                    const int nk = min(C::kKps, c0 + nck - kb);
+                    if (!mbar_wait_fast(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t* st = smem + s * C::kStage;
-                    mbar_arrive_expect_tx(full + s, C::kStage);
-                    if (p.w_tiled)
-                        tma_load_2d(st, &tmap_w, full + s, 0, static_cast<int>(wrow + kb * 128), pol_w);
-                    else
-                        tma_load_2d(st, &tmap_w, full + s, kb * 128, static_cast<int>(wrow), pol_w);
-                    tma_load_2d(st + C::kWBytes, &tmap_a, full + s, kb * 128, b * BM, pol_a);
+                    mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(nk * (C::kWBytes + C::kABytes)));
+                    for (int j = 0; j < nk; ++j) {
+                        if (p.w_tiled)
+                            tma_load_2d(st + j * C::kWBytes, &tmap_w, full + s, 0,
+                                        static_cast<int>(wrow + (kb + j) * 128), pol_w);
+                        else
+                            tma_load_2d(st + j * C::kWBytes, &tmap_w, full + s, (kb + j) * 128,
+                                        static_cast<int>(wrow), pol_w);
+                    }
+                    for (int j = 0; j < nk; ++j)
+                        tma_load_2d(st + C::kKps * C::kWBytes + j * C::kABytes, &tmap_a, full + s,
+                                    (kb + j) * 128, b * BM, pol_a);
                     ++issued;
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
@@ -295,10 +305,10 @@ __global__ void __launch_bounds__(224, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f8_f32(128, BM);
-            int s = 0, tb = 0, slot = 0;
+            int s = 0, ts = 0, slot = 0;
             uint32_t ph = 0, tph = 0, dph = 0;
             for (;;) {
-                if (!mbar_wait(dfull + slot, dph, abort_flag, p.status)) break;
+                if (!mbar_wait_fast(dfull + slot, dph, abort_flag, p.status)) break;
                 const Desc d = desc_at<BM>(ring, slot);
                 const int flags = d.hdr[6];
                 if (flags & kEnd) break;
@@ -306,21 +316,24 @@ __global__ void __launch_bounds__(224, 1)
                 mbar_arrive(dempty + slot);
                 if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
                 bool ok = true;
-                for (int kk = 0; kk < nck; ++kk) {
-                    if (!mbar_wait(tempty + tb, tph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    if (!mbar_wait(full + s, ph, abort_flag, p.status)) { ok = false; break; }
+                for (int kk = 0; kk < nck; kk += C::kKps) {
+                    const int nk = min(C::kKps, nck - kk);
+                    if (!mbar_wait_fast(tempty + ts, tph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (!mbar_wait_fast(full + s, ph, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t dt = tmem_base + static_cast<uint32_t>(tb * BM);
                     const uint32_t wa = smem_u32(smem + s * C::kStage);
-                    const uint32_t aa = wa + C::kWBytes;
+                    const uint32_t aa = wa + C::kKps * C::kWBytes;
+                    const uint32_t dt = tmem_base + static_cast<uint32_t>(ts * C::kSlotCols);
+                    for (int j = 0; j < nk; ++j) {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_f8(dt, smem_desc_sw128(wa + ks * 32), smem_desc_sw128(aa + ks * 32), idesc,
-                               ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_f8(dt + j * BM, smem_desc_sw128(wa + j * C::kWBytes + ks * 32),
+                                   smem_desc_sw128(aa + j * C::kABytes + ks * 32), idesc, ks > 0 ? 1u : 0u);
+                    }
                     mma_commit(empty + s);
-                    mma_commit(tfull + tb);
+                    mma_commit(tfull + ts);
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
-                    if (++tb == C::kBufs) { tb = 0; tph ^= 1u; }
+                    if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
                 }
                 if (!ok) break;
             }
@@ -335,13 +348,13 @@ __global__ void __launch_bounds__(224, 1)
         const int q = warp & 3;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         const int r_in_tile = q * 32 + lane;
-        int tb = 0, slot = 0;
+        int ts = 0, slot = 0;
         uint32_t tph = 0, dph = 0;
         float acc[BM];
 #pragma unroll
         for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
         for (;;) {
-            bool ok = mbar_wait(dfull + slot, dph, abort_flag, p.status);
+            bool ok = mbar_wait_fast(dfull + slot, dph, abort_flag, p.status);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             const Desc d = desc_at<BM>(ring, slot);
             const int flags = d.hdr[6];
@@ -351,67 +364,52 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
                 for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
             }
-            int kk = 0;
-            if (BM == 16) {
-                // two K-blocks per tensor-memory wait
-                for (; kk + 1 < nck; kk += 2) {
-                    const int tb1 = tb + 1 == C::kBufs ? 0 : tb + 1;
-                    const uint32_t tph1 = tb + 1 == C::kBufs ? (tph ^ 1u) : tph;
-                    ok = mbar_wait(tfull + tb, tph, abort_flag, p.status) &&
-                         mbar_wait(tfull + tb1, tph1, abort_flag, p.status);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
-                    tc_fence_after();
-                    float v[32];
-                    tmem_ld16x2(lane_base + static_cast<uint32_t>(tb * BM),
-                                lane_base + static_cast<uint32_t>(tb1 * BM), v);
-                    tc_fence_before();
-                    mbar_arrive(tempty + tb);
-                    mbar_arrive(tempty + tb1);
-                    const float sw0 = d.sw[kk], sw1 = d.sw[kk + 1];
-                    const float4* sa0 = reinterpret_cast<const float4*>(d.sa + kk * BM);
-                    const float4* sa1 = reinterpret_cast<const float4*>(d.sa + (kk + 1) * BM);
-#pragma unroll
-                    for (int j4 = 0; j4 < BM / 4; ++j4) {
-                        const float4 a0 = sa0[j4], a1 = sa1[j4];
-                        const float s0[4] = {a0.x, a0.y, a0.z, a0.w};
-                        const float s1[4] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int j = j4 * 4 + i;
-                            acc[j] = __fmaf_rn(v[j], __fmul_rn(s0[i], sw0), acc[j]);
-                            acc[j] = __fmaf_rn(v[16 + j], __fmul_rn(s1[i], sw1), acc[j]);
-                        }
-                    }
-                    tb = tb1 + 1 == C::kBufs ? 0 : tb1 + 1;
-                    tph = tb1 + 1 == C::kBufs ? (tph1 ^ 1u) : tph1;
-                }
-            }
-            for (; kk < nck; ++kk) {
-                ok = mbar_wait(tfull + tb, tph, abort_flag, p.status);
+            for (int kk = 0; kk < nck; kk += C::kKps) {
+                const int nk = min(C::kKps, nck - kk);
+                ok = mbar_wait_fast(tfull + ts, tph, abort_flag, p.status);
                 if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
                 tc_fence_after();
-                const float sw = d.sw[kk];
-                const float* sa = d.sa + kk * BM;
+                const uint32_t t0 = lane_base + static_cast<uint32_t>(ts * C::kSlotCols);
                 if (BM == 16) {
-                    float v[16];
-                    tmem_ld16(lane_base + static_cast<uint32_t>(tb * BM), v);
+                    // both K-blocks of the stage: 32 adjacent columns, one load and one wait
+                    float v[32];
+                    tmem_ld32(t0, v);
                     tc_fence_before();
-                    mbar_arrive(tempty + tb);
+                    mbar_arrive(tempty + ts);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[j] = __fmaf_rn(v[j], __fmul_rn(sa[j], sw), acc[j]);
+                    for (int j2 = 0; j2 < 2; ++j2) {
+                        if (j2 < nk) {
+                            const float sw = d.sw[kk + j2];
+                            const float4* sa = reinterpret_cast<const float4*>(d.sa + (kk + j2) * BM);
+#pragma unroll
+                            for (int j4 = 0; j4 < BM / 4; ++j4) {
+                                const float4 a4 = sa[j4];
+                                const float sv[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int j = j4 * 4 + i;
+                                    acc[j] = __fmaf_rn(v[j2 * 16 + j], __fmul_rn(sv[i], sw), acc[j]);
+                                }
+                            }
+                        }
+                    }
                 } else {
+                    for (int j2 = 0; j2 < nk; ++j2) {
+                        const float sw = d.sw[kk + j2];
+                        const float* sa = d.sa + (kk + j2) * BM;
 #pragma unroll
-                    for (int c = 0; c < BM / 32; ++c) {
-                        float v[32];
-                        tmem_ld32(lane_base + static_cast<uint32_t>(tb * BM + c * 32), v);
+                        for (int c = 0; c < BM / 32; ++c) {
+                            float v[32];
+                            tmem_ld32(t0 + static_cast<uint32_t>(j2 * BM + c * 32), v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[c * 32 + i] = __fmaf_rn(v[i], __fmul_rn(sa[c * 32 + i], sw), acc[c * 32 + i]);
+                            for (int i = 0; i < 32; ++i)
+                                acc[c * 32 + i] = __fmaf_rn(v[i], __fmul_rn(sa[c * 32 + i], sw), acc[c * 32 + i]);
+                        }
                     }
                     tc_fence_before();
-                    mbar_arrive(tempty + tb);
+                    mbar_arrive(tempty + ts);
                 }
-                if (++tb == C::kBufs) { tb = 0; tph ^= 1u; }
+                if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
             }
             if (flags & kLast) {
                 const int n = d.hdr[2] * 128 + r_in_tile;
