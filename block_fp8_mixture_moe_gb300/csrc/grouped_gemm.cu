@@ -10,8 +10,9 @@
 // Orientation (transposed / swap-AB): the MMA's M side is 128 weight rows (output features) of
 // one expert and its N side is the block's block_m tokens, so a decode block with one or two
 // real tokens still runs full-height MMAs and the weight tile is the A operand.  One work unit
-// is (block b, 128-row output tile, K split); a persistent grid of one CTA per SM walks the
-// units round-robin.  num_blocks is read on the device, so no work exists for inactive experts.
+// is (block b, 128-row output tile, K split); a persistent grid of one CTA per SM gives each CTA
+// a contiguous range of units (consecutive tiles of the same block).  num_blocks is read on the
+// device, so no work exists for inactive experts.
 //
 // Per CTA (224 threads, one CTA per SM):
 //   warp 6        : metadata.  Walks this CTA's units ahead of everyone else and writes, per
@@ -164,50 +165,91 @@ __global__ void __launch_bounds__(224, 1)
 
     if (warp == 6) {
         // ---------------- metadata warp ----------------
+        // This CTA owns the contiguous unit range [u_lo, u_hi): consecutive units are the
+        // output tiles (and K splits) of the same block, so a block's output rows and (short)
+        // token-scale runs are loaded once and reused; the experts and weight-block scales of
+        // the next 32 units are fetched in one round trip (lane l: unit u + l).
         int nblk = __ldg(p.num_blocks);
         nblk = max(0, min(nblk, p.B_cap));
         const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
+        const long long u_lo = units * blockIdx.x / gridDim.x;
+        const long long u_hi = units * (blockIdx.x + 1) / gridDim.x;
+        constexpr int kSwPre = 4;    // weight-block scales prefetched per unit when a unit has <= 4
+        constexpr int kSaCache = 2;  // token scales kept in registers (64 values) across units
         int slot = 0;
         uint32_t ph = 0;
         bool ok = true;
-        long long u = blockIdx.x;
-        while (u < units && ok) {
-            // the experts of this CTA's next 32 units in one round trip (lane l: unit u + l*grid)
+        int cached_b = -1, cached_c0 = -1, cached_nck = -1;
+        int rows[(BM + 31) / 32];
+        float sa_reg[kSaCache];
+#pragma unroll
+        for (int t = 0; t < (BM + 31) / 32; ++t) rows[t] = -1;
+#pragma unroll
+        for (int q = 0; q < kSaCache; ++q) sa_reg[q] = 0.0f;
+        long long u = u_lo;
+        while (u < u_hi && ok) {
             int e_lane = -1;
+            float sw_lane[kSwPre];
+#pragma unroll
+            for (int q = 0; q < kSwPre; ++q) sw_lane[q] = 0.0f;
             {
-                const long long ul = u + static_cast<long long>(lane) * gridDim.x;
-                if (ul < units) {
+                const long long ul = u + lane;
+                if (ul < u_hi) {
                     int b_l, nt_l, sp_l, k0_l, k1_l;
                     decode_unit(p, ul, b_l, nt_l, sp_l, k0_l, k1_l);
                     const int e_raw = __ldg(p.block_expert + b_l);
                     e_lane = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
+                    if (e_lane >= 0 && k1_l - k0_l <= kSwPre) {
+                        const float* wsc = p.w_s + (static_cast<long long>(e_lane) * p.NT + nt_l) * p.KB + k0_l;
+#pragma unroll
+                        for (int q = 0; q < kSwPre; ++q)
+                            if (q < k1_l - k0_l) sw_lane[q] = __ldg(wsc + q);
+                    }
                 }
             }
-            for (int i = 0; i < 32 && u < units && ok; ++i, u += gridDim.x) {
+            for (int i = 0; i < 32 && u < u_hi && ok; ++i, ++u) {
                 const int e = __shfl_sync(0xFFFFFFFFu, e_lane, i);
+                float sw_u[kSwPre];
+#pragma unroll
+                for (int q = 0; q < kSwPre; ++q) sw_u[q] = __shfl_sync(0xFFFFFFFFu, sw_lane[q], i);
                 if (e < 0) continue;  // not a block of a local expert: no work anywhere
                 int b, nt, sp, kb0, kb1;
                 decode_unit(p, u, b, nt, sp, kb0, kb1);
                 for (int c0 = kb0; c0 < kb1; c0 += C::kCK) {
                     const int nck = min(C::kCK, kb1 - c0);
-                    // the loads do not depend on the ring slot: issue them before waiting on it
-                    int rows[(BM + 31) / 32];
+                    const int n_sa = nck * BM;
+                    const bool sa_cached = n_sa <= 32 * kSaCache;
+                    if (b != cached_b) {
 #pragma unroll
-                    for (int t = 0; t < (BM + 31) / 32; ++t) {
-                        const int j = t * 32 + lane;
-                        int row = -1;
-                        if (j < BM) {
-                            const int slot_j = b * BM + j;
-                            const int r = __ldg(p.sorted_idx + slot_j);
-                            row = r < 0 ? -1 : (p.scatter ? r : slot_j);
-                            if (row >= p.out_rows) {
-                                if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
-                                row = -1;
+                        for (int t = 0; t < (BM + 31) / 32; ++t) {
+                            const int j = t * 32 + lane;
+                            int row = -1;
+                            if (j < BM) {
+                                const int slot_j = b * BM + j;
+                                const int r = __ldg(p.sorted_idx + slot_j);
+                                row = r < 0 ? -1 : (p.scatter ? r : slot_j);
+                                if (row >= p.out_rows) {
+                                    if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                                    row = -1;
+                                }
                             }
+                            rows[t] = row;
                         }
-                        rows[t] = row;
                     }
-                    const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB + c0;
+                    if (sa_cached && (b != cached_b || c0 != cached_c0 || nck != cached_nck)) {
+#pragma unroll
+                        for (int q = 0; q < kSaCache; ++q) {
+                            const int i2 = q * 32 + lane;
+                            const int kk = i2 / BM, j = i2 - kk * BM;
+                            sa_reg[q] = i2 < n_sa
+                                ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk) : 0.0f;
+                        }
+                        cached_c0 = c0;
+                        cached_nck = nck;
+                    } else if (!sa_cached) {
+                        cached_c0 = -1;
+                    }
+                    cached_b = b;
                     ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                     Desc d = desc_at<BM>(ring, slot);
@@ -219,21 +261,36 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
                     for (int t = 0; t < (BM + 31) / 32; ++t)
                         if (t * 32 + lane < BM) d.rows[t * 32 + lane] = rows[t];
-                    for (int kk = lane; kk < nck; kk += 32) d.sw[kk] = __ldg(wsc + kk);
-                    // token scales, 8 loads in flight per lane
-                    const int n_sa = nck * BM;
-                    for (int i0 = 0; i0 < n_sa; i0 += 256) {
-                        float v[8];
+                    if (kb1 - kb0 <= kSwPre) {
+                        float v = sw_u[0];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int i = i0 + q * 32 + lane;
-                            const int kk = i / BM, j = i - kk * BM;
-                            v[q] = i < n_sa ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk) : 0.0f;
+                        for (int q = 1; q < kSwPre; ++q) if (lane == q) v = sw_u[q];
+                        if (lane < nck) d.sw[lane] = v;
+                    } else {
+                        const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB + c0;
+                        for (int kk = lane; kk < nck; kk += 32) d.sw[kk] = __ldg(wsc + kk);
+                    }
+                    if (sa_cached) {
+#pragma unroll
+                        for (int q = 0; q < kSaCache; ++q) {
+                            const int i2 = q * 32 + lane;
+                            if (i2 < n_sa) d.sa[i2] = sa_reg[q];
                         }
+                    } else {
+                        // long chunks: 8 loads in flight per lane
+                        for (int i0 = 0; i0 < n_sa; i0 += 256) {
+                            float v8[8];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int i = i0 + q * 32 + lane;
-                            if (i < n_sa) d.sa[i] = v[q];
+                            for (int q = 0; q < 8; ++q) {
+                                const int i2 = i0 + q * 32 + lane;
+                                const int kk = i2 / BM, j = i2 - kk * BM;
+                                v8[q] = i2 < n_sa ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk) : 0.0f;
+                            }
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const int i2 = i0 + q * 32 + lane;
+                                if (i2 < n_sa) d.sa[i2] = v8[q];
+                            }
                         }
                     }
                     mbar_arrive(dfull + slot);
@@ -243,7 +300,7 @@ __global__ void __launch_bounds__(224, 1)
         }
         if (ok) {
             // end marker
-            ok = mbar_wait(dempty + slot, ph ^ 1u, abort_flag, p.status);
+            ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
             if (__all_sync(0xFFFFFFFFu, ok)) {
                 if (lane == 0) desc_at<BM>(ring, slot).hdr[6] = kEnd;
                 mbar_arrive(dfull + slot);
