@@ -65,14 +65,14 @@ struct Cfg {
     static constexpr int kABytes = BM * 128;           // one block_m x 128 activation tile
     static constexpr int kKps = 2;                     // K-blocks per pipeline stage
     static constexpr int kStage = kKps * (kWBytes + kABytes);  // multiple of 1024
-    static constexpr int kStages = BM <= 16 ? 5 : BM <= 64 ? 4 : 3;
+    static constexpr int kStages = BM <= 32 ? 5 : BM <= 64 ? 4 : 3;
     static constexpr int kTSlots = BM <= 64 ? 4 : 2;   // tensor-memory slots of kKps accumulators
     static constexpr int kSlotCols = kKps * BM;
     static constexpr int kCols = kTSlots * kSlotCols <= 32 ? 32 : kTSlots * kSlotCols <= 64 ? 64
                                : kTSlots * kSlotCols <= 128 ? 128 : kTSlots * kSlotCols <= 256 ? 256 : 512;
     // descriptor ring
-    static constexpr int kCK = 2048 / BM;              // K-blocks per descriptor chunk (even)
-    static constexpr int kRing = 3;
+    static constexpr int kCK = 512 / BM < 2 ? 2 : 512 / BM;  // K-blocks per descriptor chunk
+    static constexpr int kRing = 8;                    // descriptors in flight
     static constexpr int kDescHdr = 8;                 // ints: e, b, nt, sp, kb0, nck, flags, -
     static constexpr int kDescInts = kDescHdr + BM + kCK + kCK * BM;  // hdr, rows, sw, sa
     static constexpr int kDescBytes = ((kDescInts * 4) + 15) / 16 * 16;
