@@ -56,7 +56,26 @@ __device__ __forceinline__ void load8(const AQArgs& p, long long off, float* v) 
         float4 a = __ldg(reinterpret_cast<const float4*>(base));
         float4 b = __ldg(reinterpret_cast<const float4*>(base) + 1);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        for (int s = 1; s < p.in_splits; ++s) {
+        // splits 1.. in groups of four: the eight loads of a group are issued together, the
+        // additions still run strictly in split order
+        int s = 1;
+        for (; s + 3 < p.in_splits; s += 4) {
+            float4 c[4], d[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float* q = base + (s + t) * p.split_stride;
+                c[t] = __ldg(reinterpret_cast<const float4*>(q));
+                d[t] = __ldg(reinterpret_cast<const float4*>(q) + 1);
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                v[0] = __fadd_rn(v[0], c[t].x); v[1] = __fadd_rn(v[1], c[t].y);
+                v[2] = __fadd_rn(v[2], c[t].z); v[3] = __fadd_rn(v[3], c[t].w);
+                v[4] = __fadd_rn(v[4], d[t].x); v[5] = __fadd_rn(v[5], d[t].y);
+                v[6] = __fadd_rn(v[6], d[t].z); v[7] = __fadd_rn(v[7], d[t].w);
+            }
+        }
+        for (; s < p.in_splits; ++s) {
             const float* q = base + s * p.split_stride;
             float4 c = __ldg(reinterpret_cast<const float4*>(q));
             float4 d = __ldg(reinterpret_cast<const float4*>(q) + 1);

@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(224, 1)
                     float v[32];
                     tmem_ld32(t0, v);
                     tc_fence_before();
-                    mbar_arrive(tempty + ts);
+                    mbar_arrive_relaxed(tempty + ts);
 #pragma unroll
                     for (int j2 = 0; j2 < 2; ++j2) {
                         if (j2 < nk) {
@@ -464,28 +464,41 @@ __global__ void __launch_bounds__(224, 1)
                         }
                     }
                     tc_fence_before();
-                    mbar_arrive(tempty + ts);
+                    mbar_arrive_relaxed(tempty + ts);
                 }
                 if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
             }
             if (flags & kLast) {
                 const int n = d.hdr[2] * 128 + r_in_tile;
                 const int sp = d.hdr[3];
+                // row indices are read into registers 16 at a time before the stores, so no
+                // shared-memory load is ordered between global stores through generic pointers
 #pragma unroll
-                for (int j = 0; j < BM; ++j) {
-                    const int row = d.rows[j];
-                    if (row < 0) continue;
-                    if (p.out_f32) {
-                        float* o = static_cast<float*>(p.out);
-                        o[(static_cast<long long>(sp) * p.out_rows + row) * p.N_out + n] = acc[j];
-                    } else {
-                        uint16_t* o = static_cast<uint16_t*>(p.out);
-                        o[static_cast<long long>(row) * p.N_out + n] =
-                            static_cast<uint16_t>(f32_to_bf16_bits(acc[j]));
+                for (int j0 = 0; j0 < BM; j0 += 16) {
+                    int rws[16];
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const int4 r4 = reinterpret_cast<const int4*>(d.rows + j0)[j4];
+                        rws[j4 * 4 + 0] = r4.x; rws[j4 * 4 + 1] = r4.y;
+                        rws[j4 * 4 + 2] = r4.z; rws[j4 * 4 + 3] = r4.w;
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int row = rws[jj];
+                        if (row < 0) continue;
+                        const int j = j0 + jj;
+                        if (p.out_f32) {
+                            float* o = static_cast<float*>(p.out);
+                            o[(static_cast<long long>(sp) * p.out_rows + row) * p.N_out + n] = acc[j];
+                        } else {
+                            uint16_t* o = static_cast<uint16_t*>(p.out);
+                            o[static_cast<long long>(row) * p.N_out + n] =
+                                static_cast<uint16_t>(f32_to_bf16_bits(acc[j]));
+                        }
                     }
                 }
             }
-            mbar_arrive(dempty + slot);
+            mbar_arrive_relaxed(dempty + slot);
             if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
         }
     epi_done:;
