@@ -248,6 +248,8 @@ def run_ours(args):
     # ---- the dominant kernel (gate/up GEMM) timed with events on its own stream -------------
     gemm_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_use, wgu_s,
                                   M, H, N, E, k, args.steps, args.warmup)
+    padded_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_use, wgu_s,
+                                    M, H, N, E, k, min(args.steps, 100), args.warmup, padded=True)
     other = wgu_q if args.weights == "tiled" else ops.moe_blockfp8_pack_weights(wgu_q)
     gemm_other_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, other, wgu_s,
                                         M, H, N, E, k, min(args.steps, 200), args.warmup)
@@ -313,7 +315,8 @@ def run_ours(args):
                      "algorithmic_bytes": int(gu_mean_bytes),
                      "kernel_us": round(statistics.mean(gemm_ms) * 1e3, 2),
                      "weights": args.weights, "peak_source": peak_src,
-                     "other_layout_kernel_us": round(statistics.mean(gemm_other_ms) * 1e3, 2)},
+                     "other_layout_kernel_us": round(statistics.mean(gemm_other_ms) * 1e3, 2),
+                     "padded_grid_kernel_us": round(statistics.mean(padded_ms) * 1e3, 2)},
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -328,10 +331,30 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def padded_grid_route(route, E, bm, dev):
+    """The schedule before active-expert dispatch: one block per expert, every expert's weights
+    streamed whether or not it received routes (lmdeploy PR #4956, "Motivation").  Built from
+    the compact route table with torch ops at setup time."""
+    import torch
+    si = route["sorted_idx"].cpu()
+    be = route["block_expert"].cpu()
+    nb = int(route["num_blocks"].item())
+    assert nb <= E, "padded-grid arm assumes at most block_m routes per expert"
+    B_cap = E
+    sorted_idx = torch.full((B_cap * bm,), -1, dtype=torch.int32)
+    for b in range(nb):
+        e = int(be[b])
+        sorted_idx[e * bm:(e + 1) * bm] = si[b * bm:(b + 1) * bm]
+    return dict(sorted_idx=sorted_idx.to(dev), block_expert=torch.arange(E, dtype=torch.int32, device=dev),
+                num_blocks=torch.tensor([E], dtype=torch.int32, device=dev), B_cap=B_cap,
+                route_slot=None, moved=True)
+
+
 def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, M, H, N,
-                        E, k, steps, warmup):
+                        E, k, steps, warmup, padded=False):
     """The layer's stages launched one by one through the per-stage entry points, with events
-    around the gate/up GEMM only; returns its per-launch device times (ms)."""
+    around the gate/up GEMM only; returns its per-launch device times (ms).  padded=True times
+    the padded-grid schedule (every expert's weights) on the same activations."""
     import torch
     bm, B_cap, splits = ops.moe_blockfp8_plan(M, k, E, E, H, N)
     slots = B_cap * bm
@@ -344,6 +367,13 @@ def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, M, H
             route = ops.moe_route_prepare(ids[r], E, None, E, bm, stream=stream)
             routes.append(route)
         torch.cuda.synchronize()
+    if padded:
+        # the padded grid reads activations from slot e*bm + i: scatter the quantised rows there
+        slots_p = E * bm
+        xq_p = torch.zeros((max(slots, slots_p), H), dtype=torch.uint8, device=dev)
+        xs_p = torch.ones((max(slots, slots_p), H // 128), dtype=torch.float32, device=dev)
+        gu_p = torch.empty((splits, max(slots, slots_p), 2 * N), dtype=torch.float32, device=dev)
+        proutes = [padded_grid_route(rt, E, bm, dev) for rt in routes]
     times = []
     with torch.cuda.stream(stream):
         for i in range(warmup + steps):
@@ -355,8 +385,13 @@ def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, M, H
             torch.cuda._sleep(2_000_000)  # keep the device busy while the host enqueues
             e0, e1 = make_event(), make_event()
             e0.record(stream)
-            ops.moe_blockfp8_grouped_gemm(0, xq, xsc, wgu_q, wgu_s, route, bm, out_dtype=ops.DTYPE_F32,
-                                          out_rows=slots, splits=splits, out=gu, stream=stream)
+            if padded:
+                ops.moe_blockfp8_grouped_gemm(0, xq_p, xs_p, wgu_q, wgu_s, proutes[r], bm,
+                                              out_dtype=ops.DTYPE_F32, out_rows=xq_p.shape[0],
+                                              splits=splits, out=gu_p, stream=stream)
+            else:
+                ops.moe_blockfp8_grouped_gemm(0, xq, xsc, wgu_q, wgu_s, route, bm, out_dtype=ops.DTYPE_F32,
+                                              out_rows=slots, splits=splits, out=gu, stream=stream)
             e1.record(stream)
             if i >= warmup:
                 times.append((e0, e1))

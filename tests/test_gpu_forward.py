@@ -59,15 +59,26 @@ def test_decode_full_size(ops, M):
     assert_bf16_close(got, ref, f"decode M={M}")
 
 
-@pytest.mark.parametrize("T", [1, 10, 100])
+@pytest.mark.parametrize("T", wl.EP_TOKENS)
 def test_expert_parallel_slice(ops, T):
     """k=6 of E=256 with 32 local experts through an expert map; non-local routes are dropped
-    in every stage and add nothing to the output."""
+    in every stage and add nothing to the output (T=1024 tokens = 6144 routed rows is compared
+    on a 48-token sample, including tokens with no local route)."""
     cfg = dict(wl.CONFIGS["ep"], M=T)
     L = wl.make_layer(**cfg, seed=2, device="cuda")
-    got = _run(ops, L, clamp=7.0, fmt=1)
-    ref = oracle.moe_forward(_host(L), clamp_limit=7.0, fmt=1)
-    assert_bf16_close(got, ref, f"ep T={T}")
+    got = _run(ops, L, clamp=7.0, fmt=1, tiled=(T >= 100))
+    if T <= 100:
+        ref = oracle.moe_forward(_host(L), clamp_limit=7.0, fmt=1)
+        assert_bf16_close(got, ref, f"ep T={T}")
+    else:
+        toks = np.random.default_rng(T).choice(T, 48, replace=False)
+        ref = oracle.moe_forward(_host(L, toks), clamp_limit=7.0, fmt=1, tokens=toks)
+        assert_bf16_close(got[toks], ref[toks], f"ep T={T} sample")
+        # a token none of whose routes is local gets exactly zero
+        emap = L["expert_map"]
+        none_local = [t for t in range(T) if (emap[L["topk_ids"][t]] < 0).all()]
+        if none_local:
+            assert (oracle.bf16_to_f32(got[none_local]) == 0).all()
 
 
 def test_prefill_zipf_sampled(ops):
