@@ -8,7 +8,8 @@ activation scales.  Inputs are seeded and synthetic; weights are random (no chec
 One step = one whole layer forward (route preparation, input quantisation, gate/up GEMM,
 fused SiLU*mul + quantisation, down GEMM, moe_reduce) through moe_blockfp8_forward, replayed
 from a CUDA graph.  Eight routing batches rotate between steps and a 256 MiB buffer is written
-between timed steps (outside the events) so no step starts with its weights in L2.
+and then read back between timed steps (outside the events), so no step starts with its
+weights in L2 and no dirty line of the flush is written back inside the timed region.
 
 Prints one JSON line.  --impl reference times the CPU oracle instead (a bounded token sample
 per step, scaled to the layer latency).
@@ -175,18 +176,27 @@ def make_event(external=False):
         return torch.cuda.Event(enable_timing=True)
 
 
+def flush_l2(flush):
+    """Evicts the previous step's data from L2 (129 MB): writes a 256 MiB buffer, then reads it
+    back, so the dirty lines of the write are written back here, outside the timed region, and
+    the next step starts with a clean L2 that holds none of its weights."""
+    import torch
+    flush.zero_()
+    flush.view(torch.float32).sum()
+
+
 def time_graph_steps(graphs, steps, warmup, flush, stream):
     """Per-step device time (ms) of graph replays, L2 flushed between steps (outside events)."""
     import torch
     times = []
     with torch.cuda.stream(stream):
         for i in range(warmup):
-            flush.zero_()
+            flush_l2(flush)
             graphs[i % len(graphs)].replay()
         torch.cuda.synchronize()
         evs = [(make_event(), make_event()) for _ in range(steps)]
         for i in range(steps):
-            flush.zero_()
+            flush_l2(flush)
             evs[i][0].record(stream)
             graphs[i % len(graphs)].replay()
             evs[i][1].record(stream)
@@ -301,7 +311,7 @@ def run_ours(args):
         "config": {"workload": f"decode MoE layer M={M} H={H} N={N} E={E} top-k={k}, block-FP8 128x128",
                    "M": M, "H": H, "N": N, "E": E, "topk": k, "block_m": bm, "gate_up_splits": splits,
                    "weights": args.weights,
-                   "l2": "256 MiB buffer written between timed steps (outside the events); 8 rotating routing batches",
+                   "l2": "256 MiB buffer written then read back between timed steps (outside the events); 8 rotating routing batches",
                    "timing": "CUDA graph replay per step, CUDA events per step", "parallelism": f"replicas x{world}"},
         "layer_hbm": {"GBps": round(mean_bytes / (layer_us * 1e-6) / 1e9, 1),
                       "frac": round(mean_bytes / (layer_us * 1e-6) / 1e9 / hbm_peak, 4),
@@ -381,7 +391,7 @@ def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, M, H
             route = routes[r]
             ops.silu_mul_quant_fp8(0, xs[r], H, rows=M * k, row_map=route["route_slot"], row_div=k,
                                    out_rows=slots, out_q=xq, out_s=xsc, stream=stream)
-            flush.zero_()
+            flush_l2(flush)
             torch.cuda._sleep(2_000_000)  # keep the device busy while the host enqueues
             e0, e1 = make_event(), make_event()
             e0.record(stream)
@@ -413,7 +423,7 @@ def time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, steps, warmup):
     with torch.cuda.stream(stream):
         for i in range(warmup + steps):
             r = i % NROT
-            flush.zero_()
+            flush_l2(flush)
             e0, e1 = make_event(), make_event()
             e0.record(stream)
             xs[r].copy_(hx[r], non_blocking=True)

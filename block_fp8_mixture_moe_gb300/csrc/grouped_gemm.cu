@@ -71,28 +71,36 @@ struct Cfg {
     static constexpr int kCols = kTSlots * kSlotCols <= 32 ? 32 : kTSlots * kSlotCols <= 64 ? 64
                                : kTSlots * kSlotCols <= 128 ? 128 : kTSlots * kSlotCols <= 256 ? 256 : 512;
     // descriptor ring
-    static constexpr int kCK = 512 / BM < 2 ? 2 : 512 / BM;  // K-blocks per descriptor chunk
+    static constexpr int kCK = 512 / BM < 2 ? 2 : 512 / BM;  // K-blocks per descriptor
+    static constexpr int kSwMax = 64;                  // weight-block scales per descriptor
     static constexpr int kRing = 8;                    // descriptors in flight
-    static constexpr int kDescHdr = 8;                 // ints: e, b, nt, sp, kb0, nck, flags, -
-    static constexpr int kDescInts = kDescHdr + BM + kCK + kCK * BM;  // hdr, rows, sw, sa
+    static constexpr int kDescHdr = 8;                 // ints: e, b, nt0, ntl, sp, kb0, nck, flags
+    static constexpr int kDescInts = kDescHdr + BM + kCK * BM + kSwMax;  // hdr, rows, sa, sw
     static constexpr int kDescBytes = ((kDescInts * 4) + 15) / 16 * 16;
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmem = kStages * kStage + kRing * kDescBytes + kBarBytes + 1024;
     static constexpr int kThreads = 224;
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kTSlots * kSlotCols <= 512, "tensor memory holds 512 fp32 columns");
-    static_assert(kCK % kKps == 0, "chunks hold whole stages");
+    static_assert(kCK % kKps == 0, "descriptors hold whole stages");
+    static_assert(kCK * BM == 512, "token-scale area of a descriptor is 512 values");
+    static_assert(((kDescHdr + BM) * 4) % 16 == 0, "token scales stay 16-byte aligned");
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-// descriptor flags
+// descriptor flags: the descriptor starts / ends each of its tiles' K range
 constexpr int kFirst = 1, kLast = 2, kEnd = 4;
 
+// One descriptor: ntl consecutive output tiles nt0.. of block b (expert e), split sp, over the
+// K-blocks [kb0, kb0 + nck).  rows[j]: output row of slot j (-1: pad or dropped);
+// sa[kk * BM + j]: token scale of slot j at K-block kb0 + kk; sw[t * nck + kk]: weight-block
+// scale of tile nt0 + t at K-block kb0 + kk.  A descriptor with ntl > 1 covers each tile's
+// whole K range (kFirst | kLast).
 struct Desc {
     int* hdr;
     int* rows;
+    float* sa;
     float* sw;
-    float* sa;  // [kCK][BM]
 };
 
 template <int BM>
@@ -102,19 +110,9 @@ __device__ __forceinline__ Desc desc_at(uint8_t* ring, int slot) {
     Desc d;
     d.hdr = base;
     d.rows = base + C::kDescHdr;
-    d.sw = reinterpret_cast<float*>(d.rows + BM);
-    d.sa = d.sw + C::kCK;
+    d.sa = reinterpret_cast<float*>(d.rows + BM);
+    d.sw = d.sa + C::kCK * BM;
     return d;
-}
-
-__device__ __forceinline__ void decode_unit(const GemmArgs& p, long long u, int& b, int& nt,
-                                            int& sp, int& kb0, int& kb1) {
-    sp = static_cast<int>(u % p.splits);
-    const long long bt = u / p.splits;
-    nt = static_cast<int>(bt % p.NT);
-    b = static_cast<int>(bt / p.NT);
-    kb0 = static_cast<int>((static_cast<long long>(sp) * p.KB) / p.splits);
-    kb1 = static_cast<int>((static_cast<long long>(sp + 1) * p.KB) / p.splits);
 }
 
 template <int BM>
@@ -165,144 +163,118 @@ __global__ void __launch_bounds__(224, 1)
 
     if (warp == 6) {
         // ---------------- metadata warp ----------------
-        // This CTA owns the contiguous unit range [u_lo, u_hi): consecutive units are the
-        // output tiles (and K splits) of the same block, so a block's output rows and (short)
-        // token-scale runs are loaded once and reused; the experts and weight-block scales of
-        // the next 32 units are fetched in one round trip (lane l: unit u + l).
+        // Units are ordered (block, split, tile) with the tile fastest, and this CTA owns the
+        // contiguous range [u_lo, u_hi).  The range is walked incrementally: a run of tiles of
+        // the same block and split shares its rows and token scales, so one descriptor covers
+        // up to kSwMax / (K-blocks per unit) tiles; a unit longer than kCK K-blocks is cut into
+        // one descriptor per kCK K-blocks.  All loads of a descriptor are issued before any of
+        // its shared-memory stores.
         int nblk = __ldg(p.num_blocks);
         nblk = max(0, min(nblk, p.B_cap));
         const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
         const long long u_lo = units * blockIdx.x / gridDim.x;
         const long long u_hi = units * (blockIdx.x + 1) / gridDim.x;
-        constexpr int kSwPre = 4;    // weight-block scales prefetched per unit when a unit has <= 4
-        constexpr int kSaCache = 2;  // token scales kept in registers (64 values) across units
+        int nt = static_cast<int>(u_lo % p.NT);
+        int sp = static_cast<int>((u_lo / p.NT) % p.splits);
+        int b = static_cast<int>(u_lo / (static_cast<long long>(p.NT) * p.splits));
+        long long left = u_hi - u_lo;
         int slot = 0;
         uint32_t ph = 0;
         bool ok = true;
-        int cached_b = -1, cached_c0 = -1, cached_nck = -1;
+        int cur_b = -1, e = -1;
         int rows[(BM + 31) / 32];
-        float sa_reg[kSaCache];
 #pragma unroll
         for (int t = 0; t < (BM + 31) / 32; ++t) rows[t] = -1;
+        while (left > 0 && ok) {
+            if (b != cur_b) {
+                const int e_raw = __ldg(p.block_expert + b);
+                e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
+                if (e >= 0) {
 #pragma unroll
-        for (int q = 0; q < kSaCache; ++q) sa_reg[q] = 0.0f;
-        long long u = u_lo;
-        while (u < u_hi && ok) {
-            int e_lane = -1;
-            float sw_lane[kSwPre];
-#pragma unroll
-            for (int q = 0; q < kSwPre; ++q) sw_lane[q] = 0.0f;
-            {
-                const long long ul = u + lane;
-                if (ul < u_hi) {
-                    int b_l, nt_l, sp_l, k0_l, k1_l;
-                    decode_unit(p, ul, b_l, nt_l, sp_l, k0_l, k1_l);
-                    const int e_raw = __ldg(p.block_expert + b_l);
-                    e_lane = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
-                    if (e_lane >= 0 && k1_l - k0_l <= kSwPre) {
-                        const float* wsc = p.w_s + (static_cast<long long>(e_lane) * p.NT + nt_l) * p.KB + k0_l;
-#pragma unroll
-                        for (int q = 0; q < kSwPre; ++q)
-                            if (q < k1_l - k0_l) sw_lane[q] = __ldg(wsc + q);
+                    for (int t = 0; t < (BM + 31) / 32; ++t) {
+                        const int j = t * 32 + lane;
+                        int row = -1;
+                        if (j < BM) {
+                            const int slot_j = b * BM + j;
+                            const int r = __ldg(p.sorted_idx + slot_j);
+                            row = r < 0 ? -1 : (p.scatter ? r : slot_j);
+                            if (row >= p.out_rows) {
+                                if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                                row = -1;
+                            }
+                        }
+                        rows[t] = row;
                     }
                 }
+                cur_b = b;
             }
-            for (int i = 0; i < 32 && u < u_hi && ok; ++i, ++u) {
-                const int e = __shfl_sync(0xFFFFFFFFu, e_lane, i);
-                float sw_u[kSwPre];
-#pragma unroll
-                for (int q = 0; q < kSwPre; ++q) sw_u[q] = __shfl_sync(0xFFFFFFFFu, sw_lane[q], i);
-                if (e < 0) continue;  // not a block of a local expert: no work anywhere
-                int b, nt, sp, kb0, kb1;
-                decode_unit(p, u, b, nt, sp, kb0, kb1);
-                for (int c0 = kb0; c0 < kb1; c0 += C::kCK) {
+            const int run = static_cast<int>(min(static_cast<long long>(p.NT - nt), left));
+            int adv = run;
+            if (e >= 0) {
+                const int kb0 = sp * p.KB / p.splits, kb1 = (sp + 1) * p.KB / p.splits;
+                const int len = kb1 - kb0;
+                const bool whole = len <= C::kCK;
+                const int ntl = whole ? min(run, C::kSwMax / len) : 1;
+                adv = ntl;
+                for (int c0 = kb0; c0 < kb1 && ok; c0 += C::kCK) {
                     const int nck = min(C::kCK, kb1 - c0);
+                    // token scales: lane order (slot j, K-block kk) with kk fastest, so the
+                    // loads of one slot row are contiguous
+                    float sa_v[C::kCK * BM / 32];
                     const int n_sa = nck * BM;
-                    const bool sa_cached = n_sa <= 32 * kSaCache;
-                    if (b != cached_b) {
 #pragma unroll
-                        for (int t = 0; t < (BM + 31) / 32; ++t) {
-                            const int j = t * 32 + lane;
-                            int row = -1;
-                            if (j < BM) {
-                                const int slot_j = b * BM + j;
-                                const int r = __ldg(p.sorted_idx + slot_j);
-                                row = r < 0 ? -1 : (p.scatter ? r : slot_j);
-                                if (row >= p.out_rows) {
-                                    if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
-                                    row = -1;
-                                }
-                            }
-                            rows[t] = row;
-                        }
+                    for (int q = 0; q < C::kCK * BM / 32; ++q) {
+                        const int i = q * 32 + lane;
+                        const int j = i / nck, kk = i - j * nck;
+                        sa_v[q] = i < n_sa ? __ldg(p.a_s + static_cast<long long>(b * BM + j) * p.KB + c0 + kk) : 0.0f;
                     }
-                    if (sa_cached && (b != cached_b || c0 != cached_c0 || nck != cached_nck)) {
+                    float sw_v[C::kSwMax / 32];
+                    const int n_sw = ntl * nck;
 #pragma unroll
-                        for (int q = 0; q < kSaCache; ++q) {
-                            const int i2 = q * 32 + lane;
-                            const int kk = i2 / BM, j = i2 - kk * BM;
-                            sa_reg[q] = i2 < n_sa
-                                ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk) : 0.0f;
-                        }
-                        cached_c0 = c0;
-                        cached_nck = nck;
-                    } else if (!sa_cached) {
-                        cached_c0 = -1;
+                    for (int q = 0; q < C::kSwMax / 32; ++q) {
+                        const int i = q * 32 + lane;
+                        const int t = i / nck, kk = i - t * nck;
+                        sw_v[q] = i < n_sw ? __ldg(p.w_s + (static_cast<long long>(e) * p.NT + nt + t) * p.KB + c0 + kk) : 0.0f;
                     }
-                    cached_b = b;
                     ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                     Desc d = desc_at<BM>(ring, slot);
                     if (lane == 0) {
-                        d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt; d.hdr[3] = sp; d.hdr[4] = c0;
-                        d.hdr[5] = nck;
-                        d.hdr[6] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
+                        d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt; d.hdr[3] = ntl; d.hdr[4] = sp;
+                        d.hdr[5] = c0; d.hdr[6] = nck;
+                        d.hdr[7] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
                     }
 #pragma unroll
                     for (int t = 0; t < (BM + 31) / 32; ++t)
                         if (t * 32 + lane < BM) d.rows[t * 32 + lane] = rows[t];
-                    if (kb1 - kb0 <= kSwPre) {
-                        float v = sw_u[0];
 #pragma unroll
-                        for (int q = 1; q < kSwPre; ++q) if (lane == q) v = sw_u[q];
-                        if (lane < nck) d.sw[lane] = v;
-                    } else {
-                        const float* wsc = p.w_s + (static_cast<long long>(e) * p.NT + nt) * p.KB + c0;
-                        for (int kk = lane; kk < nck; kk += 32) d.sw[kk] = __ldg(wsc + kk);
+                    for (int q = 0; q < C::kCK * BM / 32; ++q) {
+                        const int i = q * 32 + lane;
+                        const int j = i / nck, kk = i - j * nck;
+                        if (i < n_sa) d.sa[kk * BM + j] = sa_v[q];
                     }
-                    if (sa_cached) {
 #pragma unroll
-                        for (int q = 0; q < kSaCache; ++q) {
-                            const int i2 = q * 32 + lane;
-                            if (i2 < n_sa) d.sa[i2] = sa_reg[q];
-                        }
-                    } else {
-                        // long chunks: 8 loads in flight per lane
-                        for (int i0 = 0; i0 < n_sa; i0 += 256) {
-                            float v8[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const int i2 = i0 + q * 32 + lane;
-                                const int kk = i2 / BM, j = i2 - kk * BM;
-                                v8[q] = i2 < n_sa ? __ldg(p.a_s + (static_cast<long long>(b) * BM + j) * p.KB + c0 + kk) : 0.0f;
-                            }
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const int i2 = i0 + q * 32 + lane;
-                                if (i2 < n_sa) d.sa[i2] = v8[q];
-                            }
-                        }
+                    for (int q = 0; q < C::kSwMax / 32; ++q) {
+                        const int i = q * 32 + lane;
+                        if (i < n_sw) d.sw[i] = sw_v[q];
                     }
                     mbar_arrive(dfull + slot);
                     if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
                 }
+            }
+            // advance by adv units (never past the end of this block and split's tile run)
+            nt += adv;
+            left -= adv;
+            if (nt == p.NT) {
+                nt = 0;
+                if (++sp == p.splits) { sp = 0; ++b; }
             }
         }
         if (ok) {
             // end marker
             ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
             if (__all_sync(0xFFFFFFFFu, ok)) {
-                if (lane == 0) desc_at<BM>(ring, slot).hdr[6] = kEnd;
+                if (lane == 0) desc_at<BM>(ring, slot).hdr[7] = kEnd;
                 mbar_arrive(dfull + slot);
             }
         }
@@ -314,39 +286,42 @@ __global__ void __launch_bounds__(224, 1)
             int s = 0, slot = 0;
             uint32_t ph = 0, dph = 0;
             long long issued = 0;
-            for (;;) {
+            bool ok = true;
+            while (ok) {
                 if (!mbar_wait_fast(dfull + slot, dph, abort_flag, p.status)) break;
                 const Desc d = desc_at<BM>(ring, slot);
-                const int flags = d.hdr[6];
+                const int flags = d.hdr[7];
                 if (flags & kEnd) break;
-                const int e = d.hdr[0], b = d.hdr[1], nt = d.hdr[2], c0 = d.hdr[4], nck = d.hdr[5];
+                const int e = d.hdr[0], b = d.hdr[1], nt0 = d.hdr[2], ntl = d.hdr[3];
+                const int c0 = d.hdr[5], nck = d.hdr[6];
                 mbar_arrive(dempty + slot);
                 if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
-                // row-major weights: box (kb*128, e*N_out + nt*128); tiled weights: every
-                // 128x128 tile is one contiguous 16 KB run at row ((e*NT + nt)*KB + kb)*128
-                const long long wrow = p.w_tiled ? (static_cast<long long>(e) * p.NT + nt) * p.KB * 128
-                                                 : static_cast<long long>(e) * p.N_out + nt * 128;
-                bool ok = true;
-                for (int kb = c0; kb < c0 + nck; kb += C::kKps) {
-                    const int nk = min(C::kKps, c0 + nck - kb);
-                    if (!mbar_wait_fast(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    uint8_t* st = smem + s * C::kStage;
-                    mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(nk * (C::kWBytes + C::kABytes)));
-                    for (int j = 0; j < nk; ++j) {
-                        if (p.w_tiled)
-                            tma_load_2d(st + j * C::kWBytes, &tmap_w, full + s, 0,
-                                        static_cast<int>(wrow + (kb + j) * 128), pol_w);
-                        else
-                            tma_load_2d(st + j * C::kWBytes, &tmap_w, full + s, (kb + j) * 128,
-                                        static_cast<int>(wrow), pol_w);
+                for (int t = 0; t < ntl && ok; ++t) {
+                    // row-major weights: box (kb*128, e*N_out + nt*128); tiled weights: every
+                    // 128x128 tile is one contiguous 16 KB run at row ((e*NT + nt)*KB + kb)*128
+                    const int nt = nt0 + t;
+                    const long long wrow = p.w_tiled ? (static_cast<long long>(e) * p.NT + nt) * p.KB * 128
+                                                     : static_cast<long long>(e) * p.N_out + nt * 128;
+                    for (int kb = c0; kb < c0 + nck; kb += C::kKps) {
+                        const int nk = min(C::kKps, c0 + nck - kb);
+                        if (!mbar_wait_fast(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                        uint8_t* st = smem + s * C::kStage;
+                        mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(nk * (C::kWBytes + C::kABytes)));
+                        for (int j = 0; j < nk; ++j) {
+                            if (p.w_tiled)
+                                tma_load_2d(st + j * C::kWBytes, &tmap_w, full + s, 0,
+                                            static_cast<int>(wrow + (kb + j) * 128), pol_w);
+                            else
+                                tma_load_2d(st + j * C::kWBytes, &tmap_w, full + s, (kb + j) * 128,
+                                            static_cast<int>(wrow), pol_w);
+                        }
+                        for (int j = 0; j < nk; ++j)
+                            tma_load_2d(st + C::kKps * C::kWBytes + j * C::kABytes, &tmap_a, full + s,
+                                        (kb + j) * 128, b * BM, pol_a);
+                        ++issued;
+                        if (++s == C::kStages) { s = 0; ph ^= 1u; }
                     }
-                    for (int j = 0; j < nk; ++j)
-                        tma_load_2d(st + C::kKps * C::kWBytes + j * C::kABytes, &tmap_a, full + s,
-                                    (kb + j) * 128, b * BM, pol_a);
-                    ++issued;
-                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
-                if (!ok) break;
             }
             if (*abort_flag) {
                 // never leave a TMA write in flight: wait for the last load of every stage
@@ -364,35 +339,36 @@ __global__ void __launch_bounds__(224, 1)
             constexpr uint32_t idesc = idesc_f8_f32(128, BM);
             int s = 0, ts = 0, slot = 0;
             uint32_t ph = 0, tph = 0, dph = 0;
-            for (;;) {
+            bool ok = true;
+            while (ok) {
                 if (!mbar_wait_fast(dfull + slot, dph, abort_flag, p.status)) break;
                 const Desc d = desc_at<BM>(ring, slot);
-                const int flags = d.hdr[6];
+                const int flags = d.hdr[7];
                 if (flags & kEnd) break;
-                const int nck = d.hdr[5];
+                const int ntl = d.hdr[3], nck = d.hdr[6];
                 mbar_arrive(dempty + slot);
                 if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
-                bool ok = true;
-                for (int kk = 0; kk < nck; kk += C::kKps) {
-                    const int nk = min(C::kKps, nck - kk);
-                    if (!mbar_wait_fast(tempty + ts, tph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    if (!mbar_wait_fast(full + s, ph, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t wa = smem_u32(smem + s * C::kStage);
-                    const uint32_t aa = wa + C::kKps * C::kWBytes;
-                    const uint32_t dt = tmem_base + static_cast<uint32_t>(ts * C::kSlotCols);
-                    for (int j = 0; j < nk; ++j) {
+                for (int t = 0; t < ntl && ok; ++t) {
+                    for (int kk = 0; kk < nck; kk += C::kKps) {
+                        const int nk = min(C::kKps, nck - kk);
+                        if (!mbar_wait_fast(tempty + ts, tph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                        if (!mbar_wait_fast(full + s, ph, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t wa = smem_u32(smem + s * C::kStage);
+                        const uint32_t aa = wa + C::kKps * C::kWBytes;
+                        const uint32_t dt = tmem_base + static_cast<uint32_t>(ts * C::kSlotCols);
+                        for (int j = 0; j < nk; ++j) {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_f8(dt + j * BM, smem_desc_sw128(wa + j * C::kWBytes + ks * 32),
-                                   smem_desc_sw128(aa + j * C::kABytes + ks * 32), idesc, ks > 0 ? 1u : 0u);
+                            for (int ks = 0; ks < 4; ++ks)
+                                mma_f8(dt + j * BM, smem_desc_sw128(wa + j * C::kWBytes + ks * 32),
+                                       smem_desc_sw128(aa + j * C::kABytes + ks * 32), idesc, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(empty + s);
+                        mma_commit(tfull + ts);
+                        if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                        if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
                     }
-                    mma_commit(empty + s);
-                    mma_commit(tfull + ts);
-                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
-                    if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
                 }
-                if (!ok) break;
             }
             // all issued MMAs complete before tensor memory is released
             mma_commit(mma_done);
@@ -414,86 +390,89 @@ __global__ void __launch_bounds__(224, 1)
             bool ok = mbar_wait_fast(dfull + slot, dph, abort_flag, p.status);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             const Desc d = desc_at<BM>(ring, slot);
-            const int flags = d.hdr[6];
+            const int flags = d.hdr[7];
             if (flags & kEnd) break;
-            const int nck = d.hdr[5];
-            if (flags & kFirst) {
+            const int nt0 = d.hdr[2], ntl = d.hdr[3], nck = d.hdr[6];
+            const int sp = d.hdr[4];
+            for (int t = 0; t < ntl; ++t) {
+                if (flags & kFirst) {
 #pragma unroll
-                for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
-            }
-            for (int kk = 0; kk < nck; kk += C::kKps) {
-                const int nk = min(C::kKps, nck - kk);
-                ok = mbar_wait_fast(tfull + ts, tph, abort_flag, p.status);
-                if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
-                tc_fence_after();
-                const uint32_t t0 = lane_base + static_cast<uint32_t>(ts * C::kSlotCols);
-                if (BM == 16) {
-                    // both K-blocks of the stage: 32 adjacent columns, one load and one wait
-                    float v[32];
-                    tmem_ld32(t0, v);
-                    tc_fence_before();
-                    mbar_arrive_relaxed(tempty + ts);
+                    for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
+                }
+                const float* swt = d.sw + t * nck;
+                for (int kk = 0; kk < nck; kk += C::kKps) {
+                    const int nk = min(C::kKps, nck - kk);
+                    ok = mbar_wait_fast(tfull + ts, tph, abort_flag, p.status);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
+                    tc_fence_after();
+                    const uint32_t t0 = lane_base + static_cast<uint32_t>(ts * C::kSlotCols);
+                    if (BM == 16) {
+                        // both K-blocks of the stage: 32 adjacent columns, one load and one wait
+                        float v[32];
+                        tmem_ld32(t0, v);
+                        tc_fence_before();
+                        mbar_arrive_relaxed(tempty + ts);
 #pragma unroll
-                    for (int j2 = 0; j2 < 2; ++j2) {
-                        if (j2 < nk) {
-                            const float sw = d.sw[kk + j2];
-                            const float4* sa = reinterpret_cast<const float4*>(d.sa + (kk + j2) * BM);
+                        for (int j2 = 0; j2 < 2; ++j2) {
+                            if (j2 < nk) {
+                                const float sw = swt[kk + j2];
+                                const float4* sa = reinterpret_cast<const float4*>(d.sa + (kk + j2) * BM);
 #pragma unroll
-                            for (int j4 = 0; j4 < BM / 4; ++j4) {
-                                const float4 a4 = sa[j4];
-                                const float sv[4] = {a4.x, a4.y, a4.z, a4.w};
+                                for (int j4 = 0; j4 < BM / 4; ++j4) {
+                                    const float4 a4 = sa[j4];
+                                    const float sv[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int j = j4 * 4 + i;
-                                    acc[j] = __fmaf_rn(v[j2 * 16 + j], __fmul_rn(sv[i], sw), acc[j]);
+                                    for (int i = 0; i < 4; ++i) {
+                                        const int j = j4 * 4 + i;
+                                        acc[j] = __fmaf_rn(v[j2 * 16 + j], __fmul_rn(sv[i], sw), acc[j]);
+                                    }
                                 }
                             }
                         }
-                    }
-                } else {
-                    for (int j2 = 0; j2 < nk; ++j2) {
-                        const float sw = d.sw[kk + j2];
-                        const float* sa = d.sa + (kk + j2) * BM;
+                    } else {
+                        for (int j2 = 0; j2 < nk; ++j2) {
+                            const float sw = swt[kk + j2];
+                            const float* sa = d.sa + (kk + j2) * BM;
 #pragma unroll
-                        for (int c = 0; c < BM / 32; ++c) {
-                            float v[32];
-                            tmem_ld32(t0 + static_cast<uint32_t>(j2 * BM + c * 32), v);
+                            for (int c = 0; c < BM / 32; ++c) {
+                                float v[32];
+                                tmem_ld32(t0 + static_cast<uint32_t>(j2 * BM + c * 32), v);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                acc[c * 32 + i] = __fmaf_rn(v[i], __fmul_rn(sa[c * 32 + i], sw), acc[c * 32 + i]);
+                                for (int i = 0; i < 32; ++i)
+                                    acc[c * 32 + i] = __fmaf_rn(v[i], __fmul_rn(sa[c * 32 + i], sw), acc[c * 32 + i]);
+                            }
                         }
+                        tc_fence_before();
+                        mbar_arrive_relaxed(tempty + ts);
                     }
-                    tc_fence_before();
-                    mbar_arrive_relaxed(tempty + ts);
+                    if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
                 }
-                if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
-            }
-            if (flags & kLast) {
-                const int n = d.hdr[2] * 128 + r_in_tile;
-                const int sp = d.hdr[3];
-                // row indices are read into registers 16 at a time before the stores, so no
-                // shared-memory load is ordered between global stores through generic pointers
+                if (flags & kLast) {
+                    const int n = (nt0 + t) * 128 + r_in_tile;
+                    // row indices are read into registers 16 at a time before the stores, so no
+                    // shared-memory load is ordered between global stores through generic pointers
 #pragma unroll
-                for (int j0 = 0; j0 < BM; j0 += 16) {
-                    int rws[16];
+                    for (int j0 = 0; j0 < BM; j0 += 16) {
+                        int rws[16];
 #pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4) {
-                        const int4 r4 = reinterpret_cast<const int4*>(d.rows + j0)[j4];
-                        rws[j4 * 4 + 0] = r4.x; rws[j4 * 4 + 1] = r4.y;
-                        rws[j4 * 4 + 2] = r4.z; rws[j4 * 4 + 3] = r4.w;
-                    }
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const int4 r4 = reinterpret_cast<const int4*>(d.rows + j0)[j4];
+                            rws[j4 * 4 + 0] = r4.x; rws[j4 * 4 + 1] = r4.y;
+                            rws[j4 * 4 + 2] = r4.z; rws[j4 * 4 + 3] = r4.w;
+                        }
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int row = rws[jj];
-                        if (row < 0) continue;
-                        const int j = j0 + jj;
-                        if (p.out_f32) {
-                            float* o = static_cast<float*>(p.out);
-                            o[(static_cast<long long>(sp) * p.out_rows + row) * p.N_out + n] = acc[j];
-                        } else {
-                            uint16_t* o = static_cast<uint16_t*>(p.out);
-                            o[static_cast<long long>(row) * p.N_out + n] =
-                                static_cast<uint16_t>(f32_to_bf16_bits(acc[j]));
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int row = rws[jj];
+                            if (row < 0) continue;
+                            const int j = j0 + jj;
+                            if (p.out_f32) {
+                                float* o = static_cast<float*>(p.out);
+                                o[(static_cast<long long>(sp) * p.out_rows + row) * p.N_out + n] = acc[j];
+                            } else {
+                                uint16_t* o = static_cast<uint16_t*>(p.out);
+                                o[static_cast<long long>(row) * p.N_out + n] =
+                                    static_cast<uint16_t>(f32_to_bf16_bits(acc[j]));
+                            }
                         }
                     }
                 }
