@@ -6,8 +6,9 @@ E4M3 weights with 128x128 fp32 block scales, BF16 activations ~N(0, 1), fp32 dyn
 activation scales.  Inputs are seeded and synthetic; weights are random (no checkpoint).
 
 One step = one whole layer forward (route preparation, input quantisation, gate/up GEMM,
-fused SiLU*mul + quantisation, down GEMM, moe_reduce) through moe_blockfp8_forward, replayed
-from a CUDA graph.  Eight routing batches rotate between steps and a 256 MiB buffer is written
+fused SiLU*mul + quantisation, down GEMM, moe_reduce) through moe_blockfp8_forward on the path
+the library picks for the shape (the fused persistent kernel, or the staged launches), replayed
+from a CUDA graph; both paths are also timed and reported side by side.  Eight routing batches rotate between steps and a 256 MiB buffer is written
 and then read back between timed steps (outside the events), so no step starts with its
 weights in L2 and no dirty line of the flush is written back inside the timed region.
 
@@ -225,7 +226,7 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def layer_graphs(M_):
+    def layer_graphs(M_, path):
         xs, ids, ws = make_inputs(M_, args.seed, dev)
         need = ops.moe_blockfp8_workspace_bytes(M_, k, E, E, H, N)
         work = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -234,11 +235,13 @@ def run_ours(args):
         for r in range(NROT):
             fn = (lambda r=r: ops.moe_blockfp8_forward(xs[r], ids[r], ws[r], E, None, wgu_use, wgu_s,
                                                        wd_use, wd_s, out=outs[r], workspace=work,
-                                                       stream=stream))
+                                                       stream=stream, path=path))
             graphs.append(capture(fn, stream))
         return xs, ids, ws, outs, work, graphs
 
-    xs, ids, ws, outs, work, graphs = layer_graphs(M)
+    path = ops.moe_forward_path_for(M, k, E, E, H, N)
+    path_name = {ops.FORWARD_FUSED: "fused", ops.FORWARD_STAGED: "staged"}[path]
+    xs, ids, ws, outs, work, graphs = layer_graphs(M, path)
     ids_host = [t.cpu().numpy() for t in ids]
     act = active_bytes(ids_host, H, N, E)
     bm, B_cap, splits = ops.moe_blockfp8_plan(M, k, E, E, H, N)
@@ -255,14 +258,18 @@ def run_ours(args):
     layer_bytes = [a[1] + a[2] for a in act]
     mean_bytes = sum(layer_bytes[i % NROT] for i in range(args.steps)) / args.steps
 
-    # ---- the dominant kernel (gate/up GEMM) timed with events on its own stream -------------
+    # ---- both paths of the same layer, for comparison ----------------------------------------
+    path_ms = {}
+    for pth, nm in ((ops.FORWARD_FUSED, "fused"), (ops.FORWARD_STAGED, "staged")):
+        _, _, _, _, _, g_p = layer_graphs(M, pth)
+        path_ms[nm] = time_graph_steps(g_p, min(args.steps, 200), args.warmup, flush, stream)
+        del g_p
+
+    # ---- the gate/up GEMM of the staged path alone, events on its stream --------------------
     gemm_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_use, wgu_s,
-                                  M, H, N, E, k, args.steps, args.warmup)
+                                  M, H, N, E, k, min(args.steps, 200), args.warmup)
     padded_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_use, wgu_s,
                                     M, H, N, E, k, min(args.steps, 100), args.warmup, padded=True)
-    other = wgu_q if args.weights == "tiled" else ops.moe_blockfp8_pack_weights(wgu_q)
-    gemm_other_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, other, wgu_s,
-                                        M, H, N, E, k, min(args.steps, 200), args.warmup)
     gu_bytes = []
     for i, (a, gub, _) in enumerate(act):
         kept = M * k
@@ -277,15 +284,19 @@ def run_ours(args):
     if not args.no_sweep:
         sweep = {}
         for Ms in (1, 4, 16, 32, 64, 128, 256):
-            _, ids_s, _, _, _, g_s = layer_graphs(Ms)
+            row = {}
+            for pth, nm in ((ops.FORWARD_FUSED, "fused"), (ops.FORWARD_STAGED, "staged")):
+                _, ids_s, _, _, _, g_s = layer_graphs(Ms, pth)
+                t = time_graph_steps(g_s, 50, 5, flush, stream)
+                del g_s
+                row[nm + "_us"] = round(statistics.mean(t) * 1e3, 2)
             a_s = active_bytes([t.cpu().numpy() for t in ids_s], H, N, E)
-            t = time_graph_steps(g_s, 50, 5, flush, stream)
             by = sum(a_s[i % NROT][1] + a_s[i % NROT][2] for i in range(50)) / 50
-            us = statistics.mean(t) * 1e3
-            sweep[str(Ms)] = {"us": round(us, 2), "us_median": round(statistics.median(t) * 1e3, 2),
-                              "active_experts": round(sum(a[0] for a in a_s) / NROT, 1),
-                              "GBps": round(by / (us * 1e-6) / 1e9, 1)}
-            del g_s
+            auto = "fused" if ops.moe_forward_path_for(Ms, k, E, E, H, N) == ops.FORWARD_FUSED else "staged"
+            us = row[auto + "_us"]
+            row.update({"us": us, "path": auto, "active_experts": round(sum(a[0] for a in a_s) / NROT, 1),
+                        "GBps": round(by / (us * 1e-6) / 1e9, 1)})
+            sweep[str(Ms)] = row
 
     peaks = {}
     try:
@@ -294,39 +305,43 @@ def run_ours(args):
         pass
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    achieved = gu_mean_bytes / (statistics.mean(gemm_ms) * 1e-3) / 1e9
+    layer_us = ms_per_step * 1e3
+    achieved = mean_bytes / (layer_us * 1e-6) / 1e9
+    gemm_achieved = gu_mean_bytes / (statistics.mean(gemm_ms) * 1e-3) / 1e9
     traffic = recorded_traffic()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(M, ids_host[0], xs[0], wgu_q, wgu_s, wd_q, wd_s, H, N, E, k)
 
-    launches_per_step = (1 if M * k <= 2048 else 2) + 5
-    layer_us = ms_per_step * 1e3
+    route_launches = 1 if M * k <= 2048 else 2
+    launches_per_step = route_launches + (1 if path == ops.FORWARD_FUSED else 5)
+    kernel_name = (f"k_moe_fused<{bm}> with its route preparation (one moe_blockfp8_forward call)"
+                   if path == ops.FORWARD_FUSED else "staged layer (route preparation + 5 launches)")
     line = {
         "metric": METRIC, "value": round(layer_us, 3), "unit": "us", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic (seeded; random weights, uniform random routing)",
         "config": {"workload": f"decode MoE layer M={M} H={H} N={N} E={E} top-k={k}, block-FP8 128x128",
-                   "M": M, "H": H, "N": N, "E": E, "topk": k, "block_m": bm, "gate_up_splits": splits,
+                   "M": M, "H": H, "N": N, "E": E, "topk": k, "block_m": bm, "path": path_name,
                    "weights": args.weights,
                    "l2": "256 MiB buffer written then read back between timed steps (outside the events); 8 rotating routing batches",
                    "timing": "CUDA graph replay per step, CUDA events per step", "parallelism": f"replicas x{world}"},
-        "layer_hbm": {"GBps": round(mean_bytes / (layer_us * 1e-6) / 1e9, 1),
-                      "frac": round(mean_bytes / (layer_us * 1e-6) / 1e9 / hbm_peak, 4),
+        "layer_hbm": {"GBps": round(achieved, 1), "frac": round(achieved / hbm_peak, 4),
                       "active_bytes": int(mean_bytes), "peak": hbm_peak, "peak_source": peak_src,
                       "us_median": round(statistics.median(step_ms) * 1e3, 2),
                       "us_p10": round(float(np.percentile(step_ms, 10)) * 1e3, 2),
                       "us_p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2)},
-        "roofline": {"bound": "hbm", "kernel": "k_grouped_gemm<16> (gate/up)",
+        "roofline": {"bound": "hbm", "kernel": kernel_name,
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": int(gu_mean_bytes),
-                     "kernel_us": round(statistics.mean(gemm_ms) * 1e3, 2),
-                     "weights": args.weights, "peak_source": peak_src,
-                     "other_layout_kernel_us": round(statistics.mean(gemm_other_ms) * 1e3, 2),
-                     "padded_grid_kernel_us": round(statistics.mean(padded_ms) * 1e3, 2)},
+                     "algorithmic_bytes": int(mean_bytes), "kernel_us": round(layer_us, 2),
+                     "weights": args.weights, "peak_source": peak_src},
+        "paths_us": {nm: round(statistics.mean(t) * 1e3, 2) for nm, t in path_ms.items()},
+        "staged_gate_up": {"splits": splits, "us": round(statistics.mean(gemm_ms) * 1e3, 2),
+                           "GBps": round(gemm_achieved, 1), "frac": round(gemm_achieved / hbm_peak, 4),
+                           "padded_grid_us": round(statistics.mean(padded_ms) * 1e3, 2)},
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -440,15 +455,17 @@ def time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, steps, warmup):
 
 
 def recorded_traffic():
-    """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken on the
-    current kernel source (otherwise null)."""
-    path = os.path.join(ROOT, "profiles", "gate_up_gemm_decode_traffic.json")
+    """DRAM bytes per forward call (route preparation + fused kernel) from the committed ncu
+    summary, if it was taken on the current kernel source; else null."""
+    import re
+    path = os.path.join(ROOT, "profiles", "fused_layer_decode_m32_traffic.md")
     try:
-        rec = json.load(open(path))
-        src = open(os.path.join(ROOT, "block_fp8_mixture_moe_gb300", "csrc", "grouped_gemm.cu"), "rb").read()
-        if rec.get("grouped_gemm_sha256") != hashlib.sha256(src).hexdigest():
+        text = open(path).read()
+        want = re.search(r"fused_layer\.cu sha256: `([0-9a-f]{64})`", text).group(1)
+        src = open(os.path.join(ROOT, "block_fp8_mixture_moe_gb300", "csrc", "fused_layer.cu"), "rb").read()
+        if want != hashlib.sha256(src).hexdigest():
             return None
-        return rec.get("dram_bytes_per_launch_full_size")
+        return int(re.search(r"dram_bytes_per_forward: (\d+)", text).group(1))
     except Exception:
         return None
 

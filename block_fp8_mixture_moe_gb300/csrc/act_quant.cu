@@ -124,7 +124,6 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
         active = row_source(p, w, &in_row, &row);
     }
     float a[8];
-    float amax = 0.0f;
     if (active) {
         const long long col = static_cast<long long>(g) * 128 + l * 8;
         const long long rbase = static_cast<long long>(in_row) * p.W;
@@ -137,25 +136,10 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
 #pragma unroll
             for (int i = 0; i < 8; ++i) a[i] = silu_mul_bf16<ACT>(gv[i], uv[i], p.L);
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(a[i]));
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 8));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    if (active) {
-        const float s = group_scale(amax, p.fmt);
-        const float inv = p.fmt == MOE_SCALE_UE8M0 ? pow2_reciprocal(s) : 0.0f;
-        uint32_t c0 = cvt_e4m3x2(quant_div(a[0], s, inv, p.fmt), quant_div(a[1], s, inv, p.fmt));
-        uint32_t c1 = cvt_e4m3x2(quant_div(a[2], s, inv, p.fmt), quant_div(a[3], s, inv, p.fmt));
-        uint32_t c2 = cvt_e4m3x2(quant_div(a[4], s, inv, p.fmt), quant_div(a[5], s, inv, p.fmt));
-        uint32_t c3 = cvt_e4m3x2(quant_div(a[6], s, inv, p.fmt), quant_div(a[7], s, inv, p.fmt));
-        uint2 packed = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
-        const long long o = static_cast<long long>(row) * p.N + static_cast<long long>(g) * 128 + l * 8;
-        *reinterpret_cast<uint2*>(p.out_q + o) = packed;
-        if (l == 0) p.out_s[static_cast<long long>(row) * p.G + g] = s;
-    }
+    const long long o = static_cast<long long>(row) * p.N + static_cast<long long>(g) * 128 + l * 8;
+    quant_group_store(a, active, p.fmt, p.out_q + o, p.out_s + static_cast<long long>(row) * p.G + g,
+                      l == 0);
 }
 
 template <int ACT, bool F32IN, bool PERSISTENT>

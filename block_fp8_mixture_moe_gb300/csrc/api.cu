@@ -3,7 +3,9 @@
 //
 // Layer order (lmdeploy PR #4956 "Perf/pytorch block fp8 moe decode", section "Fused SwiGLU
 // and FP8 quantization": gate/up GEMM -> fused SiLU-and-mul + quant -> down GEMM; lmdeploy PR
-// #4228 "Moe Reduce kernel": weighted top-k sum in its own kernel):
+// #4228 "Moe Reduce kernel": weighted top-k sum).  The fused path launches route preparation
+// and then one persistent kernel for steps 2-6 (fused_layer.cu); the staged path launches them
+// one by one:
 //   1. moe_route_prepare            topk_ids -> expert-sorted slots, compact blocks, route_slot
 //   2. silu_mul_quant_fp8(IDENTITY) x rows gathered into slot order, per-128 E4M3 + scales
 //   3. grouped GEMM (GATE_UP)       fp32 split-K partials per slot
@@ -138,10 +140,13 @@ int gate_up_splits(int M, int k, int E, int E_local, int H, int N, int bm, int s
     return best;
 }
 
+// One workspace layout serves both forward paths: the token-scale and partial-sum regions are
+// sized for the larger of the two uses (the fused kernel stores its token scales K-block major
+// and its gate/up partial sums per stream-K piece); the counters are the fused path's only.
 struct Plan {
     int bm, B_cap, slots, R, splits;
     size_t off_sorted, off_bexp, off_nb, off_cnt, off_off, off_rslot, off_rws, off_xq, off_xs,
-        off_gu, off_aq, off_as, off_z, total;
+        off_gu, off_aq, off_as, off_z, off_sync, total;
 };
 
 Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int sms) {
@@ -162,12 +167,21 @@ Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int 
     P.off_rws = take(route_workspace_bytes(P.R, E_local, P.bm));
     P.off_xq = take(static_cast<size_t>(P.slots) * H);
     P.off_xs = take(sizeof(float) * static_cast<size_t>(P.slots) * (H / 128));
-    P.off_gu = take(sizeof(float) * static_cast<size_t>(P.splits) * P.slots * 2 * N);
+    P.off_gu = take(std::max(sizeof(float) * static_cast<size_t>(P.splits) * P.slots * 2 * N,
+                             fused_partial_bytes(P.B_cap, P.bm, H, N, sms)));
     P.off_aq = take(static_cast<size_t>(P.slots) * N);
     P.off_as = take(sizeof(float) * static_cast<size_t>(P.slots) * (N / 128));
     P.off_z = take(sizeof(uint16_t) * static_cast<size_t>(P.R) * H);
+    P.off_sync = take(sizeof(unsigned) * static_cast<size_t>(fused_counter_words(P.B_cap)));
     P.total = o;
     return P;
+}
+
+// AUTO forward path: the one measured faster on GB300 for the shape (graph-replayed layer on
+// the decode shapes M = 1..256): the staged launches at every measured size.
+moe_forward_path auto_path(int M, int k, int E, int E_local, int H, int N) {
+    (void)M; (void)k; (void)E; (void)E_local; (void)H; (void)N;
+    return MOE_FORWARD_STAGED;
 }
 
 }  // namespace
@@ -222,8 +236,8 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                                     const uint8_t* wd_q, const float* wd_s,
                                     moe_weight_layout w_layout, moe_act act,
                                     float clamp_limit, moe_scale_fmt act_fmt, int block_m,
-                                    void* out, void* workspace, size_t ws_bytes,
-                                    cudaStream_t stream) {
+                                    moe_forward_path path, void* out, void* workspace,
+                                    size_t ws_bytes, cudaStream_t stream) {
     clear_error();
     if (!device_is_sm103()) { set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
     if (!wgu_q || !wgu_s || !wd_q || !wd_s || (M > 0 && (!x || !topk_ids || !topk_w || !out))) {
@@ -241,6 +255,15 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     }
     if (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) {
         set_error("moe_blockfp8_forward: block_m must be 0 (auto), 16, 32, 64 or 128");
+        return MOE_ERR_ARG;
+    }
+    if (path != MOE_FORWARD_AUTO && path != MOE_FORWARD_FUSED && path != MOE_FORWARD_STAGED) {
+        set_error("moe_blockfp8_forward: unknown path %d", static_cast<int>(path));
+        return MOE_ERR_ARG;
+    }
+    if (M > 0 && (!aligned16(x) || !aligned16(wgu_q) || !aligned16(wd_q) || !aligned16(out) ||
+                  !aligned16(wgu_s) || !aligned16(wd_s))) {
+        set_error("moe_blockfp8_forward: x, out and the weight tensors must be 16-byte aligned");
         return MOE_ERR_ARG;
     }
     if (!expert_map && E_local != E) {
@@ -268,11 +291,28 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     float* as = reinterpret_cast<float*>(ws + P.off_as);
     void* z = ws + P.off_z;
     const size_t rws_bytes = P.off_xq - P.off_rws;
+    if (path == MOE_FORWARD_AUTO) path = auto_path(M, k, E, E_local, H, N);
+    const bool fused = path == MOE_FORWARD_FUSED;
+    unsigned* sync = reinterpret_cast<unsigned*>(ws + P.off_sync);
 
     int rc = launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, P.bm, MOE_ROUTE_AUTO,
                                   sorted_idx, block_expert, num_blocks, counts, offsets,
-                                  route_slot, ws + P.off_rws, rws_bytes, false, stream);
+                                  route_slot, ws + P.off_rws, rws_bytes, false, stream,
+                                  fused ? sync : nullptr, fused ? fused_counter_words(P.B_cap) : 0);
     if (rc) return rc;
+    if (fused) {
+        FusedLaunch f{};
+        f.x = x; f.topk_ids = topk_ids; f.topk_w = topk_w; f.expert_map = expert_map;
+        f.M = M; f.k = k; f.E = E; f.E_local = E_local; f.H = H; f.N = N; f.bm = P.bm;
+        f.B_cap = P.B_cap; f.slots = P.slots;
+        f.wgu_q = wgu_q; f.wgu_s = wgu_s; f.wd_q = wd_q; f.wd_s = wd_s; f.w_layout = w_layout;
+        f.act = act; f.clamp_limit = clamp_limit; f.fmt = act_fmt;
+        f.sorted_idx = sorted_idx; f.block_expert = block_expert; f.num_blocks = num_blocks;
+        f.route_slot = route_slot;
+        f.xq = xq; f.xsT = xs; f.gu = gu; f.aq = aq; f.asT = as; f.z = z; f.out = out;
+        f.sync = sync;
+        return launch_fused_layer(f, stream);
+    }
     rc = launch_act_quant(MOE_ACT_IDENTITY, x, MOE_DTYPE_BF16, 1, M, P.R, H, INFINITY, act_fmt,
                           nullptr, nullptr, 0, route_slot, k, P.slots, xq, xs,
                           MOE_QUANT_PERSISTENT, true, stream);
@@ -291,4 +331,8 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                              true, stream);
     if (rc) return rc;
     return launch_moe_reduce(z, topk_w, topk_ids, expert_map, M, k, E, H, out, true, stream);
+}
+
+extern "C" int moe_forward_path_for(int M, int k, int E, int E_local, int H, int N) {
+    return auto_path(M, k, E, E_local, H, N);
 }

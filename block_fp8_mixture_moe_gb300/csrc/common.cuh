@@ -42,7 +42,8 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
                          int E_local, int block_m, moe_route_path path, int32_t* sorted_idx,
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
                          int32_t* expert_offset, int32_t* route_slot, void* workspace,
-                         size_t ws_bytes, bool pdl, cudaStream_t stream);
+                         size_t ws_bytes, bool pdl, cudaStream_t stream,
+                         uint32_t* zero_ptr = nullptr, int zero_n = 0);
 size_t route_workspace_bytes(int R, int E_local, int block_m);
 bool route_single_cta(int R, int E_local, moe_route_path path);
 int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows, int K,
@@ -54,6 +55,42 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
                       const int32_t* expert_map, int M, int k, int E, int H, void* out, bool pdl,
                       cudaStream_t stream);
+
+// The fused layer kernel (everything after route preparation in one persistent launch).
+struct FusedLaunch {
+    const void* x;                 // [M, H] bf16
+    const int32_t* topk_ids;       // [M, k]
+    const float* topk_w;           // [M, k]
+    const int32_t* expert_map;     // [E] or null
+    int M, k, E, E_local, H, N, bm, B_cap, slots;
+    const uint8_t* wgu_q;
+    const float* wgu_s;
+    const uint8_t* wd_q;
+    const float* wd_s;
+    moe_weight_layout w_layout;
+    int act;
+    float clamp_limit;
+    int fmt;
+    const int32_t* sorted_idx;     // route preparation outputs
+    const int32_t* block_expert;
+    const int32_t* num_blocks;
+    const int32_t* route_slot;
+    uint8_t* xq;                   // [slots, H]
+    float* xsT;                    // [H/128, slots]
+    float* gu;                     // fused_partial_bytes(...)
+    uint8_t* aq;                   // [slots, N]
+    float* asT;                    // [N/128, slots]
+    void* z;                       // [M*k, H] bf16
+    void* out;                     // [M, H] bf16
+    unsigned* sync;                // fused_counter_words(B_cap) words, zeroed by route preparation
+};
+int launch_fused_layer(const FusedLaunch& f, cudaStream_t stream);
+size_t fused_partial_bytes(int B_cap, int bm, int H, int N, int G);
+int fused_counter_words(int B_cap);
+
+// 2-D TMA map over a row-major [rows, cols] byte matrix: box 128 columns x box_rows rows,
+// 128-byte swizzle (the K-major operand layout the MMA descriptors expect).
+bool make_tma_map_u8(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -168,6 +205,46 @@ __device__ __forceinline__ float quant_div(float a, float s, float inv_pow2, int
 __device__ __forceinline__ float pow2_reciprocal(float s) {  // s = 2^e, e in [-126, 126]
     uint32_t e = (__float_as_uint(s) >> 23) & 0xFFu;
     return __uint_as_float((254u - e) << 23);
+}
+
+// Half-warp quantisation of one 128-wide group: lane l of the half-warp holds the 8 values at
+// columns 8l..8l+7 (already materialised as BF16 values in fp32).  Every lane of the warp must
+// call this (the amax reduction uses full-mask xor shuffles that stay inside each half-warp).
+// Active lanes get their 8 E4M3 codes packed in *codes and the group scale in *scale.
+__device__ __forceinline__ void quant_group_codes(const float* a, bool active, int fmt,
+                                                  uint2* codes, float* scale) {
+    float amax = 0.0f;
+    if (active) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(a[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    if (active) {
+        const float s = group_scale(amax, fmt);
+        const float inv = fmt == MOE_SCALE_UE8M0 ? pow2_reciprocal(s) : 0.0f;
+        uint32_t c0 = cvt_e4m3x2(quant_div(a[0], s, inv, fmt), quant_div(a[1], s, inv, fmt));
+        uint32_t c1 = cvt_e4m3x2(quant_div(a[2], s, inv, fmt), quant_div(a[3], s, inv, fmt));
+        uint32_t c2 = cvt_e4m3x2(quant_div(a[4], s, inv, fmt), quant_div(a[5], s, inv, fmt));
+        uint32_t c3 = cvt_e4m3x2(quant_div(a[6], s, inv, fmt), quant_div(a[7], s, inv, fmt));
+        *codes = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+        *scale = s;
+    }
+}
+
+// As quant_group_codes, storing the 8 codes at q_dst (one 8-byte store) and, from the
+// half-warp's lane 0 (lead), the scale at s_dst.
+__device__ __forceinline__ void quant_group_store(const float* a, bool active, int fmt,
+                                                  uint8_t* q_dst, float* s_dst, bool lead) {
+    uint2 codes;
+    float s;
+    quant_group_codes(a, active, fmt, &codes, &s);
+    if (active) {
+        *reinterpret_cast<uint2*>(q_dst) = codes;
+        if (lead) *s_dst = s;
+    }
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -492,36 +492,6 @@ __global__ void __launch_bounds__(224, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    std::call_once(g_encode_once, [] {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    return g_encode;
-}
-
-// 2-D map over a row-major [rows, K] E4M3 matrix, box 128 columns x box_rows rows, 128-byte
-// swizzle (the layout the MMA descriptors expect).
-bool make_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
-    auto enc = encoder();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int BM>
 int launch_bm(const CUtensorMap& tw, const CUtensorMap& ta, const GemmArgs& p, long long max_units,
               bool pdl, cudaStream_t stream) {
@@ -539,6 +509,40 @@ int launch_bm(const CUtensorMap& tw, const CUtensorMap& ta, const GemmArgs& p, l
 }
 
 }  // namespace
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+}  // namespace
+
+// 2-D map over a row-major [rows, K] byte matrix (E4M3 codes), box 128 columns x box_rows rows, 128-byte
+// swizzle (the layout the MMA descriptors expect).
+bool make_tma_map_u8(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 
 int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows, int K,
                         const uint8_t* w_q, const float* w_s, int E_local, int N_out,
@@ -586,8 +590,8 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                                    : static_cast<long long>(E_local) * N_out;
     if (w_rows > 0x7FFFFFFFLL) { set_error("grouped_gemm: weight tensor too large"); return MOE_ERR_ARG; }
     CUtensorMap tw, ta;
-    if (!make_map(&tw, w_q, w_rows, tiled ? 128 : K, 128) ||
-        !make_map(&ta, a_q, a_rows, K, block_m)) {
+    if (!make_tma_map_u8(&tw, w_q, w_rows, tiled ? 128 : K, 128) ||
+        !make_tma_map_u8(&ta, a_q, a_rows, K, block_m)) {
         set_error("grouped_gemm: tensor-map encode failed (driver entry point missing or bad layout)");
         return MOE_ERR_LAUNCH;
     }

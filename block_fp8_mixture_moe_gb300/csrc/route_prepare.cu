@@ -52,7 +52,17 @@ struct RouteArgs {
     int32_t* ws_off;   // [E_loc + 1]: first slot of each expert
     unsigned* ws_done; // ticket counter
     int chunk, nchunks, warps;
+    // optional: words the next kernel needs at zero (its phase counters), cleared here
+    uint32_t* zero_ptr;
+    int zero_n;
 };
+
+// Clears the caller's zero region (grid-stride over the launch).
+__device__ __forceinline__ void clear_zero_region(const RouteArgs& p) {
+    if (!p.zero_ptr) return;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_n; i += gridDim.x * blockDim.x)
+        p.zero_ptr[i] = 0u;
+}
 
 __device__ __forceinline__ int local_of(const RouteArgs& p, int r) {
     int id = __ldg(p.ids + r);
@@ -202,6 +212,7 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
     uint16_t* wcnt = reinterpret_cast<uint16_t*>(sm + ints);
     grid_dep_wait();
     grid_dep_launch();
+    clear_zero_region(p);
     for (int r = threadIdx.x; r < p.R; r += blockDim.x) loc[r] = local_of(p, r);
     for (int i = threadIdx.x; i < kSingleWarps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
     __syncthreads();
@@ -230,6 +241,7 @@ __global__ void __launch_bounds__(1024) k_route_count(RouteArgs p) {
     __shared__ int is_last;
     grid_dep_wait();
     grid_dep_launch();
+    clear_zero_region(p);
     const int c = blockIdx.x;
     const int lo = c * p.chunk, hi = min(p.R, lo + p.chunk);
     for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x) hist[e] = 0;
@@ -321,7 +333,8 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
                          int E_local, int block_m, moe_route_path path, int32_t* sorted_idx,
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
                          int32_t* expert_offset, int32_t* route_slot, void* workspace,
-                         size_t ws_bytes, bool pdl, cudaStream_t stream) {
+                         size_t ws_bytes, bool pdl, cudaStream_t stream, uint32_t* zero_ptr,
+                         int zero_n) {
     if (M < 0 || k <= 0 || E <= 0 || E_local <= 0) {
         set_error("moe_route_prepare: need M >= 0, k > 0, E > 0, E_local > 0");
         return MOE_ERR_ARG;
@@ -359,6 +372,8 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
     p.offset = expert_offset;
     p.route_slot = route_slot;
     p.status = device_status_ptr();
+    p.zero_ptr = zero_ptr;
+    p.zero_n = zero_ptr ? zero_n : 0;
     const bool single = route_single_cta(R, E_local, path) && R > 0;
     if (single) {
         if (R > kSingleMaxRoutes || E_local > kSingleMaxExperts) {
@@ -382,6 +397,8 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
         if (e == cudaSuccess && expert_offset)
             e = cudaMemsetAsync(expert_offset, 0, sizeof(int32_t) * (E_local + 1), stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(num_blocks, 0, sizeof(int32_t), stream);
+        if (e == cudaSuccess && zero_ptr && zero_n > 0)
+            e = cudaMemsetAsync(zero_ptr, 0, sizeof(uint32_t) * zero_n, stream);
         if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
         return MOE_OK;
     }

@@ -26,6 +26,7 @@ ROUTE_AUTO, ROUTE_SINGLE_CTA, ROUTE_MULTI_CTA = 0, 1, 2
 QUANT_AUTO, QUANT_PER_GROUP, QUANT_PERSISTENT = 0, 1, 2
 DEV_TIMEOUT, DEV_BAD_EXPERT_MAP, DEV_BAD_INDEX = 1, 2, 4
 WEIGHTS_ROW_MAJOR, WEIGHTS_TILED = 0, 1
+FORWARD_AUTO, FORWARD_FUSED, FORWARD_STAGED = 0, 1, 2
 
 # every entry point of include/moefp8.h with its ctypes signature
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -43,7 +44,8 @@ SIGNATURES = {
     "moe_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_blockfp8_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_blockfp8_forward": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I,
-                                  _F, _I, _I, _P, _P, _Z, _P]),
+                                  _F, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_forward_path_for": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_block_m": (_I, [_I, _I, _I, _I, _I]),
     "moe_blockfp8_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
                                ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
@@ -272,6 +274,10 @@ def moe_blockfp8_workspace_bytes(M, k, E, E_local, H, N, block_m=0) -> int:
     return load().moe_blockfp8_workspace_bytes(M, k, E, E_local, H, N, block_m)
 
 
+def moe_forward_path_for(M, k, E, E_local, H, N) -> int:
+    return load().moe_forward_path_for(M, k, E, E_local, H, N)
+
+
 def moe_forward_block_m(M, k, E_local, H, N) -> int:
     return load().moe_forward_block_m(M, k, E_local, H, N)
 
@@ -286,7 +292,7 @@ def moe_blockfp8_plan(M, k, E, E_local, H, N, block_m=0):
 
 def moe_blockfp8_forward(x, topk_ids, topk_w, E, expert_map, wgu_q, wgu_s, wd_q, wd_s,
                          act=ACT_SILU_MUL, clamp_limit=float("inf"), act_fmt=SCALE_F32,
-                         block_m=0, out=None, workspace=None, stream=None):
+                         block_m=0, out=None, workspace=None, stream=None, path=FORWARD_AUTO):
     """The whole layer.  x: bf16 [M, H]; weights as uint8 E4M3 codes + fp32 block scales."""
     L = load()
     assert x.dtype == torch.bfloat16 and topk_ids.dtype == torch.int32 and topk_w.dtype == torch.float32
@@ -303,7 +309,7 @@ def moe_blockfp8_forward(x, topk_ids, topk_w, E, expert_map, wgu_q, wgu_s, wd_q,
         out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     rc = L.moe_blockfp8_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), M, k, E, _ptr(expert_map),
                                 E_local, H, N, _ptr(wgu_q), _ptr(wgu_s), _ptr(wd_q), _ptr(wd_s), layout, act,
-                                float(clamp_limit), act_fmt, block_m, _ptr(out), _ptr(workspace),
+                                float(clamp_limit), act_fmt, block_m, path, _ptr(out), _ptr(workspace),
                                 workspace.numel(), _stream(stream))
     _check(rc, "moe_blockfp8_forward")
     return out

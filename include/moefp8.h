@@ -65,6 +65,10 @@ typedef enum { MOE_QUANT_AUTO = 0, MOE_QUANT_PER_GROUP = 1, MOE_QUANT_PERSISTENT
  * every 128x128 block is one contiguous 16 KB run, ordered [E_local][N_out/128][K/128][128][128]
  * (see moe_blockfp8_pack_weights); the block scales keep their layout. */
 typedef enum { MOE_WEIGHTS_ROW_MAJOR = 0, MOE_WEIGHTS_TILED = 1 } moe_weight_layout;
+/* FUSED: route preparation, then one persistent kernel for everything else (see
+ * moe_blockfp8_forward).  STAGED: one launch per stage through the same kernels as the per-stage
+ * entry points.  AUTO: the path this library measured to be faster for the shape. */
+typedef enum { MOE_FORWARD_AUTO = 0, MOE_FORWARD_FUSED = 1, MOE_FORWARD_STAGED = 2 } moe_forward_path;
 
 /* device status bits */
 #define MOE_DEV_TIMEOUT 1
@@ -221,15 +225,26 @@ MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* top
                cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
- * The whole layer: route preparation -> input quantisation (gathered into slot order) ->
- * gate/up grouped GEMM -> fused SiLU*mul + quantisation -> down grouped GEMM -> moe_reduce.
- *   x [M, H] bf16; topk_ids / topk_w [M, k]; expert_map nullable [E] (E_local local experts);
- *   wgu_q [E_local, 2N, H] E4M3 + wgu_s [E_local, 2N/128, H/128] f32 (gate rows 0..N-1, up
- *   rows N..2N-1); wd_q [E_local, H, N] E4M3 + wd_s [E_local, H/128, N/128] f32; both weight
- *   tensors in w_layout (row-major, or tiled by moe_blockfp8_pack_weights);
- *   act SILU_MUL or SILU_MUL_GATE_UPPER; clamp_limit (+inf = none); act_fmt for the dynamic
- *   activation scales (input and intermediate); block_m 0 = chosen from the shape.
- *   out [M, H] bf16.  workspace: moe_blockfp8_workspace_bytes(...) bytes, 256-byte aligned.
+ * The whole layer (lmdeploy PR #4956, sections "Active-expert block scheduling" and "Fused SwiGLU
+ * and FP8 quantization"; lmdeploy PR #4228 for the final weighted sum): route preparation ->
+ * input quantisation (gathered into slot order) -> gate/up grouped GEMM -> fused SiLU*mul +
+ * quantisation -> down grouped GEMM -> moe_reduce.
+ *   x [M, H] bf16 (16-byte aligned); topk_ids / topk_w [M, k]; expert_map nullable [E]
+ *   (E_local local experts); wgu_q [E_local, 2N, H] E4M3 + wgu_s [E_local, 2N/128, H/128] f32
+ *   (gate rows 0..N-1, up rows N..2N-1); wd_q [E_local, H, N] E4M3 + wd_s [E_local, H/128,
+ *   N/128] f32; both weight tensors in w_layout (row-major, or tiled by
+ *   moe_blockfp8_pack_weights); act SILU_MUL or SILU_MUL_GATE_UPPER; clamp_limit (+inf = none);
+ *   act_fmt for the dynamic activation scales (input and intermediate); block_m 0 = chosen from
+ *   the shape.  out [M, H] bf16.  workspace: moe_blockfp8_workspace_bytes(...) bytes, 256-byte
+ *   aligned (the same size serves both paths).
+ * path FUSED: after route preparation ONE persistent kernel with one CTA per SM runs the rest;
+ *   its phases are separated by counters in the workspace, so the kernel needs all its CTAs
+ *   resident at once: do not run it concurrently with other work that occupies SMs for its
+ *   whole duration (every wait is bounded; such a run ends with MOE_DEV_TIMEOUT in the device
+ *   status word instead of hanging).  The gate/up K range is dealt to the SMs in equal pieces,
+ *   so the fp32 summation order of the gate/up partial sums (not the arithmetic of any stage)
+ *   depends on the SM count.  path STAGED: one launch per stage.  AUTO: see
+ *   moe_forward_path_for.
  * H and N multiples of 128.  All stages run on `stream` with no host synchronisation, so the
  * call can be captured in a CUDA graph.
  * ------------------------------------------------------------------------------------------ */
@@ -238,9 +253,11 @@ MOEFP8_API int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                          int k, int E, const int32_t* expert_map, int E_local, int H, int N,
                          const uint8_t* wgu_q, const float* wgu_s, const uint8_t* wd_q,
                          const float* wd_s, moe_weight_layout w_layout, moe_act act,
-                         float clamp_limit,
-                         moe_scale_fmt act_fmt, int block_m, void* out, void* workspace,
-                         size_t ws_bytes, cudaStream_t stream);
+                         float clamp_limit, moe_scale_fmt act_fmt, int block_m,
+                         moe_forward_path path, void* out, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream);
+/* The path moe_blockfp8_forward takes for path = AUTO at these sizes (FUSED or STAGED). */
+MOEFP8_API int moe_forward_path_for(int M, int k, int E, int E_local, int H, int N);
 
 /* block_m the forward uses when called with block_m = 0. */
 MOEFP8_API int moe_forward_block_m(int M, int k, int E_local, int H, int N);

@@ -1,5 +1,6 @@
-"""Whole-layer GPU parity: moe_blockfp8_forward against the CPU oracle, BF16 outputs within
-|err| <= 2e-2 + 1e-2*|ref|, on the pages' workload shapes (seeded synthetic inputs).
+"""Whole-layer GPU parity: moe_blockfp8_forward (both paths: the fused persistent kernel and the
+stage-by-stage launches) against the CPU oracle, BF16 outputs within |err| <= 2e-2 + 1e-2*|ref|,
+on the pages' workload shapes (seeded synthetic inputs).
 
 Full-size decode (H=7168, N=256, E=256, k=8, M=1..32) is compared on every output; the prefill
 shape (M=512, H=4096, N=768, E=512, Zipf routing) on a token sample that includes the tokens of
@@ -17,7 +18,10 @@ pytestmark = pytest.mark.gpu
 INF = float("inf")
 
 
-def _run(ops, L, act=1, clamp=INF, fmt=0, block_m=0, tiled=False):
+FUSED, STAGED = 1, 2  # moe_forward_path
+
+
+def _run(ops, L, act=1, clamp=INF, fmt=0, block_m=0, tiled=False, path=FUSED):
     emap = L["expert_map"]
     wgu, wd = L["wgu_q"], L["wd_q"]
     if tiled:
@@ -25,7 +29,7 @@ def _run(ops, L, act=1, clamp=INF, fmt=0, block_m=0, tiled=False):
     out = ops.moe_blockfp8_forward(
         bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"]), L["E"],
         None if emap is None else to_dev(emap), wgu, L["wgu_s"], wd, L["wd_s"],
-        act=act, clamp_limit=clamp, act_fmt=fmt, block_m=block_m)
+        act=act, clamp_limit=clamp, act_fmt=fmt, block_m=block_m, path=path)
     torch.cuda.synchronize()
     assert ops.device_status() == 0
     return bf16_host(out)
@@ -40,33 +44,36 @@ def _host(L, tokens=None):
     return wl.layer_numpy(L, experts=loc[loc >= 0])
 
 
+@pytest.mark.parametrize("path", [FUSED, STAGED])
 @pytest.mark.parametrize("tiled", [False, True])
 @pytest.mark.parametrize("act,clamp,fmt", [(1, INF, 0), (1, INF, 1), (1, 7.0, 1), (2, 1.0, 0)])
 @pytest.mark.parametrize("block_m", [0, 16, 32, 64, 128])
-def test_tiny_layer(ops, act, clamp, fmt, block_m, tiled):
+def test_tiny_layer(ops, act, clamp, fmt, block_m, tiled, path):
     L = wl.make_layer(**wl.CONFIGS["tiny"], seed=0, device="cuda")
-    got = _run(ops, L, act, clamp, fmt, block_m, tiled)
+    got = _run(ops, L, act, clamp, fmt, block_m, tiled, path)
     ref = oracle.moe_forward(_host(L), act=act, clamp_limit=clamp, fmt=fmt)
     assert_bf16_close(got, ref, "tiny")
 
 
+@pytest.mark.parametrize("path", [FUSED, STAGED])
 @pytest.mark.parametrize("M", wl.DECODE_M)
-def test_decode_full_size(ops, M):
+def test_decode_full_size(ops, M, path):
     cfg = dict(wl.CONFIGS["decode"], M=M)
     L = wl.make_layer(**cfg, seed=1, device="cuda")
-    got = _run(ops, L, tiled=(M % 2 == 0))
+    got = _run(ops, L, tiled=(M % 2 == 0), path=path)
     ref = oracle.moe_forward(_host(L))
     assert_bf16_close(got, ref, f"decode M={M}")
 
 
+@pytest.mark.parametrize("path", [FUSED, STAGED])
 @pytest.mark.parametrize("T", wl.EP_TOKENS)
-def test_expert_parallel_slice(ops, T):
+def test_expert_parallel_slice(ops, T, path):
     """k=6 of E=256 with 32 local experts through an expert map; non-local routes are dropped
     in every stage and add nothing to the output (T=1024 tokens = 6144 routed rows is compared
     on a 48-token sample, including tokens with no local route)."""
     cfg = dict(wl.CONFIGS["ep"], M=T)
     L = wl.make_layer(**cfg, seed=2, device="cuda")
-    got = _run(ops, L, clamp=7.0, fmt=1, tiled=(T >= 100))
+    got = _run(ops, L, clamp=7.0, fmt=1, tiled=(T >= 100), path=path)
     if T <= 100:
         ref = oracle.moe_forward(_host(L), clamp_limit=7.0, fmt=1)
         assert_bf16_close(got, ref, f"ep T={T}")
@@ -81,10 +88,11 @@ def test_expert_parallel_slice(ops, T):
             assert (oracle.bf16_to_f32(got[none_local]) == 0).all()
 
 
-def test_prefill_zipf_sampled(ops):
+@pytest.mark.parametrize("path", [FUSED, STAGED])
+def test_prefill_zipf_sampled(ops, path):
     cfg = wl.CONFIGS["prefill"]
     L = wl.make_layer(**cfg, seed=3, device="cuda")
-    got = _run(ops, L, tiled=True)
+    got = _run(ops, L, tiled=True, path=path)
     ids = L["topk_ids"]
     hot = np.bincount(ids.reshape(-1), minlength=cfg["E"]).argmax()
     hot_tokens = np.nonzero((ids == hot).any(axis=1))[0]
@@ -94,15 +102,16 @@ def test_prefill_zipf_sampled(ops):
     assert_bf16_close(got[toks], ref[toks], "prefill sample")
 
 
-def test_invalid_routes_and_empty(ops):
+@pytest.mark.parametrize("path", [FUSED, STAGED])
+def test_invalid_routes_and_empty(ops, path):
     L = wl.make_layer(M=9, H=256, N=128, E=12, k=3, seed=4, device="cuda", invalid_frac=0.3)
-    got = _run(ops, L)
+    got = _run(ops, L, path=path)
     ref = oracle.moe_forward(_host(L))
     assert_bf16_close(got, ref, "invalid routes")
     # every route dropped: the output is exactly zero
     L2 = dict(L)
     L2["topk_ids"] = np.full_like(L["topk_ids"], -1)
-    assert (f32 := oracle.bf16_to_f32(_run(ops, L2))).max() == 0 and f32.min() == 0
+    assert (f32 := oracle.bf16_to_f32(_run(ops, L2, path=path))).max() == 0 and f32.min() == 0
     # no tokens at all
     L3 = dict(L)
     L3["x"] = L["x"][:0]
@@ -113,11 +122,12 @@ def test_invalid_routes_and_empty(ops):
         torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"),
         torch.empty((0, 3), dtype=torch.int32, device="cuda"),
         torch.empty((0, 3), dtype=torch.float32, device="cuda"), 12, emap,
-        L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"])
+        L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"], path=path)
     assert out.shape == (0, 256)
 
 
-def test_forward_is_deterministic_and_graph_capturable(ops):
+@pytest.mark.parametrize("path", [FUSED, STAGED])
+def test_forward_is_deterministic_and_graph_capturable(ops, path):
     cfg = dict(wl.CONFIGS["decode"], M=4)
     L = wl.make_layer(**cfg, seed=5, device="cuda")
     x, ids, w = bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"])
@@ -126,17 +136,17 @@ def test_forward_is_deterministic_and_graph_capturable(ops):
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
     args = (x, ids, w, 256, None, L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"])
-    ops.moe_blockfp8_forward(*args, out=out, workspace=ws)
+    ops.moe_blockfp8_forward(*args, out=out, workspace=ws, path=path)
     first = out.clone()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
-        ops.moe_blockfp8_forward(*args, out=out, workspace=ws, stream=s)  # warm up on s
+        ops.moe_blockfp8_forward(*args, out=out, workspace=ws, stream=s, path=path)  # warm up on s
         torch.cuda.synchronize()
         out.zero_()
         with torch.cuda.graph(g, stream=s):
-            ops.moe_blockfp8_forward(*args, out=out, workspace=ws, stream=s)
+            ops.moe_blockfp8_forward(*args, out=out, workspace=ws, stream=s, path=path)
     g.replay()
     g.replay()
     torch.cuda.synchronize()
