@@ -185,6 +185,18 @@ __device__ __forceinline__ float silu_mul_bf16(float g, float u, float L) {
     return bf16_round_f32(__fmul_rn(s, u));
 }
 
+// The same SiLU*mul as silu_mul_bf16<act>, with the activation chosen at run time and the code
+// kept out of line: one copy, for paths that run once per kernel, where instruction fetch and
+// not arithmetic dominates.  Identical arithmetic, operation for operation.
+static __device__ __noinline__ float silu_mul_bf16_rt(float g, float u, float L, int act) {
+    if (act == MOE_ACT_SILU_MUL) g = fmaxf(g, -L);
+    g = fminf(g, L);
+    u = fminf(fmaxf(u, -L), L);
+    const float e = exp_f32(-g);
+    const float s = __fdiv_rn(g, __fadd_rn(1.0f, e));
+    return bf16_round_f32(__fmul_rn(s, u));
+}
+
 // Group scale from the group's amax.
 __device__ __forceinline__ float group_scale(float amax, int fmt) {
     float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
@@ -229,6 +241,35 @@ __device__ __forceinline__ void quant_group_codes(const float* a, bool active, i
         uint32_t c1 = cvt_e4m3x2(quant_div(a[2], s, inv, fmt), quant_div(a[3], s, inv, fmt));
         uint32_t c2 = cvt_e4m3x2(quant_div(a[4], s, inv, fmt), quant_div(a[5], s, inv, fmt));
         uint32_t c3 = cvt_e4m3x2(quant_div(a[6], s, inv, fmt), quant_div(a[7], s, inv, fmt));
+        *codes = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+        *scale = s;
+    }
+}
+
+// Two E4M3 codes of a / s (the quantiser of quant_group_codes), out of line.
+static __device__ __noinline__ uint32_t quant_pair_rt(float a0, float a1, float s, float inv, int fmt) {
+    return cvt_e4m3x2(quant_div(a0, s, inv, fmt), quant_div(a1, s, inv, fmt));
+}
+
+// quant_group_codes with its per-value work out of line (same arithmetic and results).
+__device__ __forceinline__ void quant_group_codes_compact(const float* a, bool active, int fmt,
+                                                          uint2* codes, float* scale) {
+    float amax = 0.0f;
+    if (active) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(a[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    if (active) {
+        const float s = group_scale(amax, fmt);
+        const float inv = fmt == MOE_SCALE_UE8M0 ? pow2_reciprocal(s) : 0.0f;
+        const uint32_t c0 = quant_pair_rt(a[0], a[1], s, inv, fmt);
+        const uint32_t c1 = quant_pair_rt(a[2], a[3], s, inv, fmt);
+        const uint32_t c2 = quant_pair_rt(a[4], a[5], s, inv, fmt);
+        const uint32_t c3 = quant_pair_rt(a[6], a[7], s, inv, fmt);
         *codes = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
         *scale = s;
     }

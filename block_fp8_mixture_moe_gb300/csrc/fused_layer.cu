@@ -24,11 +24,15 @@
 //       (unit, K-block) space is cut into equal contiguous ranges, so a unit (block, 128-row
 //       tile) can be split between neighbouring CTAs; piece p of a unit writes its fp32 partial
 //       sum to partial slot p and counts itself in its block's counter (blk_done).
-//   P2  fused act-quant of a slice of (route, group) items: an item waits only for its own
-//       block's pieces, adds them in K order, rounds to BF16, optionally clamps,
-//       a = bf16(SiLU(g)*u), per-128 E4M3 + scale, and counts itself in blk_ready.
-//   P3  down GEMM over (block, 128-row tile) units, BF16 rows scattered to route order; the
-//       activation loads of a block wait for its blk_ready count; grid counter 3.
+//   P2  fused act-quant: every CTA takes the slots of a contiguous range of blocks (so mostly
+//       the blocks whose gate/up pieces it has just produced); an item (slot, group) waits only
+//       for its own block's pieces, adds them in K order, rounds to BF16, optionally clamps,
+//       a = bf16(SiLU(g)*u), per-128 E4M3 + scale.  The item that completes a block appends
+//       it to the ready list.
+//   P3  down GEMM over (block, 128-row tile) units, BF16 rows scattered to route order.  The
+//       units are handed out dynamically, in the order the blocks became ready, from a global
+//       counter: an SM that finished its gate/up work early starts on the down work at once,
+//       and SMs that stream slower take fewer units; grid counter 3 when all are stored.
 //   P4  every CTA (all its threads) reduces a slice of the tokens: out = bf16(sum_j w_j z_j)
 //       in top-k order.
 //
@@ -69,9 +73,11 @@ struct FusedArgs {
     uint16_t* out;        // [M, H] bf16
     float L;
     int act, fmt, w_tiled;
-    unsigned* sync;       // [4] grid counters (0: input quantised, 3: down done)
+    unsigned* sync;       // [4]: 0 input quantised (grid), 1 ready blocks, 2 down units handed
+                          // out, 3 down done (grid)
     unsigned* blk_done;   // [B_cap] gate/up tile pieces stored per block (x4 epilogue warps)
-    unsigned* blk_ready;  // [B_cap] act-quant groups stored per block
+    unsigned* blk_ready;  // [B_cap] act-quant items (slot, group) done per block, pads included
+    unsigned* ready_list; // [B_cap] 1 + block id, in the order the blocks became ready
     int* status;
 };
 
@@ -89,7 +95,7 @@ struct FCfg {
     static constexpr int kCK = 32;                     // K-blocks per descriptor
     static constexpr int kSwMax = 64;                  // weight-block scales per descriptor
     static constexpr int kRing = 8;
-    // header ints: e, b, nt0, ntl, piece, kb0, nck, flags, ready target (down), 3 unused
+    // header ints: e, b, nt0, ntl, piece, kb0, nck, flags, 4 unused
     static constexpr int kDescHdr = 12;
     static constexpr int kDescInts = kDescHdr + BM + kSwMax;
     static constexpr int kDescBytes = ((kDescInts * 4) + 15) / 16 * 16;
@@ -205,6 +211,7 @@ __global__ void __launch_bounds__(256, 1)
     uint64_t* mma_done = dempty + C::kRing;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* w_taken = reinterpret_cast<volatile int*>(tmem_slot + 2);  // descriptors the weight producer took
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
@@ -214,6 +221,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = 0; i < C::kRing; ++i) { mbar_init(dfull + i, 32); mbar_init(dempty + i, 131); }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
+        *w_taken = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -234,15 +242,24 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // route preparation (the launch this one depends on) is complete past this point; its
-    // outputs are read through L2 (ld.global.cg), the caller's inputs through the read-only path
-    grid_dep_wait();
+    // Route preparation (the launch this one depends on) is complete once a thread has passed
+    // grid_dep_wait(); its outputs are read through L2 (ld.global.cg), the caller's inputs
+    // through the read-only path.  The epilogue warps first load and quantise the input rows,
+    // which do not depend on the routing, and wait inside P0; every other warp waits here.
     grid_dep_launch();
-
-    const int nblk = max(0, min(__ldcg(p.num_blocks), p.B_cap));
-    const long long W1 = static_cast<long long>(nblk) * p.NT1 * p.KB1;  // gate/up K-block work
-    const int G1 = static_cast<int>(max(1LL, min(static_cast<long long>(G), W1)));  // CTAs with gate/up work
-    const int rows1 = nblk * BM;                                          // rows of a partial slot
+    const bool epi_warp = warp >= 2 && warp <= 5;
+    if (!epi_warp) grid_dep_wait();
+    int nblk = 0;
+    long long W1 = 0;  // gate/up K-block work
+    int G1 = 1;        // CTAs with gate/up work
+    int rows1 = 0;     // rows of a partial-sum slot
+    auto read_plan = [&]() {
+        nblk = max(0, min(__ldcg(p.num_blocks), p.B_cap));
+        W1 = static_cast<long long>(nblk) * p.NT1 * p.KB1;
+        G1 = static_cast<int>(max(1LL, min(static_cast<long long>(G), W1)));
+        rows1 = nblk * BM;
+    };
+    if (!epi_warp) read_plan();
 
     if (warp == 6) {
         // ---------------- metadata warp ----------------
@@ -250,6 +267,7 @@ __global__ void __launch_bounds__(256, 1)
         uint32_t ph = 0;
         bool ok = true;
         int cur_b = -1, e = -1, nkept = 0;
+        long long base_desc = 0;  // descriptors written so far (all phases, markers included)
         int rows[(BM + 31) / 32];
         // Writes one descriptor (tiles nt0..nt0+ntl-1 of block b, K-blocks [c0, c0+nck)).
         auto emit = [&](int down, int b, int nt0, int ntl, int piece, int c0, int nck, int flags) {
@@ -269,7 +287,6 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) {
                 d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt0; d.hdr[3] = ntl; d.hdr[4] = piece;
                 d.hdr[5] = c0; d.hdr[6] = nck; d.hdr[7] = flags | (down ? kDown : 0);
-                d.hdr[8] = nkept * (p.N / 128);  // act-quant groups of this block
             }
 #pragma unroll
             for (int t = 0; t < (BM + 31) / 32; ++t)
@@ -281,6 +298,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             mbar_arrive(dfull + slot);
             if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
+            ++base_desc;
         };
         // Control descriptor (phase marker or end).
         auto emit_ctl = [&](int flags) {
@@ -289,9 +307,16 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) fdesc_at<BM>(ring, slot).hdr[7] = flags;
             mbar_arrive(dfull + slot);
             if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
+            ++base_desc;
         };
         // Loads block b's expert and output rows (down: route ids; gate/up: slot ids).
         auto load_block = [&](int b, int down) {
+            int r_raw[(BM + 31) / 32];
+#pragma unroll
+            for (int t = 0; t < (BM + 31) / 32; ++t) {
+                const int j = t * 32 + lane;
+                r_raw[t] = j < BM ? __ldcg(p.sorted_idx + b * BM + j) : -1;
+            }
             const int e_raw = __ldcg(p.block_expert + b);
             e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
 #pragma unroll
@@ -300,7 +325,7 @@ __global__ void __launch_bounds__(256, 1)
                 int row = -1;
                 if (j < BM && e >= 0) {
                     const int slot_j = b * BM + j;
-                    const int r = __ldcg(p.sorted_idx + slot_j);
+                    const int r = r_raw[t];
                     row = r < 0 ? -1 : (down ? r : slot_j);
                     if (row >= (down ? p.R : p.slots)) {
                         if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
@@ -347,32 +372,80 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         if (ok) emit_ctl(kMarker);
-        // ---- down: (block, tile) units, contiguous ranges ----
+        // ---- down: (block, tile) units handed out dynamically ----
+        // Units are numbered (ready-list position, tile); a grab takes kGrab consecutive units.
+        // A grab is made only when at most kAhead descriptors wait for the weight producer (on
+        // top of the stages it has in flight), so a CTA holds about as much down work as its
+        // pipeline needs to stay busy, and no more.
         if (ok) {
+            constexpr int kAhead = 2;
             cur_b = -1;
             const long long units = static_cast<long long>(nblk) * p.NT2;
-            const long long u_lo = units * cta / G, u_hi = units * (cta + 1) / G;
-            int nt = static_cast<int>(u_lo % p.NT2);
-            int b = static_cast<int>(u_lo / p.NT2);
-            long long left = u_hi - u_lo;
-            while (left > 0 && ok) {
-                if (b != cur_b) load_block(b, 1);
-                const int run = static_cast<int>(min(static_cast<long long>(p.NT2 - nt), left));
-                int adv = run;
-                if (p.KB2 <= C::kCK) {
-                    const int ntl = min(run, C::kSwMax / p.KB2);
-                    if (e >= 0) emit(1, b, nt, ntl, 0, 0, p.KB2, kFirst | kLast);
-                    adv = ntl;
-                } else {
-                    for (int c0 = 0; c0 < p.KB2 && ok && e >= 0; c0 += C::kCK) {
-                        const int nck = min(C::kCK, p.KB2 - c0);
-                        emit(1, b, nt, 1, 0, c0, nck, (c0 == 0 ? kFirst : 0) | (c0 + nck == p.KB2 ? kLast : 0));
+            int bi_cur = -1, b_ready = -1;
+            long long seen = 0;  // the hand-out counter as last seen by this CTA
+            for (;;) {
+                {
+                    // bounded wait until the weight producer has taken all but kAhead descriptors
+                    const uint64_t t0 = globaltimer_ns();
+                    bool late = false;
+                    while (static_cast<long long>(*w_taken) + kAhead < base_desc) {
+                        if (*abort_flag) { late = true; break; }
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            if (lane == 0) {
+                                if (p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
+                                *abort_flag = 1;
+                            }
+                            late = true;
+                            break;
+                        }
+                        __nanosleep(64);
                     }
-                    adv = 1;
+                    if (__any_sync(0xFFFFFFFFu, late)) { ok = false; break; }
                 }
-                nt += adv;
-                left -= adv;
-                if (nt == p.NT2) { nt = 0; ++b; }
+                // grab size: up to 8 units while much work is left, down to 1 near the end
+                const int grab = static_cast<int>(max(1LL, min(8LL, (units - seen) / (4LL * G))));
+                long long g0 = 0;
+                if (lane == 0) g0 = static_cast<long long>(atomicAdd(p.sync + 2, static_cast<unsigned>(grab)));
+                g0 = __shfl_sync(0xFFFFFFFFu, g0, 0);
+                seen = g0 + grab;
+                if (g0 >= units) break;
+                const long long g1 = min(units, g0 + grab);
+                for (long long u = g0; u < g1 && ok;) {
+                    const int bi = static_cast<int>(u / p.NT2);
+                    const int nt = static_cast<int>(u - static_cast<long long>(bi) * p.NT2);
+                    if (bi != bi_cur) {
+                        // the block at ready-list position bi (bounded wait, acquire)
+                        bool okw = true;
+                        unsigned v = 0;
+                        if (lane == 0) {
+                            okw = wait_counter(p.ready_list + bi, 1u, abort_flag, p.status);
+                            v = ld_acquire_gpu(p.ready_list + bi);
+                        }
+                        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                        v = __shfl_sync(0xFFFFFFFFu, v, 0);
+                        if (!okw) { ok = false; break; }
+                        b_ready = static_cast<int>(v) - 1;
+                        bi_cur = bi;
+                    }
+                    const int b = b_ready;
+                    if (b < 0 || b >= nblk) { if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX); ok = false; break; }
+                    if (b != cur_b) load_block(b, 1);
+                    const int run = static_cast<int>(min(static_cast<long long>(p.NT2 - nt), g1 - u));
+                    int adv = run;
+                    if (p.KB2 <= C::kCK) {
+                        const int ntl = min(run, C::kSwMax / p.KB2);
+                        if (e >= 0) emit(1, b, nt, ntl, 0, 0, p.KB2, kFirst | kLast);
+                        adv = ntl;
+                    } else {
+                        for (int c0 = 0; c0 < p.KB2 && ok && e >= 0; c0 += C::kCK) {
+                            const int nck = min(C::kCK, p.KB2 - c0);
+                            emit(1, b, nt, 1, 0, c0, nck, (c0 == 0 ? kFirst : 0) | (c0 + nck == p.KB2 ? kLast : 0));
+                        }
+                        adv = 1;
+                    }
+                    u += adv;
+                }
+                if (!ok) break;
             }
         }
         if (ok) emit_ctl(kEnd);
@@ -399,17 +472,20 @@ __global__ void __launch_bounds__(256, 1)
                 if (flags & kMarker) {
                     mbar_arrive(dempty + slot);
                     if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
+                    if (wprod) *w_taken = *w_taken + 1;
                     continue;
                 }
                 const int down = flags & kDown;
                 const int e = d.hdr[0], b = d.hdr[1], nt0 = d.hdr[2], ntl = d.hdr[3];
-                const int c0 = d.hdr[5], nck = d.hdr[6], target = d.hdr[8];
+                const int c0 = d.hdr[5], nck = d.hdr[6];
                 mbar_arrive(dempty + slot);
                 if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
+                if (wprod) *w_taken = *w_taken + 1;
                 if (!wprod && down && b != ready_b) {
-                    // the block's quantised activations (written by the act-quant items of any
-                    // CTA) must be in memory before TMA reads them
-                    if (!wait_counter(p.blk_ready + b, static_cast<unsigned>(target), abort_flag, p.status)) break;
+                    // The block's quantised activations were published before it entered the
+                    // ready list; the metadata warp acquired that entry before writing this
+                    // descriptor, and the descriptor hand-off orders this thread after it.  The
+                    // proxy fence orders those generic-proxy writes before the TMA reads.
                     fence_proxy_async_global();
                     ready_b = b;
                 }
@@ -507,43 +583,73 @@ __global__ void __launch_bounds__(256, 1)
 
         // ---- P0: input quantisation of this CTA's slice of (token, group) items ----
         // Each token row is quantised once and its codes and scale are stored to the slot of
-        // every kept route of the token (the same values the per-route gather produces).
+        // every kept route of the token (the same values the per-route gather produces).  The
+        // first kHold pairs of each warp are loaded and quantised before the wait for route
+        // preparation (the input does not depend on it); only the stores to the slots follow it.
         {
+            constexpr int kHold = 4;
             const long long groups = static_cast<long long>(p.M) * p.KB1;
             const long long pairs = (groups + 1) / 2;
             const long long lo = pairs * cta / G, hi = pairs * (cta + 1) / G;
-            for (long long pr = lo + ewarp; pr < hi; pr += 4) {
+            auto item_of = [&](long long pr, int& t, int& g) -> bool {
                 const long long item = pr * 2 + half;
-                const bool active = item < groups;
-                int t = 0, g = 0;
-                float a[8];
-                if (active) {
-                    t = static_cast<int>(item / p.KB1);
-                    g = static_cast<int>(item - static_cast<long long>(t) * p.KB1);
-                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                        p.x + static_cast<long long>(t) * p.H + g * 128 + l * 8));
-                    a[0] = bf16_lo(v.x); a[1] = bf16_hi(v.x); a[2] = bf16_lo(v.y); a[3] = bf16_hi(v.y);
-                    a[4] = bf16_lo(v.z); a[5] = bf16_hi(v.z); a[6] = bf16_lo(v.w); a[7] = bf16_hi(v.w);
-                }
-                uint2 codes;
-                float sc;
-                quant_group_codes(a, active, p.fmt, &codes, &sc);
-                if (active) {
-                    for (int j0 = 0; j0 < p.k; j0 += 8) {
-                        int ms[8];
+                if (pr >= hi || item >= groups) return false;
+                t = static_cast<int>(item / p.KB1);
+                g = static_cast<int>(item - static_cast<long long>(t) * p.KB1);
+                return true;
+            };
+            auto scatter = [&](int t, int g, uint2 codes, float sc) {
+                for (int j0 = 0; j0 < p.k; j0 += 8) {
+                    int ms[8];
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj)
-                            ms[jj] = j0 + jj < p.k ? __ldcg(p.route_slot + t * p.k + j0 + jj) : -1;
+                    for (int jj = 0; jj < 8; ++jj)
+                        ms[jj] = j0 + jj < p.k ? __ldcg(p.route_slot + t * p.k + j0 + jj) : -1;
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            int m = ms[jj];
-                            if (m >= p.slots) { if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX); m = -1; }
-                            if (m < 0) continue;
-                            *reinterpret_cast<uint2*>(p.xq + static_cast<long long>(m) * p.H + g * 128 + l * 8) = codes;
-                            if (l == 0) p.xsT[static_cast<long long>(g) * p.slots + m] = sc;
-                        }
+                    for (int jj = 0; jj < 8; ++jj) {
+                        int m = ms[jj];
+                        if (m >= p.slots) { if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX); m = -1; }
+                        if (m < 0) continue;
+                        *reinterpret_cast<uint2*>(p.xq + static_cast<long long>(m) * p.H + g * 128 + l * 8) = codes;
+                        if (l == 0) p.xsT[static_cast<long long>(g) * p.slots + m] = sc;
                     }
                 }
+            };
+            auto decode8 = [](const uint4& v, float* a) {
+                a[0] = bf16_lo(v.x); a[1] = bf16_hi(v.x); a[2] = bf16_lo(v.y); a[3] = bf16_hi(v.y);
+                a[4] = bf16_lo(v.z); a[5] = bf16_hi(v.z); a[6] = bf16_lo(v.w); a[7] = bf16_hi(v.w);
+            };
+            // the held pairs: all loads first, then the quantisation
+            uint4 xv[kHold];
+            int ht[kHold], hg[kHold];
+            bool ha[kHold];
+#pragma unroll
+            for (int i = 0; i < kHold; ++i) {
+                ha[i] = item_of(lo + ewarp + 4LL * i, ht[i], hg[i]);
+                if (ha[i]) xv[i] = __ldg(reinterpret_cast<const uint4*>(
+                               p.x + static_cast<long long>(ht[i]) * p.H + hg[i] * 128 + l * 8));
+            }
+            uint2 hc[kHold];
+            float hs[kHold];
+#pragma unroll
+            for (int i = 0; i < kHold; ++i) {
+                float a[8];
+                if (ha[i]) decode8(xv[i], a);
+                quant_group_codes_compact(a, ha[i], p.fmt, &hc[i], &hs[i]);
+            }
+            grid_dep_wait();  // route preparation is complete from here on
+            read_plan();
+#pragma unroll
+            for (int i = 0; i < kHold; ++i)
+                if (ha[i]) scatter(ht[i], hg[i], hc[i], hs[i]);
+            for (long long pr = lo + ewarp + 4LL * kHold; pr < hi; pr += 4) {
+                int t = 0, g = 0;
+                const bool act = item_of(pr, t, g);
+                float a[8];
+                if (act) decode8(__ldg(reinterpret_cast<const uint4*>(p.x + static_cast<long long>(t) * p.H + g * 128 + l * 8)), a);
+                uint2 codes;
+                float sc;
+                quant_group_codes_compact(a, act, p.fmt, &codes, &sc);
+                if (act) scatter(t, g, codes, sc);
             }
             fence_proxy_async_global();  // the quantised rows are read by TMA
         }
@@ -560,12 +666,8 @@ __global__ void __launch_bounds__(256, 1)
             const int b = d.hdr[1], nt0 = d.hdr[2], ntl = d.hdr[3], piece = d.hdr[4];
             const int c0 = d.hdr[5], nck = d.hdr[6], flags = d.hdr[7];
             const float* sT = down ? p.asT : p.xsT;
-            if (down) {
-                // acquire the block's act-quant results (scales read below)
-                bool okr = true;
-                if (lane == 0) okr = wait_counter(p.blk_ready + b, static_cast<unsigned>(d.hdr[8]), abort_flag, p.status);
-                if (!__shfl_sync(0xFFFFFFFFu, okr, 0)) return false;
-            }
+            // (down: the block's scales were published before the block entered the ready list,
+            // which the metadata warp acquired before writing this descriptor)
             for (int t = 0; t < ntl; ++t) {
                 if (flags & kFirst) {
 #pragma unroll
@@ -681,121 +783,157 @@ __global__ void __launch_bounds__(256, 1)
             if (flags & (kMarker | kEnd)) break;
         }
 
-        // ---- P2: fused act-quant of this CTA's slice of (route, group) items ----
-        // An item waits only for the gate/up pieces of its own block; when its codes and scale
-        // are stored it counts itself in the block's ready counter, which the down phase
-        // waits on.
+        // ---- P2: fused act-quant of the slots of this CTA's range of blocks ----
+        // The CTA walks its slots 32 at a time; every warp drops the pad slots of the chunk
+        // (ballot over sorted_idx) and the remaining (slot, group) items are dealt to the 8
+        // half-warps of the group, so a chunk takes one pass.  An item waits only for the
+        // gate/up pieces of its own block.  Every stored item, and warp 0 for the pad items of the
+        // chunk, counts itself in its block; the count that completes a block (BM * N/128)
+        // appends the block to the ready list.
         if (!*abort_flag) {
             const int GN = p.N / 128;
             const int W = 2 * p.N;
+            const unsigned blk_items = static_cast<unsigned>(BM * GN);
             const long long pstride = static_cast<long long>(rows1) * W;
-            const long long groups = static_cast<long long>(p.R) * GN;
-            const long long pairs = (groups + 1) / 2;
-            const long long lo = pairs * cta / G, hi = pairs * (cta + 1) / G;
-            for (long long pr = lo + ewarp; pr < hi; pr += 4) {
-                const long long item = pr * 2 + half;
-                bool active = item < groups;
-                int g = 0, m = -1;
-                if (active) {
-                    const int w = static_cast<int>(item / GN);
-                    g = static_cast<int>(item - static_cast<long long>(w) * GN);
-                    m = __ldcg(p.route_slot + w);
-                    if (m >= rows1) { if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX); m = -1; }
-                    active = m >= 0;
+            const long long s_lo = static_cast<long long>(nblk) * cta / G * BM;
+            const long long s_hi = static_cast<long long>(nblk) * (cta + 1) / G * BM;
+            bool stop = false;
+            auto count_in = [&](long long bb, unsigned cnt) {
+                const unsigned old = atomicAdd(p.blk_ready + bb, cnt);
+                if (old + cnt == blk_items) {
+                    // acquire the other items' stores of this block (each was released by a
+                    // fence + atomic), then publish the block
+                    __threadfence();
+                    const unsigned pos = atomicAdd(p.sync + 1, 1u);
+                    if (pos < static_cast<unsigned>(nblk))
+                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.ready_list + pos),
+                                     "r"(static_cast<unsigned>(bb) + 1u) : "memory");
                 }
-                const int b = active ? m / BM : 0;
-                {
-                    // wait (bounded, the whole warp) until every active item's block is stored
-                    const unsigned tgt = active ? 4u * block_pieces(b, p.NT1, p.KB1, W1, G1) : 0u;
-                    const uint64_t t0 = globaltimer_ns();
-                    for (;;) {
-                        const bool rdy = !active || ld_acquire_gpu(p.blk_done + b) >= tgt;
-                        if (__all_sync(0xFFFFFFFFu, rdy)) break;
-                        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
-                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                            if (lane == 0) {
-                                if (p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
-                                *abort_flag = 1;
-                            }
-                            __syncwarp();
-                        }
-                        __nanosleep(32);
+            };
+            for (long long base = s_lo; base < s_hi && !stop; base += 32) {
+                const long long m_l = base + lane;
+                const bool real = m_l < s_hi && __ldcg(p.sorted_idx + m_l) >= 0;
+                const unsigned mask = __ballot_sync(0xFFFFFFFFu, real);
+                const int n_items = __popc(mask) * GN;
+                for (int it0 = 2 * ewarp; it0 < n_items && !stop; it0 += 8) {
+                    const int it = it0 + half;
+                    const bool active = it < n_items;
+                    int m = static_cast<int>(base), g = 0;
+                    if (active) {
+                        const int kth = it / GN;
+                        g = it - kth * GN;
+                        unsigned mm = mask;
+                        for (int q2 = 0; q2 < kth; ++q2) mm &= mm - 1;
+                        m = static_cast<int>(base) + __ffs(mm) - 1;
                     }
-                    if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
-                }
-                float a[8];
-                if (active) {
-                    // gate tile g and up tile N/128 + g: each unit's pieces added in K order;
-                    // the loads of four pieces of both tiles are issued together
-                    const long long ug = static_cast<long long>(b) * p.NT1 + g;
-                    const long long uu = ug + GN;
-                    const int cg = cta_of(ug * p.KB1, W1, G1);
-                    const int cu = cta_of(uu * p.KB1, W1, G1);
-                    const int npg = cta_of(ug * p.KB1 + p.KB1 - 1, W1, G1) - cg + 1;
-                    const int npu = cta_of(uu * p.KB1 + p.KB1 - 1, W1, G1) - cu + 1;
-                    const float* srcg = p.gu + static_cast<long long>(m) * W + g * 128 + l * 8;
-                    const float* srcu = srcg + p.N;
-                    float gv[8], uv[8];
-                    const int npmax = max(npg, npu);
-                    for (int pc0 = 0; pc0 < npmax; pc0 += 4) {
-                        float4 ga[4], gb[4], ua[4], ub[4];
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            if (pc0 + q4 < npg) {
-                                const float* s2 = srcg + (pc0 + q4) * pstride;
-                                ga[q4] = *reinterpret_cast<const float4*>(s2);
-                                gb[q4] = *reinterpret_cast<const float4*>(s2 + 4);
+                    const int b = m / BM;
+                    {
+                        // wait (bounded, the whole warp) until every active item's block is stored
+                        const unsigned tgt = active ? 4u * block_pieces(b, p.NT1, p.KB1, W1, G1) : 0u;
+                        const uint64_t t0 = globaltimer_ns();
+                        for (;;) {
+                            const bool rdy = !active || ld_acquire_gpu(p.blk_done + b) >= tgt;
+                            if (__all_sync(0xFFFFFFFFu, rdy)) break;
+                            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+                            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                                if (lane == 0) {
+                                    if (p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
+                                    *abort_flag = 1;
+                                }
+                                __syncwarp();
                             }
-                            if (pc0 + q4 < npu) {
-                                const float* s2 = srcu + (pc0 + q4) * pstride;
-                                ua[q4] = *reinterpret_cast<const float4*>(s2);
-                                ub[q4] = *reinterpret_cast<const float4*>(s2 + 4);
-                            }
+                            __nanosleep(32);
                         }
+                        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) { stop = true; break; }
+                    }
+                    float a[8];
+                    if (active) {
+                        // gate tile g and up tile N/128 + g: each unit's pieces added in K order;
+                        // the loads of four pieces of both tiles are issued together
+                        const long long ug = static_cast<long long>(b) * p.NT1 + g;
+                        const long long uu = ug + GN;
+                        const int cg = cta_of(ug * p.KB1, W1, G1);
+                        const int cu = cta_of(uu * p.KB1, W1, G1);
+                        const int npg = cta_of(ug * p.KB1 + p.KB1 - 1, W1, G1) - cg + 1;
+                        const int npu = cta_of(uu * p.KB1 + p.KB1 - 1, W1, G1) - cu + 1;
+                        const float* srcg = p.gu + static_cast<long long>(m) * W + g * 128 + l * 8;
+                        const float* srcu = srcg + p.N;
+                        float gv[8], uv[8];
+                        const int npmax = max(npg, npu);
+                        for (int pc0 = 0; pc0 < npmax; pc0 += 4) {
+                            float4 ga[4], gb[4], ua[4], ub[4];
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int pc = pc0 + q4;
-                            if (pc < npg) {
-                                if (pc == 0) {
-                                    gv[0] = ga[0].x; gv[1] = ga[0].y; gv[2] = ga[0].z; gv[3] = ga[0].w;
-                                    gv[4] = gb[0].x; gv[5] = gb[0].y; gv[6] = gb[0].z; gv[7] = gb[0].w;
-                                } else {
-                                    gv[0] = __fadd_rn(gv[0], ga[q4].x); gv[1] = __fadd_rn(gv[1], ga[q4].y);
-                                    gv[2] = __fadd_rn(gv[2], ga[q4].z); gv[3] = __fadd_rn(gv[3], ga[q4].w);
-                                    gv[4] = __fadd_rn(gv[4], gb[q4].x); gv[5] = __fadd_rn(gv[5], gb[q4].y);
-                                    gv[6] = __fadd_rn(gv[6], gb[q4].z); gv[7] = __fadd_rn(gv[7], gb[q4].w);
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                if (pc0 + q4 < npg) {
+                                    const float* s2 = srcg + (pc0 + q4) * pstride;
+                                    ga[q4] = *reinterpret_cast<const float4*>(s2);
+                                    gb[q4] = *reinterpret_cast<const float4*>(s2 + 4);
+                                }
+                                if (pc0 + q4 < npu) {
+                                    const float* s2 = srcu + (pc0 + q4) * pstride;
+                                    ua[q4] = *reinterpret_cast<const float4*>(s2);
+                                    ub[q4] = *reinterpret_cast<const float4*>(s2 + 4);
                                 }
                             }
-                            if (pc < npu) {
-                                if (pc == 0) {
-                                    uv[0] = ua[0].x; uv[1] = ua[0].y; uv[2] = ua[0].z; uv[3] = ua[0].w;
-                                    uv[4] = ub[0].x; uv[5] = ub[0].y; uv[6] = ub[0].z; uv[7] = ub[0].w;
-                                } else {
-                                    uv[0] = __fadd_rn(uv[0], ua[q4].x); uv[1] = __fadd_rn(uv[1], ua[q4].y);
-                                    uv[2] = __fadd_rn(uv[2], ua[q4].z); uv[3] = __fadd_rn(uv[3], ua[q4].w);
-                                    uv[4] = __fadd_rn(uv[4], ub[q4].x); uv[5] = __fadd_rn(uv[5], ub[q4].y);
-                                    uv[6] = __fadd_rn(uv[6], ub[q4].z); uv[7] = __fadd_rn(uv[7], ub[q4].w);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const int pc = pc0 + q4;
+                                if (pc < npg) {
+                                    if (pc == 0) {
+                                        gv[0] = ga[0].x; gv[1] = ga[0].y; gv[2] = ga[0].z; gv[3] = ga[0].w;
+                                        gv[4] = gb[0].x; gv[5] = gb[0].y; gv[6] = gb[0].z; gv[7] = gb[0].w;
+                                    } else {
+                                        gv[0] = __fadd_rn(gv[0], ga[q4].x); gv[1] = __fadd_rn(gv[1], ga[q4].y);
+                                        gv[2] = __fadd_rn(gv[2], ga[q4].z); gv[3] = __fadd_rn(gv[3], ga[q4].w);
+                                        gv[4] = __fadd_rn(gv[4], gb[q4].x); gv[5] = __fadd_rn(gv[5], gb[q4].y);
+                                        gv[6] = __fadd_rn(gv[6], gb[q4].z); gv[7] = __fadd_rn(gv[7], gb[q4].w);
+                                    }
+                                }
+                                if (pc < npu) {
+                                    if (pc == 0) {
+                                        uv[0] = ua[0].x; uv[1] = ua[0].y; uv[2] = ua[0].z; uv[3] = ua[0].w;
+                                        uv[4] = ub[0].x; uv[5] = ub[0].y; uv[6] = ub[0].z; uv[7] = ub[0].w;
+                                    } else {
+                                        uv[0] = __fadd_rn(uv[0], ua[q4].x); uv[1] = __fadd_rn(uv[1], ua[q4].y);
+                                        uv[2] = __fadd_rn(uv[2], ua[q4].z); uv[3] = __fadd_rn(uv[3], ua[q4].w);
+                                        uv[4] = __fadd_rn(uv[4], ub[q4].x); uv[5] = __fadd_rn(uv[5], ub[q4].y);
+                                        uv[6] = __fadd_rn(uv[6], ub[q4].z); uv[7] = __fadd_rn(uv[7], ub[q4].w);
+                                    }
                                 }
                             }
                         }
+                        // (out of line: this runs once per item, where instruction fetch dominates)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            a[i] = silu_mul_bf16_rt(bf16_round_f32(gv[i]), bf16_round_f32(uv[i]), p.L, p.act);
                     }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) { gv[i] = bf16_round_f32(gv[i]); uv[i] = bf16_round_f32(uv[i]); }
-                    if (p.act == MOE_ACT_SILU_MUL_GATE_UPPER) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) a[i] = silu_mul_bf16<MOE_ACT_SILU_MUL_GATE_UPPER>(gv[i], uv[i], p.L);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) a[i] = silu_mul_bf16<MOE_ACT_SILU_MUL>(gv[i], uv[i], p.L);
+                    {
+                        uint2 codes;
+                        float sc;
+                        quant_group_codes_compact(a, active, p.fmt, &codes, &sc);
+                        if (active) {
+                            *reinterpret_cast<uint2*>(p.aq + static_cast<long long>(m) * p.N + g * 128 + l * 8) = codes;
+                            if (l == 0) p.asT[static_cast<long long>(g) * p.slots + m] = sc;
+                        }
+                    }
+                    fence_proxy_async_global();  // the quantised activations are read by TMA
+                    __threadfence();
+                    __syncwarp();
+                    if (active && l == 0) count_in(b, 1u);
+                }
+                if (stop) break;
+                // pad items of this chunk, counted once (warp 0)
+                if (ewarp == 0 && lane == 0) {
+                    const long long c_hi = min(base + 32, s_hi);
+                    for (long long bb = base / BM; bb * BM < c_hi; ++bb) {
+                        const long long lo_s = max(bb * BM, base), hi_s = min((bb + 1) * BM, c_hi);
+                        const unsigned slots_in = static_cast<unsigned>(hi_s - lo_s);
+                        unsigned reals = 0;
+                        for (long long mm = lo_s; mm < hi_s; ++mm) reals += (mask >> (mm - base)) & 1u;
+                        const unsigned pads = (slots_in - reals) * GN;
+                        if (pads) count_in(bb, pads);
                     }
                 }
-                quant_group_store(a, active, p.fmt,
-                                  p.aq + static_cast<long long>(max(m, 0)) * p.N + g * 128 + l * 8,
-                                  p.asT + static_cast<long long>(g) * p.slots + max(m, 0), l == 0);
-                fence_proxy_async_global();  // the quantised activations are read by TMA
-                __threadfence();
-                __syncwarp();
-                if (active && l == 0) atomicAdd(p.blk_ready + b, 1u);
             }
         }
 
@@ -811,43 +949,51 @@ __global__ void __launch_bounds__(256, 1)
             if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
             if (flags & kEnd) break;
         }
-        epi_phase_barrier(p.sync + 3, G, etid, abort_flag, p.status);
     }
 
     // ---- P4 (all 256 threads): weighted top-k reduce of this CTA's slice of (token,
-    // 8 columns) items ----
+    // 8 columns) items.  The ids, weights and keep flags of each thread's first item are
+    // loaded before the last grid counter, so only the z rows are read after it.
+    const int C8 = p.H / 8;
+    const long long items4 = static_cast<long long>(p.M) * C8;
+    const long long lo4 = items4 * cta / G, hi4 = items4 * (cta + 1) / G;
+    int ids8[8];
+    float w8[8];
+    bool keep8[8];
+    auto load_routes = [&](int t, int j0) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int r = t * p.k + j0 + jj;
+            const bool in = j0 + jj < p.k;
+            ids8[jj] = in ? __ldg(p.topk_ids + r) : -1;
+            w8[jj] = in ? __ldg(p.topk_w + r) : 0.0f;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int id = ids8[jj];
+            bool keep = id >= 0 && id < p.E;
+            if (keep && p.expert_map) {
+                const int le = __ldg(p.expert_map + id);
+                keep = le >= 0 && le < p.E_local;
+            }
+            keep8[jj] = keep;
+        }
+    };
+    long long it4 = lo4 + threadIdx.x;
+    if (it4 < hi4) load_routes(static_cast<int>(it4 / C8), 0);
+    if (warp >= 2 && warp <= 5)
+        epi_phase_barrier(p.sync + 3, G, static_cast<int>(threadIdx.x) - 64, abort_flag, p.status);
     __syncthreads();  // every role is done; the epilogue group has passed the last counter
     if (!*abort_flag) {
-        const int C8 = p.H / 8;
-        const long long items = static_cast<long long>(p.M) * C8;
-        const long long lo = items * cta / G, hi = items * (cta + 1) / G;
-        for (long long it = lo + threadIdx.x; it < hi; it += blockDim.x) {
-            const int t = static_cast<int>(it / C8);
-            const int col = static_cast<int>(it - static_cast<long long>(t) * C8) * 8;
+        bool first = true;
+        for (; it4 < hi4; it4 += blockDim.x) {
+            const int t = static_cast<int>(it4 / C8);
+            const int col = static_cast<int>(it4 - static_cast<long long>(t) * C8) * 8;
             float accr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             // routes in groups of eight: ids, weights and rows of a group are loaded together;
             // the multiply-adds run in top-k order
             for (int j0 = 0; j0 < p.k; j0 += 8) {
-                int ids8[8];
-                float w8[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int r = t * p.k + j0 + jj;
-                    const bool in = j0 + jj < p.k;
-                    ids8[jj] = in ? __ldg(p.topk_ids + r) : -1;
-                    w8[jj] = in ? __ldg(p.topk_w + r) : 0.0f;
-                }
-                bool keep8[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int id = ids8[jj];
-                    bool keep = id >= 0 && id < p.E;
-                    if (keep && p.expert_map) {
-                        const int le = __ldg(p.expert_map + id);
-                        keep = le >= 0 && le < p.E_local;
-                    }
-                    keep8[jj] = keep;
-                }
+                if (!(first && j0 == 0)) load_routes(t, j0);
                 uint4 v8[8];
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
@@ -869,6 +1015,7 @@ __global__ void __launch_bounds__(256, 1)
                     accr[7] = __fmaf_rn(wj, bf16_hi(v.w), accr[7]);
                 }
             }
+            first = false;
             uint4 o;
             o.x = f32_to_bf16_bits(accr[0]) | (f32_to_bf16_bits(accr[1]) << 16);
             o.y = f32_to_bf16_bits(accr[2]) | (f32_to_bf16_bits(accr[3]) << 16);
@@ -911,8 +1058,9 @@ size_t fused_partial_bytes(int B_cap, int bm, int H, int N, int G) {
     return best;
 }
 
-// Counter words of the fused kernel: 4 grid counters, then blk_done and blk_ready per block.
-int fused_counter_words(int B_cap) { return 4 + 2 * B_cap; }
+// Counter words of the fused kernel: 4 phase counters, then blk_done, blk_ready and the ready
+// list per block.
+int fused_counter_words(int B_cap) { return 4 + 3 * B_cap; }
 
 int launch_fused_layer(const FusedLaunch& f, cudaStream_t stream) {
     const int bm = f.bm;
@@ -943,6 +1091,7 @@ int launch_fused_layer(const FusedLaunch& f, cudaStream_t stream) {
     a.z = static_cast<uint16_t*>(f.z); a.out = static_cast<uint16_t*>(f.out);
     a.L = f.clamp_limit; a.act = f.act; a.fmt = f.fmt; a.w_tiled = tiled ? 1 : 0;
     a.sync = f.sync; a.blk_done = f.sync + 4; a.blk_ready = f.sync + 4 + f.B_cap;
+    a.ready_list = f.sync + 4 + 2 * f.B_cap;
     a.status = device_status_ptr();
     const void* fn;
     int smem;
