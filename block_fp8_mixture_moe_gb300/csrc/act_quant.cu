@@ -21,6 +21,8 @@
 // that strides over the group pairs, for filtered (expert-parallel) inputs and large outputs.
 #include "common.cuh"
 
+#include <algorithm>
+
 namespace moe {
 namespace {
 
@@ -40,6 +42,7 @@ struct AQArgs {
     uint8_t* out_q;
     float* out_s;
     int in_splits;
+    int map_early;  // row_map was written two or more launches back: read it before the wait
     int* status;
 };
 
@@ -90,7 +93,8 @@ __device__ __forceinline__ void load8(const AQArgs& p, long long off, float* v) 
 }
 
 // Decides whether work row `w` is produced, and its input and output rows.
-__device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, int* out_row) {
+__device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, int* out_row,
+                                           int pre_m = -2) {
     int src = w, dst = w;
     if (p.row_expert) {
         int id = __ldg(p.row_expert + w);
@@ -98,7 +102,7 @@ __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, 
         if (p.expert_map && __ldg(p.expert_map + id) < 0) return false;
     }
     if (p.row_map) {
-        int m = __ldg(p.row_map + w);
+        int m = pre_m != -2 ? pre_m : __ldg(p.row_map + w);
         if (m < 0) return false;
         dst = m;
         src = p.row_div > 0 ? w / p.row_div : m;
@@ -113,7 +117,7 @@ __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, 
 }
 
 template <int ACT, bool F32IN>
-__device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int lane) {
+__device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int lane, int pre_m = -2) {
     const int half = lane >> 4, l = lane & 15;
     const long long item = pair * 2 + half;
     bool active = item < static_cast<long long>(p.rows) * p.G;
@@ -121,7 +125,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
     if (active) {
         const int w = static_cast<int>(item / p.G);
         g = static_cast<int>(item - static_cast<long long>(w) * p.G);
-        active = row_source(p, w, &in_row, &row);
+        active = row_source(p, w, &in_row, &row, pre_m);
     }
     float a[8];
     if (active) {
@@ -133,29 +137,109 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
             float gv[8], uv[8];
             load8<F32IN>(p, rbase + col, gv);
             load8<F32IN>(p, rbase + p.N + col, uv);
+            // out of line: the kernel is short, so its instruction fetch, not its arithmetic,
+            // is what one warp waits for
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = silu_mul_bf16<ACT>(gv[i], uv[i], p.L);
+            for (int i = 0; i < 8; ++i) a[i] = silu_mul_bf16_rt(gv[i], uv[i], p.L, ACT);
         }
     }
     const long long o = static_cast<long long>(row) * p.N + static_cast<long long>(g) * 128 + l * 8;
-    quant_group_store(a, active, p.fmt, p.out_q + o, p.out_s + static_cast<long long>(row) * p.G + g,
-                      l == 0);
+    uint2 codes;
+    float sc;
+    quant_group_codes_compact(a, active, p.fmt, &codes, &sc);
+    if (active) {
+        *reinterpret_cast<uint2*>(p.out_q + o) = codes;
+        if (l == 0) p.out_s[static_cast<long long>(row) * p.G + g] = sc;
+    }
 }
 
 template <int ACT, bool F32IN, bool PERSISTENT>
 __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
-    grid_dep_wait();
-    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const long long warps_per_block = blockDim.x >> 5;
     const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
     long long pair = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
+    // the first pair's row map entry, when it was written two or more launches back
+    int pre_m = -2;
+    if (p.map_early && p.row_map && !p.row_expert && pair < pairs) {
+        const long long item = pair * 2 + (lane >> 4);
+        if (item < static_cast<long long>(p.rows) * p.G) pre_m = __ldcg(p.row_map + item / p.G);
+    }
+    grid_dep_wait();
+    grid_dep_launch();
     if (!PERSISTENT) {
-        if (pair < pairs) quant_pair<ACT, F32IN>(p, pair, lane);
+        if (pair < pairs) quant_pair<ACT, F32IN>(p, pair, lane, pre_m);
         return;
     }
     const long long stride = static_cast<long long>(gridDim.x) * warps_per_block;
-    for (; pair < pairs; pair += stride) quant_pair<ACT, F32IN>(p, pair, lane);
+    if (pair < pairs) quant_pair<ACT, F32IN>(p, pair, lane, pre_m);
+    for (pair += stride; pair < pairs; pair += stride) quant_pair<ACT, F32IN>(p, pair, lane);
+}
+
+// Input quantisation of the layer, once per token: every (token, 128-column group) is quantised
+// and its codes and scale are stored to the expert-sorted slot of each kept route of the token
+// (route_slot), giving exactly the rows the per-route gather of k_act_quant gives.  The token
+// rows are the caller's input, so a warp loads and quantises its first kHold items before
+// waiting for route preparation; only the stores wait for the routing.
+__global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __restrict__ x, int M,
+                                                            int H, int k, const int32_t* route_slot,
+                                                            int slots, uint8_t* xq, float* xs,
+                                                            int fmt, int* status) {
+    constexpr int kHold = 2;
+    const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
+    const int G = H / 128;
+    const long long groups = static_cast<long long>(M) * G;
+    const long long pairs = (groups + 1) / 2;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long w0 = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    auto quant = [&](long long pr, int& t, int& g, uint2& codes, float& sc) -> bool {
+        const long long item = pr * 2 + half;
+        const bool active = pr < pairs && item < groups;
+        float a[8];
+        t = 0; g = 0;
+        if (active) {
+            t = static_cast<int>(item / G);
+            g = static_cast<int>(item - static_cast<long long>(t) * G);
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * H + g * 128 + l * 8));
+            a[0] = bf16_lo(v.x); a[1] = bf16_hi(v.x); a[2] = bf16_lo(v.y); a[3] = bf16_hi(v.y);
+            a[4] = bf16_lo(v.z); a[5] = bf16_hi(v.z); a[6] = bf16_lo(v.w); a[7] = bf16_hi(v.w);
+        }
+        quant_group_codes_compact(a, active, fmt, &codes, &sc);
+        return active;
+    };
+    auto scatter = [&](int t, int g, uint2 codes, float sc) {
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            int ms[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                ms[jj] = j0 + jj < k ? __ldcg(route_slot + static_cast<long long>(t) * k + j0 + jj) : -1;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                int m = ms[jj];
+                if (m >= slots) { if (status) atomicOr(status, MOE_DEV_BAD_INDEX); m = -1; }
+                if (m < 0) continue;
+                *reinterpret_cast<uint2*>(xq + static_cast<long long>(m) * H + g * 128 + l * 8) = codes;
+                if (l == 0) xs[static_cast<long long>(m) * G + g] = sc;
+            }
+        }
+    };
+    uint2 hc[kHold];
+    float hs[kHold];
+    int ht[kHold], hg[kHold];
+    bool ha[kHold];
+#pragma unroll
+    for (int i = 0; i < kHold; ++i) ha[i] = quant(w0 + i * warps, ht[i], hg[i], hc[i], hs[i]);
+    grid_dep_wait();
+    grid_dep_launch();
+#pragma unroll
+    for (int i = 0; i < kHold; ++i)
+        if (ha[i]) scatter(ht[i], hg[i], hc[i], hs[i]);
+    for (long long pr = w0 + kHold * warps; pr < pairs; pr += warps) {
+        int t, g;
+        uint2 codes;
+        float sc;
+        if (quant(pr, t, g, codes, sc)) scatter(t, g, codes, sc);
+    }
 }
 
 // The unfused first half: BF16 SiLU*mul written to memory, 8 outputs per thread.
@@ -211,7 +295,8 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
                      int rows, int N, float clamp_limit, moe_scale_fmt fmt,
                      const int32_t* row_expert, const int32_t* expert_map, int E,
                      const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
-                     float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream) {
+                     float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream,
+                     bool map_early) {
     if (!in || !out_q || !out_s) { set_error("silu_mul_quant_fp8: null pointer"); return MOE_ERR_ARG; }
     if (!aligned16(in) || !aligned16(out_q) || (reinterpret_cast<uintptr_t>(out_s) & 3u)) {
         set_error("silu_mul_quant_fp8: in/out_q must be 16-byte aligned, out_s 4-byte aligned");
@@ -257,6 +342,7 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
     p.out_rows = out_rows;
     p.out_q = out_q;
     p.out_s = out_s;
+    p.map_early = map_early ? 1 : 0;
     p.status = device_status_ptr();
     bool persistent;
     if (strategy == MOE_QUANT_PER_GROUP) persistent = false;
@@ -274,6 +360,21 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
             return f32 ? launch_aq<MOE_ACT_SILU_MUL_GATE_UPPER, true>(p, persistent, pdl, stream)
                        : launch_aq<MOE_ACT_SILU_MUL_GATE_UPPER, false>(p, persistent, pdl, stream);
     }
+}
+
+int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t* route_slot,
+                              int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
+                              cudaStream_t stream) {
+    const long long pairs = (static_cast<long long>(M) * (H / 128) + 1) / 2;
+    if (pairs == 0) return MOE_OK;
+    // at most two CTAs per SM, so the next kernel's CTAs fit beside them
+    long long blocks = std::min<long long>((pairs + 7) / 8, static_cast<long long>(sm_count()) * 2);
+    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl);
+    cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_input_quant_tokens, static_cast<const uint16_t*>(x),
+                                       M, H, k, route_slot, slots, xq, xs, static_cast<int>(fmt),
+                                       device_status_ptr());
+    if (e != cudaSuccess) { set_error("input quant launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    return MOE_OK;
 }
 
 }  // namespace moe

@@ -7,7 +7,7 @@
 // and then one persistent kernel for steps 2-6 (fused_layer.cu); the staged path launches them
 // one by one:
 //   1. moe_route_prepare            topk_ids -> expert-sorted slots, compact blocks, route_slot
-//   2. silu_mul_quant_fp8(IDENTITY) x rows gathered into slot order, per-128 E4M3 + scales
+//   2. input quantisation           x rows quantised once per token, stored to the route slots
 //   3. grouped GEMM (GATE_UP)       fp32 split-K partials per slot
 //   4. silu_mul_quant_fp8(SILU_MUL) partials summed, BF16 materialised in registers, E4M3
 //   5. grouped GEMM (DOWN)          BF16 rows scattered back to route order
@@ -313,9 +313,7 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
         f.sync = sync;
         return launch_fused_layer(f, stream);
     }
-    rc = launch_act_quant(MOE_ACT_IDENTITY, x, MOE_DTYPE_BF16, 1, M, P.R, H, INFINITY, act_fmt,
-                          nullptr, nullptr, 0, route_slot, k, P.slots, xq, xs,
-                          MOE_QUANT_PERSISTENT, true, stream);
+    rc = launch_input_quant_tokens(x, M, H, k, route_slot, P.slots, xq, xs, act_fmt, true, stream);
     if (rc) return rc;
     rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
                              w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
@@ -323,7 +321,7 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     if (rc) return rc;
     rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
                           nullptr, nullptr, 0, route_slot, 0, P.slots, aq, as,
-                          MOE_QUANT_PERSISTENT, true, stream);
+                          MOE_QUANT_PERSISTENT, true, stream, /*map_early=*/true);
     if (rc) return rc;
     rc = launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, w_layout,
                              sorted_idx,

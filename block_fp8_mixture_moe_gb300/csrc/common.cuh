@@ -37,7 +37,12 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
                      int rows, int N, float clamp_limit, moe_scale_fmt fmt,
                      const int32_t* row_expert, const int32_t* expert_map, int E,
                      const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
-                     float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream);
+                     float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream,
+                     bool map_early = false);
+// Per-token input quantisation scattered to the route slots (the layer's first stage).
+int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t* route_slot,
+                              int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
+                              cudaStream_t stream);
 int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int32_t* expert_map,
                          int E_local, int block_m, moe_route_path path, int32_t* sorted_idx,
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,

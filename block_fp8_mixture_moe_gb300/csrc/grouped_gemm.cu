@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t* tempty = tfull + C::kTSlots;
     uint64_t* dfull = tempty + C::kTSlots;
     uint64_t* dempty = dfull + C::kRing;
-    uint64_t* mma_done = dempty + C::kRing;
+    uint64_t* dsa = dempty + C::kRing;  // the descriptor's token scales are written
+    uint64_t* mma_done = dsa + C::kRing;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -138,7 +139,11 @@ __global__ void __launch_bounds__(224, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
         for (int i = 0; i < C::kTSlots; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
-        for (int i = 0; i < C::kRing; ++i) { mbar_init(dfull + i, 32); mbar_init(dempty + i, 130); }
+        for (int i = 0; i < C::kRing; ++i) {
+            mbar_init(dfull + i, 32);
+            mbar_init(dempty + i, 130);
+            mbar_init(dsa + i, 32);
+        }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -157,8 +162,11 @@ __global__ void __launch_bounds__(224, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // everything below reads what earlier kernels on the stream wrote
-    grid_dep_wait();
+    // With programmatic dependent launch the previous kernel may still be running here.  The
+    // routing metadata (route preparation, complete before that kernel began) and the weights
+    // do not depend on it, so the metadata warp publishes the descriptor headers and the
+    // producer streams the first stages' weight tiles at once; only the activation tiles and
+    // token scales, which that kernel writes, wait for it (grid_dep_wait).
     grid_dep_launch();
 
     if (warp == 6) {
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(224, 1)
         // up to kSwMax / (K-blocks per unit) tiles; a unit longer than kCK K-blocks is cut into
         // one descriptor per kCK K-blocks.  All loads of a descriptor are issued before any of
         // its shared-memory stores.
-        int nblk = __ldg(p.num_blocks);
+        int nblk = __ldcg(p.num_blocks);
         nblk = max(0, min(nblk, p.B_cap));
         const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
         const long long u_lo = units * blockIdx.x / gridDim.x;
@@ -181,13 +189,14 @@ __global__ void __launch_bounds__(224, 1)
         int slot = 0;
         uint32_t ph = 0;
         bool ok = true;
+        bool dep_done = false;
         int cur_b = -1, e = -1;
         int rows[(BM + 31) / 32];
 #pragma unroll
         for (int t = 0; t < (BM + 31) / 32; ++t) rows[t] = -1;
         while (left > 0 && ok) {
             if (b != cur_b) {
-                const int e_raw = __ldg(p.block_expert + b);
+                const int e_raw = __ldcg(p.block_expert + b);
                 e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
                 if (e >= 0) {
 #pragma unroll
@@ -196,7 +205,7 @@ __global__ void __launch_bounds__(224, 1)
                         int row = -1;
                         if (j < BM) {
                             const int slot_j = b * BM + j;
-                            const int r = __ldg(p.sorted_idx + slot_j);
+                            const int r = __ldcg(p.sorted_idx + slot_j);
                             row = r < 0 ? -1 : (p.scatter ? r : slot_j);
                             if (row >= p.out_rows) {
                                 if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
@@ -218,16 +227,6 @@ __global__ void __launch_bounds__(224, 1)
                 adv = ntl;
                 for (int c0 = kb0; c0 < kb1 && ok; c0 += C::kCK) {
                     const int nck = min(C::kCK, kb1 - c0);
-                    // token scales: lane order (slot j, K-block kk) with kk fastest, so the
-                    // loads of one slot row are contiguous
-                    float sa_v[C::kCK * BM / 32];
-                    const int n_sa = nck * BM;
-#pragma unroll
-                    for (int q = 0; q < C::kCK * BM / 32; ++q) {
-                        const int i = q * 32 + lane;
-                        const int j = i / nck, kk = i - j * nck;
-                        sa_v[q] = i < n_sa ? __ldg(p.a_s + static_cast<long long>(b * BM + j) * p.KB + c0 + kk) : 0.0f;
-                    }
                     float sw_v[C::kSwMax / 32];
                     const int n_sw = ntl * nck;
 #pragma unroll
@@ -248,17 +247,29 @@ __global__ void __launch_bounds__(224, 1)
                     for (int t = 0; t < (BM + 31) / 32; ++t)
                         if (t * 32 + lane < BM) d.rows[t * 32 + lane] = rows[t];
 #pragma unroll
+                    for (int q = 0; q < C::kSwMax / 32; ++q) {
+                        const int i = q * 32 + lane;
+                        if (i < n_sw) d.sw[i] = sw_v[q];
+                    }
+                    mbar_arrive(dfull + slot);  // header, rows and weight scales
+                    if (!dep_done) { grid_dep_wait(); dep_done = true; }
+                    // token scales (written by the previous kernel): lane order (slot j,
+                    // K-block kk) with kk fastest, so the loads of one slot row are contiguous
+                    float sa_v[C::kCK * BM / 32];
+                    const int n_sa = nck * BM;
+#pragma unroll
+                    for (int q = 0; q < C::kCK * BM / 32; ++q) {
+                        const int i = q * 32 + lane;
+                        const int j = i / nck, kk = i - j * nck;
+                        sa_v[q] = i < n_sa ? __ldcg(p.a_s + static_cast<long long>(b * BM + j) * p.KB + c0 + kk) : 0.0f;
+                    }
+#pragma unroll
                     for (int q = 0; q < C::kCK * BM / 32; ++q) {
                         const int i = q * 32 + lane;
                         const int j = i / nck, kk = i - j * nck;
                         if (i < n_sa) d.sa[kk * BM + j] = sa_v[q];
                     }
-#pragma unroll
-                    for (int q = 0; q < C::kSwMax / 32; ++q) {
-                        const int i = q * 32 + lane;
-                        if (i < n_sw) d.sw[i] = sw_v[q];
-                    }
-                    mbar_arrive(dfull + slot);
+                    mbar_arrive(dsa + slot);
                     if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
                 }
             }
@@ -276,10 +287,16 @@ __global__ void __launch_bounds__(224, 1)
             if (__all_sync(0xFFFFFFFFu, ok)) {
                 if (lane == 0) desc_at<BM>(ring, slot).hdr[7] = kEnd;
                 mbar_arrive(dfull + slot);
+                mbar_arrive(dsa + slot);
             }
         }
     } else if (warp == 0) {
         // ---------------- TMA producer ----------------
+        // Until the previous kernel is done (grid_dep_wait) only the weight tiles are loaded; a
+        // stage's activation tiles are recorded and issued right after the wait, which happens
+        // when every stage holds weights, or before the second descriptor is read.  Each stage
+        // expects its full byte count from the start, so its barrier completes only when both
+        // halves have landed.
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_a = l2_policy_evict_last();
@@ -287,11 +304,29 @@ __global__ void __launch_bounds__(224, 1)
             uint32_t ph = 0, dph = 0;
             long long issued = 0;
             bool ok = true;
+            bool dep_done = false;
+            int npend = 0;
+            int pend_s[C::kStages], pend_kb[C::kStages], pend_nk[C::kStages], pend_b[C::kStages];
+            auto load_a = [&](int st_i, int kb, int nk, int b) {
+                uint8_t* st = smem + st_i * C::kStage;
+                for (int j = 0; j < nk; ++j)
+                    tma_load_2d(st + C::kKps * C::kWBytes + j * C::kABytes, &tmap_a, full + st_i,
+                                (kb + j) * 128, b * BM, pol_a);
+            };
+            auto resolve = [&]() {
+                grid_dep_wait();
+                dep_done = true;
+                for (int i = 0; i < npend; ++i) load_a(pend_s[i], pend_kb[i], pend_nk[i], pend_b[i]);
+                npend = 0;
+            };
+            long long ndesc = 0;
             while (ok) {
+                if (!dep_done && ndesc > 0) resolve();
                 if (!mbar_wait_fast(dfull + slot, dph, abort_flag, p.status)) break;
                 const Desc d = desc_at<BM>(ring, slot);
                 const int flags = d.hdr[7];
                 if (flags & kEnd) break;
+                ++ndesc;
                 const int e = d.hdr[0], b = d.hdr[1], nt0 = d.hdr[2], ntl = d.hdr[3];
                 const int c0 = d.hdr[5], nck = d.hdr[6];
                 mbar_arrive(dempty + slot);
@@ -304,6 +339,7 @@ __global__ void __launch_bounds__(224, 1)
                                                      : static_cast<long long>(e) * p.N_out + nt * 128;
                     for (int kb = c0; kb < c0 + nck; kb += C::kKps) {
                         const int nk = min(C::kKps, c0 + nck - kb);
+                        if (!dep_done && npend == C::kStages) resolve();  // every stage holds weights
                         if (!mbar_wait_fast(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                         uint8_t* st = smem + s * C::kStage;
                         mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(nk * (C::kWBytes + C::kABytes)));
@@ -315,14 +351,18 @@ __global__ void __launch_bounds__(224, 1)
                                 tma_load_2d(st + j * C::kWBytes, &tmap_w, full + s, (kb + j) * 128,
                                             static_cast<int>(wrow), pol_w);
                         }
-                        for (int j = 0; j < nk; ++j)
-                            tma_load_2d(st + C::kKps * C::kWBytes + j * C::kABytes, &tmap_a, full + s,
-                                        (kb + j) * 128, b * BM, pol_a);
+                        if (dep_done) {
+                            load_a(s, kb, nk, b);
+                        } else {
+                            pend_s[npend] = s; pend_kb[npend] = kb; pend_nk[npend] = nk; pend_b[npend] = b;
+                            ++npend;
+                        }
                         ++issued;
                         if (++s == C::kStages) { s = 0; ph ^= 1u; }
                     }
                 }
             }
+            if (!dep_done) resolve();  // no stage may stay without its activation tiles
             if (*abort_flag) {
                 // never leave a TMA write in flight: wait for the last load of every stage
                 for (int i = 0; i < C::kStages; ++i) {
@@ -386,8 +426,9 @@ __global__ void __launch_bounds__(224, 1)
         float acc[BM];
 #pragma unroll
         for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
+        grid_dep_wait();  // (returns at once: the activations it consumes come after it)
         for (;;) {
-            bool ok = mbar_wait_fast(dfull + slot, dph, abort_flag, p.status);
+            bool ok = mbar_wait_fast(dsa + slot, dph, abort_flag, p.status);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             const Desc d = desc_at<BM>(ring, slot);
             const int flags = d.hdr[7];

@@ -27,7 +27,6 @@ __global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__
                                                     int E, int H, uint16_t* __restrict__ out) {
     __shared__ float s_w[kMaxTopk];
     __shared__ int s_keep[kMaxTopk];
-    grid_dep_wait();
     grid_dep_launch();
     const int t = blockIdx.x;
     if (threadIdx.x < k) {
@@ -38,6 +37,9 @@ __global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__
         s_keep[j] = keep ? 1 : 0;
         s_w[j] = __ldg(w + static_cast<long long>(t) * k + j);
     }
+    // ids, weights and the expert map are the caller's inputs, not the previous kernel's
+    // outputs: they are read above; the expert outputs z are read after the wait
+    grid_dep_wait();
     __syncthreads();
     const int col = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
     if (col >= H) return;
@@ -45,7 +47,7 @@ __global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__
 #pragma unroll
     for (int j = 0; j < kMaxTopk; ++j)
         if (j < k && s_keep[j])
-            v[j] = __ldg(reinterpret_cast<const uint4*>(z + (static_cast<long long>(t) * k + j) * H + col));
+            v[j] = __ldcg(reinterpret_cast<const uint4*>(z + (static_cast<long long>(t) * k + j) * H + col));
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < kMaxTopk; ++j) {
