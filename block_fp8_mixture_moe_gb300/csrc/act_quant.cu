@@ -92,6 +92,54 @@ __device__ __forceinline__ void load8(const AQArgs& p, long long off, float* v) 
     }
 }
 
+// The gate and up inputs of one lane (8 values each).  For fp32 split-K partials the loads of
+// up to eight splits of both operands are in flight together, so a row with S splits costs
+// ceil(S / 8) dependent round trips to memory instead of one per four splits and operand; the
+// additions still run strictly in split order, starting from split 0.
+template <bool F32IN>
+__device__ __forceinline__ void load_gate_up(const AQArgs& p, long long off_g, long long off_u,
+                                             float* g, float* u) {
+    if (!F32IN) {
+        load8<false>(p, off_g, g);
+        load8<false>(p, off_u, u);
+        return;
+    }
+    constexpr int kGroup = 8;
+    const float* bg = static_cast<const float*>(p.in) + off_g;
+    const float* bu = static_cast<const float*>(p.in) + off_u;
+    for (int s0 = 0; s0 < p.in_splits; s0 += kGroup) {
+        float4 cg[kGroup][2], cu[kGroup][2];
+#pragma unroll
+        for (int t = 0; t < kGroup; ++t) {
+            if (s0 + t < p.in_splits) {
+                const long long so = static_cast<long long>(s0 + t) * p.split_stride;
+                const float4* qg = reinterpret_cast<const float4*>(bg + so);
+                const float4* qu = reinterpret_cast<const float4*>(bu + so);
+                cg[t][0] = __ldg(qg); cg[t][1] = __ldg(qg + 1);
+                cu[t][0] = __ldg(qu); cu[t][1] = __ldg(qu + 1);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kGroup; ++t) {
+            if (s0 + t < p.in_splits) {
+                const float vg[8] = {cg[t][0].x, cg[t][0].y, cg[t][0].z, cg[t][0].w,
+                                     cg[t][1].x, cg[t][1].y, cg[t][1].z, cg[t][1].w};
+                const float vu[8] = {cu[t][0].x, cu[t][0].y, cu[t][0].z, cu[t][0].w,
+                                     cu[t][1].x, cu[t][1].y, cu[t][1].z, cu[t][1].w};
+                if (s0 + t == 0) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) { g[i] = vg[i]; u[i] = vu[i]; }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) { g[i] = __fadd_rn(g[i], vg[i]); u[i] = __fadd_rn(u[i], vu[i]); }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { g[i] = bf16_round_f32(g[i]); u[i] = bf16_round_f32(u[i]); }
+}
+
 // Decides whether work row `w` is produced, and its input and output rows.
 __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, int* out_row,
                                            int pre_m = -2) {
@@ -135,8 +183,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
             load8<F32IN>(p, rbase + col, a);
         } else {
             float gv[8], uv[8];
-            load8<F32IN>(p, rbase + col, gv);
-            load8<F32IN>(p, rbase + p.N + col, uv);
+            load_gate_up<F32IN>(p, rbase + col, rbase + p.N + col, gv, uv);
             // out of line: the kernel is short, so its instruction fetch, not its arithmetic,
             // is what one warp waits for
 #pragma unroll

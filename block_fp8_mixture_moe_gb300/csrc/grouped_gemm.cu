@@ -14,7 +14,7 @@
 // a contiguous range of units (consecutive tiles of the same block).  num_blocks is read on the
 // device, so no work exists for inactive experts.
 //
-// Per CTA (224 threads, one CTA per SM):
+// Per CTA (352 threads; 224 for block_m = 128; one CTA per SM):
 //   warp 6        : metadata.  Walks this CTA's units ahead of everyone else and writes, per
 //                   chunk of up to CK K-blocks of a unit, a descriptor into a shared-memory
 //                   ring: expert, block, tile, K range, the block's output rows, and the token
@@ -26,12 +26,16 @@
 //   warp 1  lane 0: MMA issuer.  Per K-block: 4 tcgen05.mma (K = 32 each) into a fresh fp32
 //                   accumulator buffer in tensor memory, then tcgen05.commit frees the smem
 //                   stage and signals the accumulator buffer.
-//   warps 2-5     : epilogue / scale promotion.  Each thread owns one weight row; per K-block
-//                   it reads its block_m partial sums (tcgen05.ld, two buffers per wait when
-//                   block_m = 16), frees the buffer, and accumulates
-//                   partial * a_s[token, kb] * w_s[expert, tile, kb] in fp32 registers with the
-//                   scales read from the descriptor; at the end of the unit it writes BF16 or
-//                   fp32 (split-K partials) outputs to the rows the descriptor lists.
+//   warps 2-5, 7-10: epilogue / scale promotion, two warpgroups that take alternate units.
+//                   Each thread owns one weight row; per K-block it reads its block_m partial
+//                   sums (tcgen05.ld, two buffers per wait when block_m = 16), frees the
+//                   buffer, and accumulates partial * a_s[token, kb] * w_s[expert, tile, kb] in
+//                   fp32 registers with the scales read from the descriptor; at the end of the
+//                   unit it writes BF16 or fp32 (split-K partials) outputs to the rows the
+//                   descriptor lists.  A unit of the down projection (K = 256) is a single
+//                   pipeline stage, so one warpgroup's promotion and stores per unit would take
+//                   longer than the unit's weight tile takes to stream; with two warpgroups the
+//                   epilogue keeps up with HBM.
 // Block scales differ per K-block, so every K-block gets its own accumulator buffer; 4-8
 // buffers let the MMA run ahead of the promotion.  Every wait is bounded (see mbar_wait).
 #include "common.cuh"
@@ -66,7 +70,15 @@ struct Cfg {
     static constexpr int kKps = 2;                     // K-blocks per pipeline stage
     static constexpr int kStage = kKps * (kWBytes + kABytes);  // multiple of 1024
     static constexpr int kStages = BM <= 32 ? 5 : BM <= 64 ? 4 : 3;
-    static constexpr int kTSlots = BM <= 64 ? 4 : 2;   // tensor-memory slots of kKps accumulators
+    // two epilogue warpgroups, except for block_m = 128, whose 128 accumulators per thread need
+    // the register file of the 224-thread shape
+    static constexpr int kEpiGroups = BM <= 64 ? 2 : 1;
+    static constexpr int kEpiThreads = 128 * kEpiGroups;
+    static constexpr int kThreads = 96 + kEpiThreads;
+    // tensor-memory slots of kKps accumulators: each epilogue warpgroup owns its own ring of
+    // kTSlotsG slots
+    static constexpr int kTSlotsG = BM <= 32 ? 4 : 2;
+    static constexpr int kTSlots = kEpiGroups * kTSlotsG;
     static constexpr int kSlotCols = kKps * BM;
     static constexpr int kCols = kTSlots * kSlotCols <= 32 ? 32 : kTSlots * kSlotCols <= 64 ? 64
                                : kTSlots * kSlotCols <= 128 ? 128 : kTSlots * kSlotCols <= 256 ? 256 : 512;
@@ -79,7 +91,6 @@ struct Cfg {
     static constexpr int kDescBytes = ((kDescInts * 4) + 15) / 16 * 16;
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmem = kStages * kStage + kRing * kDescBytes + kBarBytes + 1024;
-    static constexpr int kThreads = 224;
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kTSlots * kSlotCols <= 512, "tensor memory holds 512 fp32 columns");
     static_assert(kCK % kKps == 0, "descriptors hold whole stages");
@@ -116,7 +127,7 @@ __device__ __forceinline__ Desc desc_at(uint8_t* ring, int slot) {
 }
 
 template <int BM>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_a, GemmArgs p) {
     using C = Cfg<BM>;
@@ -141,7 +152,7 @@ __global__ void __launch_bounds__(224, 1)
         for (int i = 0; i < C::kTSlots; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
         for (int i = 0; i < C::kRing; ++i) {
             mbar_init(dfull + i, 32);
-            mbar_init(dempty + i, 130);
+            mbar_init(dempty + i, C::kEpiThreads + 2);
             mbar_init(dsa + i, 32);
         }
         mbar_init(mma_done, 1);
@@ -377,8 +388,11 @@ __global__ void __launch_bounds__(224, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f8_f32(128, BM);
-            int s = 0, ts = 0, slot = 0;
-            uint32_t ph = 0, tph = 0, dph = 0;
+            int s = 0, slot = 0;
+            uint32_t ph = 0, dph = 0;
+            // one slot ring per epilogue warpgroup; units alternate between the groups
+            int ts0 = 0, ts1 = 0, unit = 0, owner = 0;
+            uint32_t tph0 = 0, tph1 = 0;
             bool ok = true;
             while (ok) {
                 if (!mbar_wait_fast(dfull + slot, dph, abort_flag, p.status)) break;
@@ -389,8 +403,11 @@ __global__ void __launch_bounds__(224, 1)
                 mbar_arrive(dempty + slot);
                 if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
                 for (int t = 0; t < ntl && ok; ++t) {
+                    if (flags & kFirst) owner = C::kEpiGroups == 1 ? 0 : ((unit++) & 1);
                     for (int kk = 0; kk < nck; kk += C::kKps) {
                         const int nk = min(C::kKps, nck - kk);
+                        const int ts = owner * C::kTSlotsG + (owner ? ts1 : ts0);
+                        const uint32_t tph = owner ? tph1 : tph0;
                         if (!mbar_wait_fast(tempty + ts, tph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                         if (!mbar_wait_fast(full + s, ph, abort_flag, p.status)) { ok = false; break; }
                         tc_fence_after();
@@ -406,7 +423,8 @@ __global__ void __launch_bounds__(224, 1)
                         mma_commit(empty + s);
                         mma_commit(tfull + ts);
                         if (++s == C::kStages) { s = 0; ph ^= 1u; }
-                        if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
+                        if (owner) { if (++ts1 == C::kTSlotsG) { ts1 = 0; tph1 ^= 1u; } }
+                        else { if (++ts0 == C::kTSlotsG) { ts0 = 0; tph0 ^= 1u; } }
                     }
                 }
             }
@@ -416,13 +434,19 @@ __global__ void __launch_bounds__(224, 1)
             mbar_wait(mma_done, 0, &no_abort, p.status);
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        // warp & 3 selects the 32-lane quarter of tensor memory this warp may read
+        // ---------------- epilogue (warps 2..5 and 7..10) ----------------
+        // warp & 3 selects the 32-lane quarter of tensor memory this warp may read.  Both
+        // warpgroups walk every descriptor; units (a unit starts at a kFirst tile) alternate
+        // between them, and each group reads only its own ring of tensor-memory slots.
         const int q = warp & 3;
+        const int wg = warp >= 7 ? 1 : 0;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         const int r_in_tile = q * 32 + lane;
         int ts = 0, slot = 0;
         uint32_t tph = 0, dph = 0;
+        const int ts_base = wg * C::kTSlotsG;
+        int unit = 0;
+        bool mine = false;
         float acc[BM];
 #pragma unroll
         for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
@@ -436,6 +460,8 @@ __global__ void __launch_bounds__(224, 1)
             const int nt0 = d.hdr[2], ntl = d.hdr[3], nck = d.hdr[6];
             const int sp = d.hdr[4];
             for (int t = 0; t < ntl; ++t) {
+                if (flags & kFirst) mine = C::kEpiGroups == 1 || ((unit++) & 1) == wg;
+                if (!mine) continue;
                 if (flags & kFirst) {
 #pragma unroll
                     for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
@@ -443,16 +469,16 @@ __global__ void __launch_bounds__(224, 1)
                 const float* swt = d.sw + t * nck;
                 for (int kk = 0; kk < nck; kk += C::kKps) {
                     const int nk = min(C::kKps, nck - kk);
-                    ok = mbar_wait_fast(tfull + ts, tph, abort_flag, p.status);
+                    ok = mbar_wait_fast(tfull + ts_base + ts, tph, abort_flag, p.status);
                     if (!__all_sync(0xFFFFFFFFu, ok)) goto epi_done;
                     tc_fence_after();
-                    const uint32_t t0 = lane_base + static_cast<uint32_t>(ts * C::kSlotCols);
+                    const uint32_t t0 = lane_base + static_cast<uint32_t>((ts_base + ts) * C::kSlotCols);
                     if (BM == 16) {
                         // both K-blocks of the stage: 32 adjacent columns, one load and one wait
                         float v[32];
                         tmem_ld32(t0, v);
                         tc_fence_before();
-                        mbar_arrive_relaxed(tempty + ts);
+                        mbar_arrive_relaxed(tempty + ts_base + ts);
 #pragma unroll
                         for (int j2 = 0; j2 < 2; ++j2) {
                             if (j2 < nk) {
@@ -484,9 +510,9 @@ __global__ void __launch_bounds__(224, 1)
                             }
                         }
                         tc_fence_before();
-                        mbar_arrive_relaxed(tempty + ts);
+                        mbar_arrive_relaxed(tempty + ts_base + ts);
                     }
-                    if (++ts == C::kTSlots) { ts = 0; tph ^= 1u; }
+                    if (++ts == C::kTSlotsG) { ts = 0; tph ^= 1u; }
                 }
                 if (flags & kLast) {
                     const int n = (nt0 + t) * 128 + r_in_tile;
