@@ -106,7 +106,8 @@ constexpr int kFirst = 1, kLast = 2, kEnd = 4;
 // K-blocks [kb0, kb0 + nck).  rows[j]: output row of slot j (-1: pad or dropped);
 // sa[kk * BM + j]: token scale of slot j at K-block kb0 + kk; sw[t * nck + kk]: weight-block
 // scale of tile nt0 + t at K-block kb0 + kk.  A descriptor with ntl > 1 covers each tile's
-// whole K range (kFirst | kLast).
+// whole K range (kFirst | kLast).  The header is released first (dfull), for the producer and
+// the MMA issuer; the rows and scales follow (dsa), for the epilogue.
 struct Desc {
     int* hdr;
     int* rows;
@@ -207,21 +208,23 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         for (int t = 0; t < (BM + 31) / 32; ++t) rows[t] = -1;
         while (left > 0 && ok) {
             if (b != cur_b) {
+                // the block's expert and its slot rows, loaded together
                 const int e_raw = __ldcg(p.block_expert + b);
+                int rr[(BM + 31) / 32];
+#pragma unroll
+                for (int t = 0; t < (BM + 31) / 32; ++t) {
+                    const int j = t * 32 + lane;
+                    rr[t] = j < BM ? __ldcg(p.sorted_idx + b * BM + j) : -1;
+                }
                 e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
                 if (e >= 0) {
 #pragma unroll
                     for (int t = 0; t < (BM + 31) / 32; ++t) {
-                        const int j = t * 32 + lane;
-                        int row = -1;
-                        if (j < BM) {
-                            const int slot_j = b * BM + j;
-                            const int r = __ldcg(p.sorted_idx + slot_j);
-                            row = r < 0 ? -1 : (p.scatter ? r : slot_j);
-                            if (row >= p.out_rows) {
-                                if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
-                                row = -1;
-                            }
+                        const int slot_j = b * BM + t * 32 + lane;
+                        int row = rr[t] < 0 ? -1 : (p.scatter ? rr[t] : slot_j);
+                        if (row >= p.out_rows) {
+                            if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                            row = -1;
                         }
                         rows[t] = row;
                     }
@@ -254,6 +257,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                         d.hdr[5] = c0; d.hdr[6] = nck;
                         d.hdr[7] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
                     }
+                    mbar_arrive(dfull + slot);  // the header: the producer and the MMA go ahead
 #pragma unroll
                     for (int t = 0; t < (BM + 31) / 32; ++t)
                         if (t * 32 + lane < BM) d.rows[t * 32 + lane] = rows[t];
@@ -262,7 +266,6 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                         const int i = q * 32 + lane;
                         if (i < n_sw) d.sw[i] = sw_v[q];
                     }
-                    mbar_arrive(dfull + slot);  // header, rows and weight scales
                     if (!dep_done) { grid_dep_wait(); dep_done = true; }
                     // token scales (written by the previous kernel): lane order (slot j,
                     // K-block kk) with kk fastest, so the loads of one slot row are contiguous
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                         const int j = i / nck, kk = i - j * nck;
                         if (i < n_sa) d.sa[kk * BM + j] = sa_v[q];
                     }
-                    mbar_arrive(dsa + slot);
+                    mbar_arrive(dsa + slot);  // rows, weight and token scales: the epilogue goes ahead
                     if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
                 }
             }
