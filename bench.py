@@ -12,6 +12,13 @@ from a CUDA graph; both paths are also timed and reported side by side.  Eight r
 and then read back between timed steps (outside the events), so no step starts with its
 weights in L2 and no dirty line of the flush is written back inside the timed region.
 
+Beside the headline, "configs" holds the other measured rows: every stage of the decode layer
+alone through its own entry point (device time, algorithmic bytes, fraction of the HBM peak),
+the fused SiLU*mul + quantisation against the two-kernel arm (clamped UE8M0 sweep and the decode
+shape), route preparation on both paths, and whole layers at the expert-parallel shape (T=1024
+tokens, 32 of 256 experts local) and at the prefill shape (M=512, Zipf routing), the latter with
+its FP8 MMA rate against the FP8 peak.  --no-configs skips them.
+
 Prints one JSON line.  --impl reference times the CPU oracle instead (a bounded token sample
 per step, scaled to the layer latency).
 """
@@ -46,6 +53,8 @@ def parse():
     ap.add_argument("--M", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-stage, act-quant, route-preparation, expert-parallel and prefill arms")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--weights", default="tiled", choices=["tiled", "row"],
                     help="expert weight layout: 128x128 tiles contiguous (packed once) or row-major")
@@ -280,6 +289,29 @@ def run_ours(args):
     e2e_ms, h2d, d2h = time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, args.steps, args.warmup)
     clocks = sampler.stop()
 
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    # FP8 dense peak: the measured bf16 GEMM peak times the nominal fp8 / bf16 ratio (2)
+    fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)
+    configs = None
+    if not args.no_configs:
+        from block_fp8_mixture_moe_gb300 import workloads as wl
+        configs = {
+            "stages_decode": dict(M=M, **stage_times(ops, dev, stream, flush, xs, ids, ws, wgu_use, wgu_s, wd_use,
+                                                     wd_s, M, H, N, E, k, act, hbm_peak)),
+            "act_quant": act_quant_arms(ops, dev, stream, flush),
+            "route_prepare_us": route_prep_arms(ops, dev, stream, flush),
+            "expert_parallel": layer_arm(ops, dev, stream, flush, dict(wl.CONFIGS["ep"], M=1024), 2, hbm_peak,
+                                         fp8_peak, clamp=7.0, fmt=1),
+            "prefill": layer_arm(ops, dev, stream, flush, wl.CONFIGS["prefill"], 3, hbm_peak, fp8_peak),
+            "fp8_peak_source": "measured bf16 GEMM peak x 2 (nominal fp8/bf16 ratio)" if "bf16_tflops" in peaks
+                              else "fallback bf16 1.9 PFLOP/s x 2",
+        }
+
     sweep = None
     if not args.no_sweep:
         sweep = {}
@@ -298,12 +330,6 @@ def run_ours(args):
                         "GBps": round(by / (us * 1e-6) / 1e9, 1)})
             sweep[str(Ms)] = row
 
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except Exception:
-        pass
-    hbm_peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     layer_us = ms_per_step * 1e3
     achieved = mean_bytes / (layer_us * 1e-6) / 1e9
@@ -356,12 +382,189 @@ def run_ours(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "sweep_M": sweep,
+        "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_events(fn, steps, warmup, flush, stream):
+    """Device time (ms) of fn() per call: L2 flushed before each call, the device kept busy while
+    the host enqueues (so the events time the GPU work, not the host), events on the stream."""
+    import torch
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            flush_l2(flush)
+            torch.cuda._sleep(2_000_000)
+            e0, e1 = make_event(), make_event()
+            e0.record(stream)
+            fn(i)
+            e1.record(stream)
+            if i >= warmup:
+                times.append((e0, e1))
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def stage_times(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, wd_q, wd_s, M, H, N, E, k,
+                act, hbm_peak, steps=50, warmup=5):
+    """Each stage of the staged layer through its own C-ABI entry point, on the decode inputs,
+    L2 flushed before each call: device time, algorithmic bytes, GB/s and fraction of the HBM
+    peak.  The input quantisation goes through the public per-route entry (silu_mul_quant_fp8,
+    identity, one gathered row per route); inside the layer forward the same codes come from a
+    per-token kernel that scatters each token's row to its routes' slots."""
+    import torch
+    bm, B_cap, splits = ops.moe_blockfp8_plan(M, k, E, E, H, N)
+    slots, R = B_cap * bm, M * k
+    with torch.cuda.stream(stream):
+        routes = [ops.moe_route_prepare(ids[r], E, None, E, bm, stream=stream) for r in range(NROT)]
+        xq = torch.zeros((slots, H), dtype=torch.uint8, device=dev)
+        xsc = torch.ones((slots, H // 128), dtype=torch.float32, device=dev)
+        gu = torch.zeros((splits, slots, 2 * N), dtype=torch.float32, device=dev)
+        aq = torch.zeros((slots, N), dtype=torch.uint8, device=dev)
+        asc = torch.ones((slots, N // 128), dtype=torch.float32, device=dev)
+        z = torch.zeros((R, H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        for r in range(NROT):  # one pass so every stage reads well-formed inputs
+            rt = routes[r]
+            ops.silu_mul_quant_fp8(0, xs[r], H, rows=R, row_map=rt["route_slot"], row_div=k,
+                                   out_rows=slots, out_q=xq, out_s=xsc, stream=stream)
+        torch.cuda.synchronize()
+    n_act = [a[0] for a in act]
+    mean_act = sum(n_act) / len(n_act)
+    gu_w = 2 * N * H + (2 * N // 128) * (H // 128) * 4
+    d_w = H * N + (H // 128) * (N // 128) * 4
+    stages = [
+        ("route_prepare", lambda i: ops.moe_route_prepare(ids[i % NROT], E, None, E, bm, stream=stream),
+         R * 4 + slots * 4 + R * 4),
+        ("input_quant", lambda i: ops.silu_mul_quant_fp8(0, xs[i % NROT], H, rows=R,
+                                                          row_map=routes[i % NROT]["route_slot"], row_div=k,
+                                                          out_rows=slots, out_q=xq, out_s=xsc, stream=stream),
+         M * 2 * H + R * (H + 4 * H // 128)),
+        ("gate_up_gemm", lambda i: ops.moe_blockfp8_grouped_gemm(0, xq, xsc, wgu_q, wgu_s, routes[i % NROT], bm,
+                                                                 out_dtype=ops.DTYPE_F32, out_rows=slots,
+                                                                 splits=splits, out=gu, stream=stream),
+         mean_act * gu_w + R * (H + 4 * H // 128) + R * 2 * N * 4 * splits),
+        ("act_quant", lambda i: ops.silu_mul_quant_fp8(1, gu, N, rows=R, row_map=routes[i % NROT]["route_slot"],
+                                                        out_rows=slots, out_q=aq, out_s=asc, in_splits=splits,
+                                                        strategy=2, stream=stream),
+         R * splits * 2 * N * 4 + R * (N + 4 * N // 128)),
+        ("down_gemm", lambda i: ops.moe_blockfp8_grouped_gemm(1, aq, asc, wd_q, wd_s, routes[i % NROT], bm,
+                                                              out_dtype=ops.DTYPE_BF16, out_rows=R, out=z,
+                                                              stream=stream),
+         mean_act * d_w + R * (N + 4 * N // 128) + R * 2 * H),
+        ("moe_reduce", lambda i: ops.moe_reduce(z, ws[i % NROT], ids[i % NROT], None, E, H, out=out, stream=stream),
+         R * 2 * H + M * 2 * H),
+    ]
+    res = {}
+    for name, fn, nbytes in stages:
+        t = time_events(fn, steps, warmup, flush, stream)
+        us = statistics.mean(t) * 1e3
+        gbps = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us": round(us, 2), "algorithmic_bytes": int(nbytes), "GBps": round(gbps, 1),
+                     "frac": round(gbps / hbm_peak, 4)}
+    res["sum_us"] = round(sum(v["us"] for v in res.values()), 2)
+    # the same protocol around a one-element fill: what a kernel costs here before it does work
+    one = torch.zeros(1, device=dev)
+    res["event_floor_us"] = round(statistics.mean(time_events(lambda i: one.fill_(1.0), steps, warmup,
+                                                              flush, stream)) * 1e3, 2)
+    res["note"] = ("each stage alone, L2 flushed before it; event_floor_us is the same protocol around a "
+                   "trivial kernel; the layer overlaps a stage's start with the previous stage's tail "
+                   "(programmatic dependent launch), so the layer is below the sum")
+    return res
+
+
+def act_quant_arms(ops, dev, stream, flush, steps=50, warmup=5):
+    """Fused SiLU*mul + quantisation against the two-kernel arm (BF16 SiLU*mul written to memory,
+    then quantised).  (1) the clamped UE8M0 sweep: rows 8*T, gate/up width 1024, activation width
+    512, clamp +-7; (2) the decode shape of the fused-vs-separate comparison: 8 routed rows
+    (M=1, top-8), activation width 256, fp32 scales."""
+    import torch
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    per_row = lambda n: 2 * (2 * n) + n + 4 * (n // 128)  # bf16 in, e4m3 + fp32 scales out
+    out = {"clamped_ue8m0_width512": {}, "decode_width256_f32": {}}
+    cases = [("clamped_ue8m0_width512", T, 8 * T, 512, 7.0, ops.SCALE_UE8M0) for T in wl.ACT_SWEEP_TOKENS]
+    cases.append(("decode_width256_f32", 1, 8, 256, float("inf"), ops.SCALE_F32))
+    for key, T, rows, n, clamp, fmt in cases:
+        bits = wl.act_rows(rows, 2 * n, 2.0 if clamp < 1e9 else 1.0, 31 + T)
+        x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        q = torch.empty((rows, n), dtype=torch.uint8, device=dev)
+        sc = torch.empty((rows, n // 128), dtype=torch.float32, device=dev)
+        fused = lambda i: ops.silu_mul_quant_fp8(1, x, n, clamp_limit=clamp, fmt=fmt, out_q=q, out_s=sc,
+                                                stream=stream)
+
+        def separate(i):
+            a = ops.silu_and_mul_bf16(1, x, n, clamp_limit=clamp, stream=stream)
+            ops.silu_mul_quant_fp8(0, a, n, fmt=fmt, out_q=q, out_s=sc, stream=stream)
+        tf = statistics.mean(time_events(fused, steps, warmup, flush, stream)) * 1e3
+        ts = statistics.mean(time_events(separate, steps, warmup, flush, stream)) * 1e3
+        out[key][str(rows)] = {"fused_us": round(tf, 2), "separate_us": round(ts, 2),
+                               "fused_GBps": round(rows * per_row(n) / (tf * 1e-6) / 1e9, 1)}
+    return out
+
+
+def route_prep_arms(ops, dev, stream, flush, steps=50, warmup=5):
+    """Route preparation alone: 512 routes over 256 experts (single CTA), 2048 routes over 512
+    experts on both paths, and the prefill's 4096 routes over 512 experts (multi-CTA)."""
+    import torch
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    res = {}
+    for M, E, path, name in ((64, 256, 1, "512_routes_256_experts_single"),
+                             (256, 512, 1, "2048_routes_512_experts_single"),
+                             (256, 512, 2, "2048_routes_512_experts_multi"),
+                             (512, 512, 2, "4096_routes_512_experts_multi")):
+        i, _ = wl.routing_topk(M, E, 8, seed=97 + M, kind="uniform")
+        ids = torch.from_numpy(i).to(dev)
+        fn = lambda it: ops.moe_route_prepare(ids, E, None, E, 16, path=path, stream=stream)
+        res[name] = round(statistics.mean(time_events(fn, steps, warmup, flush, stream)) * 1e3, 2)
+    return res
+
+
+def layer_arm(ops, dev, stream, flush, cfg, seed, hbm_peak, fp8_peak_tflops, steps=20, warmup=3,
+              clamp=float("inf"), fmt=0):
+    """One forward of a whole layer at a non-decode configuration (graph-replayed, L2 flushed
+    between steps): latency, active-expert weight bytes against HBM, and FP8 MMA flops against
+    the FP8 peak."""
+    import torch
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    M, H, N, E, k, El = cfg["M"], cfg["H"], cfg["N"], cfg["E"], cfg["k"], cfg["E_local"]
+    wgu_q, wgu_s = wl.quantized_weights(El, 2 * N, H, seed=seed * 7919 + 5, device=dev)
+    wd_q, wd_s = wl.quantized_weights(El, H, N, seed=seed * 7919 + 6, device=dev)
+    wgu_t, wd_t = ops.moe_blockfp8_pack_weights(wgu_q), ops.moe_blockfp8_pack_weights(wd_q)
+    del wgu_q, wd_q
+    i, w = wl.routing_topk(M, E, k, seed=seed * 7919 + 1, kind=cfg["routing"])
+    emap = None if El == E else wl.expert_map_random(E, El, seed * 7919 + 3)
+    x = wl.bf16_normal((M, H), 1.0, seed * 7919 + 4).to(dev)
+    ids, ws = torch.from_numpy(i).to(dev), torch.from_numpy(w).to(dev)
+    em = None if emap is None else torch.from_numpy(emap).to(dev)
+    work = torch.empty(ops.moe_blockfp8_workspace_bytes(M, k, E, El, H, N), dtype=torch.uint8, device=dev)
+    out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    fn = lambda: ops.moe_blockfp8_forward(x, ids, ws, E, em, wgu_t, wgu_s, wd_t, wd_s, clamp_limit=clamp,
+                                          act_fmt=fmt, out=out, workspace=work, stream=stream)
+    g = capture(fn, stream)
+    t = time_graph_steps([g], steps, warmup, flush, stream)
+    us = statistics.mean(t) * 1e3
+    loc = i[(i >= 0) & (i < E)]
+    if emap is not None:
+        loc = emap[loc]
+        loc = loc[loc >= 0]
+    counts = np.bincount(loc, minlength=El)
+    active = int((counts > 0).sum())
+    wbytes = active * (3 * H * N + ((2 * N // 128) * (H // 128) + (H // 128) * (N // 128)) * 4)
+    flops = 2.0 * 3 * H * N * int(counts.sum())
+    bm = ops.moe_forward_block_m(M, k, El, H, N)
+    return {"workload": f"M={M} H={H} N={N} E={E} E_local={El} top-k={k} {cfg['routing']} routing",
+            "block_m": bm, "us": round(us, 2), "active_experts": active, "routes_kept": int(counts.sum()),
+            "max_routes_per_expert": int(counts.max()),
+            "hbm": {"bytes": int(wbytes), "GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
+                    "frac": round(wbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)},
+            "fp8_mma": {"flops": flops, "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1),
+                        "frac": round(flops / (us * 1e-6) / 1e12 / fp8_peak_tflops, 4),
+                        "peak_TFLOPs": round(fp8_peak_tflops, 1)}}
 
 
 def padded_grid_route(route, E, bm, dev):
