@@ -508,14 +508,15 @@ def act_quant_arms(ops, dev, stream, flush, steps=50, warmup=5):
 
 
 def route_prep_arms(ops, dev, stream, flush, steps=50, warmup=5):
-    """Route preparation alone: 512 routes over 256 experts (single CTA), 2048 routes over 512
-    experts on both paths, and the prefill's 4096 routes over 512 experts (multi-CTA)."""
+    """Route preparation alone: 512 routes over 256 experts (single CTA), and 2048 and 4096 (the
+    prefill's) routes over 512 experts on both paths."""
     import torch
     from block_fp8_mixture_moe_gb300 import workloads as wl
     res = {}
     for M, E, path, name in ((64, 256, 1, "512_routes_256_experts_single"),
                              (256, 512, 1, "2048_routes_512_experts_single"),
                              (256, 512, 2, "2048_routes_512_experts_multi"),
+                             (512, 512, 1, "4096_routes_512_experts_single"),
                              (512, 512, 2, "4096_routes_512_experts_multi")):
         i, _ = wl.routing_topk(M, E, 8, seed=97 + M, kind="uniform")
         ids = torch.from_numpy(i).to(dev)

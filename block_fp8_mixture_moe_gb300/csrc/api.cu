@@ -108,10 +108,12 @@ namespace {
 
 int forward_block_m(int M, int k, int E_local, int H, int N) {
     (void)k; (void)E_local; (void)H; (void)N;
-    // Decode sizes: 16-token blocks measured fastest on GB300 up to M = 256 (each active expert's
-    // weights are streamed once per block, and fewer pad rows mean less promotion work).
+    // Measured on GB300 with the graph-replayed layer: 16-token blocks are fastest up to
+    // M = 256 (each active expert's weights are streamed once per block, and fewer pad rows mean
+    // less promotion work); above, 32-token blocks beat 64 at both the expert-parallel shape
+    // (M=1024, 6 of 256 experts per token, 32 local) and the Zipf prefill (M=512, E=512).
     if (M <= 256) return 16;
-    return 64;
+    return 32;
 }
 
 // Expected number of blocks under uniform routing, used only to size the split-K of the
