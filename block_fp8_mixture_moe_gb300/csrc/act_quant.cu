@@ -93,10 +93,11 @@ __device__ __forceinline__ void load8(const AQArgs& p, long long off, float* v) 
 }
 
 // The gate and up inputs of one lane (8 values each).  For fp32 split-K partials the loads of
-// up to eight splits of both operands are in flight together, so a row with S splits costs
-// ceil(S / 8) dependent round trips to memory instead of one per four splits and operand; the
-// additions still run strictly in split order, starting from split 0.
-template <bool F32IN>
+// up to KG splits of both operands are in flight together, so a row with S splits costs
+// ceil(S / KG) dependent round trips to memory; the additions still run strictly in split
+// order, starting from split 0.  KG follows the split count: the registers of the in-flight
+// loads bound how many warps an SM holds, and this kernel is latency-bound.
+template <bool F32IN, int KG>
 __device__ __forceinline__ void load_gate_up(const AQArgs& p, long long off_g, long long off_u,
                                              float* g, float* u) {
     if (!F32IN) {
@@ -104,7 +105,7 @@ __device__ __forceinline__ void load_gate_up(const AQArgs& p, long long off_g, l
         load8<false>(p, off_u, u);
         return;
     }
-    constexpr int kGroup = 8;
+    constexpr int kGroup = KG;
     const float* bg = static_cast<const float*>(p.in) + off_g;
     const float* bu = static_cast<const float*>(p.in) + off_u;
     for (int s0 = 0; s0 < p.in_splits; s0 += kGroup) {
@@ -164,7 +165,7 @@ __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, 
     return true;
 }
 
-template <int ACT, bool F32IN>
+template <int ACT, bool F32IN, int KG>
 __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int lane, int pre_m = -2) {
     const int half = lane >> 4, l = lane & 15;
     const long long item = pair * 2 + half;
@@ -183,7 +184,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
             load8<F32IN>(p, rbase + col, a);
         } else {
             float gv[8], uv[8];
-            load_gate_up<F32IN>(p, rbase + col, rbase + p.N + col, gv, uv);
+            load_gate_up<F32IN, KG>(p, rbase + col, rbase + p.N + col, gv, uv);
             // out of line: the kernel is short, so its instruction fetch, not its arithmetic,
             // is what one warp waits for
 #pragma unroll
@@ -200,7 +201,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
     }
 }
 
-template <int ACT, bool F32IN, bool PERSISTENT>
+template <int ACT, bool F32IN, bool PERSISTENT, int KG>
 __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     const int lane = threadIdx.x & 31;
     const long long warps_per_block = blockDim.x >> 5;
@@ -215,12 +216,25 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     grid_dep_wait();
     grid_dep_launch();
     if (!PERSISTENT) {
-        if (pair < pairs) quant_pair<ACT, F32IN>(p, pair, lane, pre_m);
+        if (pair < pairs) quant_pair<ACT, F32IN, KG>(p, pair, lane, pre_m);
         return;
     }
     const long long stride = static_cast<long long>(gridDim.x) * warps_per_block;
-    if (pair < pairs) quant_pair<ACT, F32IN>(p, pair, lane, pre_m);
-    for (pair += stride; pair < pairs; pair += stride) quant_pair<ACT, F32IN>(p, pair, lane);
+    // with a row map, each pair's map entry is loaded one pair ahead, so a pair whose route is
+    // dropped (most of them at expert-parallel shapes) costs no round trip of its own
+    const bool ahead = p.row_map && !p.row_expert;
+    const long long items = static_cast<long long>(p.rows) * p.G;
+    auto map_of = [&](long long pr) -> int {
+        const long long item = pr * 2 + (lane >> 4);
+        return (pr < pairs && item < items) ? __ldcg(p.row_map + item / p.G) : -1;
+    };
+    int cur = pre_m;
+    if (ahead && cur == -2) cur = map_of(pair);
+    for (; pair < pairs; pair += stride) {
+        const int nxt = ahead ? map_of(pair + stride) : -2;
+        quant_pair<ACT, F32IN, KG>(p, pair, lane, ahead ? cur : -2);
+        cur = nxt;
+    }
 }
 
 // Input quantisation of the layer, once per token: every (token, 128-column group) is quantised
@@ -315,25 +329,41 @@ __global__ void __launch_bounds__(256) k_silu_and_mul(const uint16_t* in, int ro
     }
 }
 
-template <int ACT, bool F32IN>
-int launch_aq(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream) {
+template <int ACT, bool F32IN, int KG>
+int launch_aq_kg(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream) {
     const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
     if (pairs == 0) return MOE_OK;
     const int threads = 256, wpb = threads / 32;
     long long blocks = (pairs + wpb - 1) / wpb;
     if (persistent) {
-        long long cap = static_cast<long long>(sm_count()) * 8;
+        // as many CTAs as are resident at once, so the grid runs in one wave
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_act_quant<ACT, F32IN, true, KG>, threads, 0) !=
+                cudaSuccess || occ < 1)
+            occ = 1;
+        long long cap = static_cast<long long>(sm_count()) * occ;
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7FFFFFFFLL) { set_error("act_quant: too many groups"); return MOE_ERR_ARG; }
     Launch L(dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, pdl);
-    cudaError_t e = persistent ? cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, true>, p)
-                               : cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, false>, p);
+    cudaError_t e = persistent ? cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, true, KG>, p)
+                               : cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, false, KG>, p);
     if (e != cudaSuccess) {
         set_error("act_quant launch: %s", cudaGetErrorString(e));
         return MOE_ERR_LAUNCH;
     }
     return MOE_OK;
+}
+
+template <int ACT, bool F32IN>
+int launch_aq(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream) {
+    if constexpr (!F32IN) {
+        return launch_aq_kg<ACT, F32IN, 1>(p, persistent, pdl, stream);
+    } else {
+        if (p.in_splits <= 1) return launch_aq_kg<ACT, F32IN, 1>(p, persistent, pdl, stream);
+        if (p.in_splits <= 4) return launch_aq_kg<ACT, F32IN, 4>(p, persistent, pdl, stream);
+        return launch_aq_kg<ACT, F32IN, 8>(p, persistent, pdl, stream);
+    }
 }
 
 }  // namespace
