@@ -43,6 +43,11 @@ struct AQArgs {
     float* out_s;
     int in_splits;
     int map_early;  // row_map was written two or more launches back: read it before the wait
+    // slot rows: row w is produced iff slot_route[w] >= 0 (input and output row w), and only
+    // rows below n_blocks[0] * bm exist (n_blocks read on the device)
+    const int32_t* slot_route;
+    const int32_t* n_blocks;
+    int bm;
     int* status;
 };
 
@@ -145,6 +150,7 @@ __device__ __forceinline__ void load_gate_up(const AQArgs& p, long long off_g, l
 __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, int* out_row,
                                            int pre_m = -2) {
     int src = w, dst = w;
+    if (p.slot_route && __ldcg(p.slot_route + w) < 0) return false;
     if (p.row_expert) {
         int id = __ldg(p.row_expert + w);
         if (id < 0 || id >= p.E) return false;
@@ -205,6 +211,12 @@ template <int ACT, bool F32IN, bool PERSISTENT, int KG>
 __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     const int lane = threadIdx.x & 31;
     const long long warps_per_block = blockDim.x >> 5;
+    if (p.n_blocks) {
+        // slot rows of the blocks that exist (the route preparation ran two or more launches
+        // back, so its count is read before the wait)
+        const long long nb = max(0, __ldcg(p.n_blocks));
+        p.rows = static_cast<int>(min(static_cast<long long>(p.rows), nb * p.bm));
+    }
     const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
     long long pair = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
     // the first pair's row map entry, when it was written two or more launches back
@@ -373,7 +385,7 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
                      const int32_t* row_expert, const int32_t* expert_map, int E,
                      const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
                      float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream,
-                     bool map_early) {
+                     bool map_early, const int32_t* slot_route, const int32_t* n_blocks, int bm) {
     if (!in || !out_q || !out_s) { set_error("silu_mul_quant_fp8: null pointer"); return MOE_ERR_ARG; }
     if (!aligned16(in) || !aligned16(out_q) || (reinterpret_cast<uintptr_t>(out_s) & 3u)) {
         set_error("silu_mul_quant_fp8: in/out_q must be 16-byte aligned, out_s 4-byte aligned");
@@ -420,6 +432,13 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
     p.out_q = out_q;
     p.out_s = out_s;
     p.map_early = map_early ? 1 : 0;
+    if (n_blocks && (!slot_route || bm <= 0 || row_map)) {
+        set_error("silu_mul_quant_fp8: slot rows need slot_route, bm > 0 and no row map");
+        return MOE_ERR_ARG;
+    }
+    p.slot_route = slot_route;
+    p.n_blocks = n_blocks;
+    p.bm = bm;
     p.status = device_status_ptr();
     bool persistent;
     if (strategy == MOE_QUANT_PER_GROUP) persistent = false;

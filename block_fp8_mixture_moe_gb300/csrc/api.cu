@@ -324,9 +324,17 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                              w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
                              MOE_DTYPE_F32, P.slots, P.splits, true, stream);
     if (rc) return rc;
-    rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
-                          nullptr, nullptr, 0, route_slot, 0, P.slots, aq, as,
-                          MOE_QUANT_PERSISTENT, true, stream, /*map_early=*/true);
+    // act-quant walks the routes (through route_slot) or, when the blocks hold fewer slots than
+    // there are routes (an expert map that keeps few of them), the slots of the blocks that exist
+    const bool slot_rows = expected_blocks(M, k, E, E_local, P.bm) * P.bm < P.R;
+    if (slot_rows)
+        rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.slots, N, clamp_limit, act_fmt,
+                              nullptr, nullptr, 0, nullptr, 0, P.slots, aq, as, MOE_QUANT_PERSISTENT,
+                              true, stream, false, sorted_idx, num_blocks, P.bm);
+    else
+        rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
+                              nullptr, nullptr, 0, route_slot, 0, P.slots, aq, as,
+                              MOE_QUANT_PERSISTENT, true, stream, /*map_early=*/true);
     if (rc) return rc;
     rc = launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, w_layout,
                              sorted_idx,
