@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--M", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    ap.add_argument("--layer", choices=["prefill", "ep"], default=None,
+                    help="only run this configuration's layer forward --steps times (no timing line): "
+                         "the command a profiler wraps")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="with --layer: number of experts (0 = the configuration's), for a small profiling case")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-stage, act-quant, route-preparation, expert-parallel and prefill arms")
     ap.add_argument("--seed", type=int, default=0)
@@ -525,6 +530,41 @@ def route_prep_arms(ops, dev, stream, flush, steps=50, warmup=5):
     return res
 
 
+def layer_only(args):
+    """--layer: the prefill or expert-parallel layer forward, run --steps times back to back, for
+    a profiler to wrap.  --experts shrinks the expert count (the expert-parallel shape keeps its
+    1/8 local fraction)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_fp8_mixture_moe_gb300 import ops, workloads as wl
+    dev = torch.device("cuda", 0)
+    cfg = dict(wl.CONFIGS["prefill"]) if args.layer == "prefill" else dict(wl.CONFIGS["ep"], M=1024)
+    if args.experts > 0:
+        cfg["E_local"] = max(1, cfg["E_local"] * args.experts // cfg["E"])
+        cfg["E"] = args.experts
+    seed = 3 if args.layer == "prefill" else 2
+    clamp, fmt = (float("inf"), 0) if args.layer == "prefill" else (7.0, 1)
+    M, H, N, E, k, El = cfg["M"], cfg["H"], cfg["N"], cfg["E"], cfg["k"], cfg["E_local"]
+    wgu_q, wgu_s = wl.quantized_weights(El, 2 * N, H, seed=seed * 7919 + 5, device=dev)
+    wd_q, wd_s = wl.quantized_weights(El, H, N, seed=seed * 7919 + 6, device=dev)
+    wgu_t, wd_t = ops.moe_blockfp8_pack_weights(wgu_q), ops.moe_blockfp8_pack_weights(wd_q)
+    del wgu_q, wd_q
+    i, w = wl.routing_topk(M, E, k, seed=seed * 7919 + 1, kind=cfg["routing"])
+    emap = None if El == E else torch.from_numpy(wl.expert_map_random(E, El, seed * 7919 + 3)).to(dev)
+    x = wl.bf16_normal((M, H), 1.0, seed * 7919 + 4).to(dev)
+    ids, ws = torch.from_numpy(i).to(dev), torch.from_numpy(w).to(dev)
+    work = torch.empty(ops.moe_blockfp8_workspace_bytes(M, k, E, El, H, N), dtype=torch.uint8, device=dev)
+    out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    for _ in range(max(1, args.steps)):
+        ops.moe_blockfp8_forward(x, ids, ws, E, emap, wgu_t, wgu_s, wd_t, wd_s, clamp_limit=clamp,
+                                 act_fmt=fmt, out=out, workspace=work)
+    torch.cuda.synchronize()
+    print(json.dumps({"layer": args.layer, "M": M, "H": H, "N": N, "E": E, "E_local": El, "k": k,
+                      "block_m": ops.moe_forward_block_m(M, k, El, H, N), "forwards": max(1, args.steps),
+                      "device_status": ops.device_status()}))
+
+
 def layer_arm(ops, dev, stream, flush, cfg, seed, hbm_peak, fp8_peak_tflops, steps=20, warmup=3,
               clamp=float("inf"), fmt=0):
     """One forward of a whole layer at a non-decode configuration (graph-replayed, L2 flushed
@@ -762,7 +802,9 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.layer:
+        layer_only(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)
