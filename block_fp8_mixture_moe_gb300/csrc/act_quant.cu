@@ -17,8 +17,9 @@
 // same loop and the full-mask shuffles never see a divergent partner.
 //
 // Two launch shapes (the pages' two strategies): PER_GROUP -- one warp per group pair, no loop,
-// for launch-bound decode shapes without a filter; PERSISTENT -- a grid sized to the SM count
-// that strides over the group pairs, for filtered (expert-parallel) inputs and large outputs.
+// for launch-bound decode shapes without a filter; PERSISTENT -- a grid of as many CTAs as are
+// resident at once that strides over the group pairs, for filtered (expert-parallel) inputs,
+// row maps and large outputs.
 #include "common.cuh"
 
 #include <algorithm>

@@ -15,7 +15,8 @@ Workloads (sizes from the pages; names describe what they are):
                    ~N(0, 2^2), clamp +-7, UE8M0 (vLLM PR #53875, "Kernel microbenchmarks");
 * ``ep``        -- k=6, E=256, 32 local experts through an expert map, H=N=2048, routed rows
                    {6, 60, 600, 6144} (vLLM PR #53875, DeepSeek-V4-style EP8 benchmark);
-* ``prefill``   -- M=512, H=4096, N=768, E=512, k=8, Zipf(1.1) expert popularity, block_m 64.
+* ``prefill``   -- M=512, H=4096, N=768, E=512, k=8, Zipf(1.1) expert popularity, block_m 64
+                   (the pages' tile; the layer's automatic choice on GB300 is 32).
 
 Weights are drawn ~N(0, 0.02) and stored as E4M3 with fp32 scales per 128x128 block (scale =
 block amax / 448, codes from torch's float8_e4m3fn cast); this stands in for the real
