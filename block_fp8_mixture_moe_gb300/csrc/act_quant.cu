@@ -297,6 +297,9 @@ __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __re
             }
         }
     };
+    // the next launch (the gate/up GEMM) may start at once: it waits for this one before it reads
+    // anything, so its set-up overlaps this kernel
+    grid_dep_launch();
     uint2 hc[kHold];
     float hs[kHold];
     int ht[kHold], hg[kHold];
@@ -304,7 +307,6 @@ __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __re
 #pragma unroll
     for (int i = 0; i < kHold; ++i) ha[i] = quant(w0 + i * warps, ht[i], hg[i], hc[i], hs[i]);
     grid_dep_wait();
-    grid_dep_launch();
 #pragma unroll
     for (int i = 0; i < kHold; ++i)
         if (ha[i]) scatter(ht[i], hg[i], hc[i], hs[i]);

@@ -322,7 +322,7 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     if (rc) return rc;
     rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
                              w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
-                             MOE_DTYPE_F32, P.slots, P.splits, true, stream);
+                             MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/true);
     if (rc) return rc;
     // act-quant walks the routes (through route_slot) or, when the blocks hold fewer slots than
     // there are routes (an expert map that keeps few of them), the slots of the blocks that exist

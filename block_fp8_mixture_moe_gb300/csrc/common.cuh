@@ -57,7 +57,7 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         moe_weight_layout w_layout, const int32_t* sorted_idx, const int32_t* block_expert,
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool wait_first = false);
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
                       const int32_t* expert_map, int M, int k, int E, int H, void* out, bool pdl,
                       cudaStream_t stream);

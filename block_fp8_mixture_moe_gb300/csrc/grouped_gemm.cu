@@ -61,6 +61,7 @@ struct GemmArgs {
     int out_f32, out_rows, splits, scatter;
     int w_tiled;
     int* status;
+    int wait_first;  // wait for the previous launch before anything (its predecessor is not done)
 };
 
 template <int BM>
@@ -178,7 +179,11 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     // routing metadata (route preparation, complete before that kernel began) and the weights
     // do not depend on it, so the metadata warp publishes the descriptor headers and the
     // producer streams the first stages' weight tiles at once; only the activation tiles and
-    // token scales, which that kernel writes, wait for it (grid_dep_wait).
+    // token scales, which that kernel writes, wait for it (grid_dep_wait).  With wait_first the
+    // previous kernel released this one before the routing it reads was complete: everything
+    // waits for it, and the next launch is released only after that wait, so that it may read
+    // the routing early too.
+    if (p.wait_first) grid_dep_wait();
     grid_dep_launch();
 
     if (warp == 6) {
@@ -619,7 +624,7 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         moe_weight_layout w_layout, const int32_t* sorted_idx, const int32_t* block_expert,
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool wait_first) {
     if (proj != MOE_PROJ_GATE_UP && proj != MOE_PROJ_DOWN) { set_error("grouped_gemm: bad proj"); return MOE_ERR_ARG; }
     if (!a_q || !a_s || !w_q || !w_s || !sorted_idx || !block_expert || !num_blocks || !out) {
         set_error("grouped_gemm: null pointer");
@@ -685,6 +690,7 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
     p.scatter = proj == MOE_PROJ_DOWN;
     p.w_tiled = tiled ? 1 : 0;
     p.status = device_status_ptr();
+    p.wait_first = wait_first ? 1 : 0;
     const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
     switch (block_m) {
         case 16: return launch_bm<16>(tw, ta, p, max_units, pdl, stream);
