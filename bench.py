@@ -160,16 +160,36 @@ def active_bytes(ids_list, H, N, E):
 
 
 def make_inputs(M, seed, dev):
+    """The layer inputs of each routing batch: x [M, H] bf16, topk_ids [M, k] i32 and topk_w
+    [M, k] f32, laid out back to back (256-byte aligned) in one device buffer, so that one copy
+    moves a step's inputs from the host."""
     import torch
     from block_fp8_mixture_moe_gb300 import workloads as wl
+    H, k = DECODE["H"], DECODE["k"]
+    al = lambda n: (n + 255) // 256 * 256
+    o_ids = al(M * H * 2)
+    o_w = o_ids + al(M * k * 4)
     xs, ids, ws = [], [], []
     for r in range(NROT):
-        i, w = wl.routing_topk(M, DECODE["E"], DECODE["k"], seed=seed * 1000 + r, kind="uniform")
-        x = wl.bf16_normal((M, DECODE["H"]), 1.0, seed * 1000 + 500 + r)
-        xs.append(x.to(dev))
-        ids.append(torch.from_numpy(i).to(dev))
-        ws.append(torch.from_numpy(w).to(dev))
+        i, w = wl.routing_topk(M, DECODE["E"], k, seed=seed * 1000 + r, kind="uniform")
+        x = wl.bf16_normal((M, H), 1.0, seed * 1000 + 500 + r)
+        buf = torch.zeros(o_w + M * k * 4, dtype=torch.uint8, device=dev)
+        xv = buf[:M * H * 2].view(torch.bfloat16).view(M, H)
+        iv = buf[o_ids:o_ids + M * k * 4].view(torch.int32).view(M, k)
+        wv = buf[o_w:o_w + M * k * 4].view(torch.float32).view(M, k)
+        xv.copy_(x.to(dev))
+        iv.copy_(torch.from_numpy(i).to(dev))
+        wv.copy_(torch.from_numpy(w).to(dev))
+        xs.append(xv)
+        ids.append(iv)
+        ws.append(wv)
     return xs, ids, ws
+
+
+def packed_buffer(t):
+    """The whole device buffer a make_inputs view lives in."""
+    import torch
+    return torch.empty(0, dtype=torch.uint8, device=t.device).set_(t.untyped_storage())
 
 
 def capture(fn, stream):
@@ -677,14 +697,14 @@ def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, M, H
 
 
 def time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, steps, warmup):
-    """Per step: host->device copy of x, topk_ids, topk_w from pinned host buffers, the layer
-    (graph of moe_blockfp8_forward), device->host copy of the output; events around all of it."""
+    """Per step: one host->device copy of the step's inputs (x, topk_ids and topk_w, packed in
+    one pinned host buffer that mirrors the device buffer the layer reads), the layer (graph of
+    moe_blockfp8_forward), the device->host copy of the output; events around all of it."""
     import torch
-    hx = [x.cpu().pin_memory() for x in xs]
-    hi = [t.cpu().pin_memory() for t in ids]
-    hw = [t.cpu().pin_memory() for t in ws]
+    dbuf = [packed_buffer(x) for x in xs]
+    hbuf = [b.cpu().pin_memory() for b in dbuf]
     ho = [o.cpu().pin_memory() for o in outs]
-    h2d = hx[0].numel() * 2 + hi[0].numel() * 4 + hw[0].numel() * 4
+    h2d = hbuf[0].numel()
     d2h = ho[0].numel() * 2
     evs = []
     with torch.cuda.stream(stream):
@@ -693,9 +713,7 @@ def time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, steps, warmup):
             flush_l2(flush)
             e0, e1 = make_event(), make_event()
             e0.record(stream)
-            xs[r].copy_(hx[r], non_blocking=True)
-            ids[r].copy_(hi[r], non_blocking=True)
-            ws[r].copy_(hw[r], non_blocking=True)
+            dbuf[r].copy_(hbuf[r], non_blocking=True)
             graphs[r].replay()
             ho[r].copy_(outs[r], non_blocking=True)
             e1.record(stream)
