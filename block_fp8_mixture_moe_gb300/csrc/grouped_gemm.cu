@@ -71,15 +71,19 @@ struct Cfg {
     static constexpr int kKps = 2;                     // K-blocks per pipeline stage
     static constexpr int kStage = kKps * (kWBytes + kABytes);  // multiple of 1024
     static constexpr int kStages = BM <= 32 ? 5 : BM <= 64 ? 4 : 3;
-    // two epilogue warpgroups, except for block_m = 128, whose 128 accumulators per thread need
-    // the register file of the 224-thread shape
-    static constexpr int kEpiGroups = BM <= 64 ? 2 : 1;
+    // two epilogue warpgroups.  block_m <= 32: they take alternate units, each with its own
+    // ring of tensor-memory slots.  block_m >= 64 (column split): both take every unit, each the
+    // promotion of half of its block_m token columns, on one shared ring
+    static constexpr int kEpiGroups = 2;
     static constexpr int kEpiThreads = 128 * kEpiGroups;
     static constexpr int kThreads = 96 + kEpiThreads;
-    // tensor-memory slots of kKps accumulators: each epilogue warpgroup owns its own ring of
-    // kTSlotsG slots
-    static constexpr int kTSlotsG = BM <= 32 ? 4 : 2;
-    static constexpr int kTSlots = kEpiGroups * kTSlotsG;
+    static constexpr bool kColSplit = BM >= 64;
+    static constexpr int kCpw = kColSplit ? BM / 2 : BM;  // accumulator columns per thread
+    static constexpr int kRings = kColSplit ? 1 : 2;
+    // tensor-memory slots of kKps accumulators: kTSlotsG per ring
+    static constexpr int kTSlotsG = BM <= 64 ? 4 : 2;
+    static constexpr int kTSlots = kRings * kTSlotsG;
+    static constexpr int kTemptyArrivals = kColSplit ? 256 : 128;
     static constexpr int kSlotCols = kKps * BM;
     static constexpr int kCols = kTSlots * kSlotCols <= 32 ? 32 : kTSlots * kSlotCols <= 64 ? 64
                                : kTSlots * kSlotCols <= 128 ? 128 : kTSlots * kSlotCols <= 256 ? 256 : 512;
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
-        for (int i = 0; i < C::kTSlots; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
+        for (int i = 0; i < C::kTSlots; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, C::kTemptyArrivals); }
         for (int i = 0; i < C::kRing; ++i) {
             mbar_init(dfull + i, 32);
             mbar_init(dempty + i, C::kEpiThreads + 2);
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                 mbar_arrive(dempty + slot);
                 if (++slot == C::kRing) { slot = 0; dph ^= 1u; }
                 for (int t = 0; t < ntl && ok; ++t) {
-                    if (flags & kFirst) owner = C::kEpiGroups == 1 ? 0 : ((unit++) & 1);
+                    if (flags & kFirst) owner = C::kRings == 1 ? 0 : ((unit++) & 1);
                     for (int kk = 0; kk < nck; kk += C::kKps) {
                         const int nk = min(C::kKps, nck - kk);
                         const int ts = owner * C::kTSlotsG + (owner ? ts1 : ts0);
@@ -452,12 +456,13 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         const int r_in_tile = q * 32 + lane;
         int ts = 0, slot = 0;
         uint32_t tph = 0, dph = 0;
-        const int ts_base = wg * C::kTSlotsG;
+        const int ts_base = C::kColSplit ? 0 : wg * C::kTSlotsG;
+        const int c0 = C::kColSplit ? wg * C::kCpw : 0;  // this thread's first token column
         int unit = 0;
         bool mine = false;
-        float acc[BM];
+        float acc[C::kCpw];
 #pragma unroll
-        for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < C::kCpw; ++j) acc[j] = 0.0f;
         grid_dep_wait();  // (returns at once: the activations it consumes come after it)
         for (;;) {
             bool ok = mbar_wait_fast(dsa + slot, dph, abort_flag, p.status);
@@ -468,11 +473,11 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
             const int nt0 = d.hdr[2], ntl = d.hdr[3], nck = d.hdr[6];
             const int sp = d.hdr[4];
             for (int t = 0; t < ntl; ++t) {
-                if (flags & kFirst) mine = C::kEpiGroups == 1 || ((unit++) & 1) == wg;
+                if (flags & kFirst) mine = C::kColSplit || ((unit++) & 1) == wg;
                 if (!mine) continue;
                 if (flags & kFirst) {
 #pragma unroll
-                    for (int j = 0; j < BM; ++j) acc[j] = 0.0f;
+                    for (int j = 0; j < C::kCpw; ++j) acc[j] = 0.0f;
                 }
                 const float* swt = d.sw + t * nck;
                 for (int kk = 0; kk < nck; kk += C::kKps) {
@@ -507,11 +512,11 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                     } else {
                         for (int j2 = 0; j2 < nk; ++j2) {
                             const float sw = swt[kk + j2];
-                            const float* sa = d.sa + (kk + j2) * BM;
+                            const float* sa = d.sa + (kk + j2) * BM + c0;
 #pragma unroll
-                            for (int c = 0; c < BM / 32; ++c) {
+                            for (int c = 0; c < C::kCpw / 32; ++c) {
                                 float v[32];
-                                tmem_ld32(t0 + static_cast<uint32_t>(j2 * BM + c * 32), v);
+                                tmem_ld32(t0 + static_cast<uint32_t>(j2 * BM + c0 + c * 32), v);
 #pragma unroll
                                 for (int i = 0; i < 32; ++i)
                                     acc[c * 32 + i] = __fmaf_rn(v[i], __fmul_rn(sa[c * 32 + i], sw), acc[c * 32 + i]);
@@ -527,11 +532,11 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                     // row indices are read into registers 16 at a time before the stores, so no
                     // shared-memory load is ordered between global stores through generic pointers
 #pragma unroll
-                    for (int j0 = 0; j0 < BM; j0 += 16) {
+                    for (int j0 = 0; j0 < C::kCpw; j0 += 16) {
                         int rws[16];
 #pragma unroll
                         for (int j4 = 0; j4 < 4; ++j4) {
-                            const int4 r4 = reinterpret_cast<const int4*>(d.rows + j0)[j4];
+                            const int4 r4 = reinterpret_cast<const int4*>(d.rows + c0 + j0)[j4];
                             rws[j4 * 4 + 0] = r4.x; rws[j4 * 4 + 1] = r4.y;
                             rws[j4 * 4 + 2] = r4.z; rws[j4 * 4 + 3] = r4.w;
                         }
