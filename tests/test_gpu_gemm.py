@@ -54,6 +54,8 @@ def _oracle_rows(ref_route, aq, a_s, wq_h, ws_h, bm):
     (64, 8, 512, 512, 64, 1024, 384, "zipf"),       # skewed routing, block_m 64
     (300, 2, 4, 4, 128, 512, 256, "uniform"),       # many tokens per expert, block_m 128
     (5, 3, 7, 7, 16, 128, 128, "uniform"),          # one K-block, one tile
+    (128, 4, 4, 4, 16, 1024, 256, "uniform"),       # runs of 8 blocks of one expert
+    (600, 2, 2, 2, 16, 256, 384, "uniform"),        # runs longer than 32 blocks
 ])
 def test_gemm_bf16_vs_oracle(ops, proj, M, k, E, E_loc, bm, K, N_out, kind, tiled):
     route, rr, aq, a_s, wq, ws = _setup(ops, M, k, E, E_loc, bm, K, N_out, kind, seed=M + K)
