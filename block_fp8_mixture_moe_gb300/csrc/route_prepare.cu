@@ -40,6 +40,7 @@ struct RouteArgs {
     int R, E;
     const int32_t* map;
     int E_loc, bm, B_cap;
+    int bm_shift;  // log2(bm): bm is a power of two, so block arithmetic is shifts
     int32_t* sorted_idx;
     int32_t* block_expert;
     int32_t* num_blocks;
@@ -177,16 +178,16 @@ __device__ __forceinline__ void warp_scatter(const RouteArgs& p, const int* loc,
 // Writes counts, offsets, num_blocks, the block table and every -1 pad from the expert totals
 // `tot` and the padded starts `start` (start[E_loc] = padded total).
 __device__ void write_metadata(const RouteArgs& p, const int* tot, const int* start) {
-    const int nb = start[p.E_loc] / p.bm;
+    const int nb = start[p.E_loc] >> p.bm_shift;
     for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x) {
         p.count[e] = tot[e];
         if (p.offset) p.offset[e] = start[e];
-        for (int b = start[e] / p.bm; b < start[e + 1] / p.bm; ++b) p.block_expert[b] = e;
+        for (int b = start[e] >> p.bm_shift; b < (start[e + 1] >> p.bm_shift); ++b) p.block_expert[b] = e;
         for (int s = start[e] + tot[e]; s < start[e + 1]; ++s) p.sorted_idx[s] = -1;
     }
     for (int b = nb + threadIdx.x; b < p.B_cap; b += blockDim.x) p.block_expert[b] = -1;
-    for (long long s = static_cast<long long>(nb) * p.bm + threadIdx.x;
-         s < static_cast<long long>(p.B_cap) * p.bm; s += blockDim.x)
+    for (long long s = (static_cast<long long>(nb) << p.bm_shift) + threadIdx.x;
+         s < (static_cast<long long>(p.B_cap) << p.bm_shift); s += blockDim.x)
         p.sorted_idx[s] = -1;
     if (threadIdx.x == 0) {
         *p.num_blocks = nb;
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
     column_scan(wcnt, kSingleWarps, p.E_loc, tot);
     __syncthreads();
     for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x)
-        start[e] = (tot[e] + p.bm - 1) / p.bm * p.bm;
+        start[e] = ((tot[e] + p.bm - 1) >> p.bm_shift) << p.bm_shift;
     __syncthreads();
     const int total = block_exclusive_scan(start, p.E_loc, tmp);
     if (threadIdx.x == 0) start[p.E_loc] = total;
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(1024) k_route_count(RouteArgs p) {
             run += v;
         }
         tot[e] = run;
-        start[e] = (run + p.bm - 1) / p.bm * p.bm;
+        start[e] = ((run + p.bm - 1) >> p.bm_shift) << p.bm_shift;
     }
     __syncthreads();
     const int total = block_exclusive_scan(start, p.E_loc, tmp);
@@ -366,6 +367,7 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
     p.map = expert_map;
     p.E_loc = E_local;
     p.bm = block_m;
+    p.bm_shift = block_m == 16 ? 4 : block_m == 32 ? 5 : block_m == 64 ? 6 : 7;
     p.B_cap = (R + block_m - 1) / block_m + std::min(E_local, R);
     p.sorted_idx = sorted_idx;
     p.block_expert = block_expert;
@@ -566,6 +568,7 @@ extern "C" int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, 
     p.map = expert_map;
     p.E_loc = E_local;
     p.bm = block_m;
+    p.bm_shift = block_m == 16 ? 4 : block_m == 32 ? 5 : block_m == 64 ? 6 : 7;
     p.B_cap = static_cast<int>((R + block_m - 1) / block_m + std::min<long long>(E_local, R));
     p.sorted_idx = sorted_idx;
     p.block_expert = block_expert;
