@@ -296,8 +296,9 @@ def run_ours(args):
     # ---- both paths of the same layer, for comparison ----------------------------------------
     path_ms = {}
     for pth, nm in ((ops.FORWARD_FUSED, "fused"), (ops.FORWARD_STAGED, "staged")):
-        _, _, _, _, _, g_p = layer_graphs(M, pth)
-        path_ms[nm] = time_graph_steps(g_p, min(args.steps, 200), args.warmup, flush, stream)
+        arm = layer_graphs(M, pth)  # the graphs write into these tensors: kept alive while replayed
+        path_ms[nm] = time_graph_steps(arm[-1], min(args.steps, 200), args.warmup, flush, stream)
+        del arm
         del g_p
 
     # ---- the gate/up GEMM of the staged path alone, events on its stream --------------------
@@ -344,9 +345,10 @@ def run_ours(args):
         for Ms in (1, 4, 16, 32, 64, 128, 256):
             row = {}
             for pth, nm in ((ops.FORWARD_FUSED, "fused"), (ops.FORWARD_STAGED, "staged")):
-                _, ids_s, _, _, _, g_s = layer_graphs(Ms, pth)
-                t = time_graph_steps(g_s, 50, 5, flush, stream)
-                del g_s
+                arm = layer_graphs(Ms, pth)  # kept alive while its graphs are replayed
+                ids_s = arm[1]
+                t = time_graph_steps(arm[-1], 50, 5, flush, stream)
+                del arm
                 row[nm + "_us"] = round(statistics.mean(t) * 1e3, 2)
             a_s = active_bytes([t.cpu().numpy() for t in ids_s], H, N, E)
             by = sum(a_s[i % NROT][1] + a_s[i % NROT][2] for i in range(50)) / 50
