@@ -151,3 +151,78 @@ def test_forward_is_deterministic_and_graph_capturable(ops, path):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, first)
+
+
+@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("M", (64, 128, 256))
+def test_decode_large_m_sampled(ops, M, path):
+    """The decode sweep's larger batches (H=7168, N=256, E=256, k=8), compared on a token
+    sample: each token's output depends only on its own routes, so a sampled oracle row is
+    exactly the full-run row."""
+    cfg = dict(wl.CONFIGS["decode"], M=M)
+    L = wl.make_layer(**cfg, seed=6, device="cuda")
+    got = _run(ops, L, tiled=True, path=path)
+    toks = np.unique(np.concatenate([np.random.default_rng(M).choice(M, 12, replace=False), [0, M - 1]]))
+    ref = oracle.moe_forward(_host(L, toks), tokens=toks)
+    assert_bf16_close(got[toks], ref[toks], f"decode M={M} sample")
+
+
+@pytest.mark.parametrize("path", [FUSED, STAGED])
+def test_decode_hot_experts(ops, path):
+    """Decode shape with every route on 12 hot experts (64 routes each, so several block_m=16
+    blocks per expert and 244 idle experts)."""
+    M, E, k = 96, 256, 8
+    cfg = dict(wl.CONFIGS["decode"], M=M)
+    L = wl.make_layer(**cfg, seed=7, device="cuda")
+    r = np.random.default_rng(7)
+    hot = r.choice(E, 12, replace=False)
+    ids = np.stack([hot[r.permutation(12)[:k]] for _ in range(M)]).astype(np.int32)
+    w = r.random((M, k)).astype(np.float32) + 0.05
+    L["topk_ids"], L["topk_w"] = ids, (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    got = _run(ops, L, tiled=True, path=path)
+    toks = np.unique(np.concatenate([r.choice(M, 16, replace=False), [0, M - 1]]))
+    ref = oracle.moe_forward(_host(L, toks), tokens=toks)
+    assert_bf16_close(got[toks], ref[toks], "hot experts sample")
+
+
+@pytest.mark.parametrize("path", [FUSED, STAGED])
+def test_graphs_with_different_routings_share_a_workspace(ops, path):
+    """Three captured forwards with different routings on one workspace, replayed in a mixed
+    order: every replay reproduces its own eager output bit for bit, so no state (counters,
+    block tables, cleared regions) carries over from the previous call."""
+    cfg = dict(wl.CONFIGS["decode"], M=16)
+    L = wl.make_layer(**cfg, seed=8, device="cuda")
+    M, H, E, k = 16, cfg["H"], cfg["E"], cfg["k"]
+    x = bf16_to_dev(L["x"])
+    routes = []
+    for s in range(3):
+        i, w = wl.routing_topk(M, E, k, seed=100 + s, kind="uniform")
+        routes.append((to_dev(i), to_dev(w)))
+    need = ops.moe_blockfp8_workspace_bytes(M, k, E, E, H, cfg["N"])
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((M, H), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    eager = []
+    for s in range(3):
+        ops.moe_blockfp8_forward(x, routes[s][0], routes[s][1], E, None, L["wgu_q"], L["wgu_s"],
+                                 L["wd_q"], L["wd_s"], out=outs[s], workspace=ws, path=path)
+        eager.append(outs[s].clone())
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(st):
+        torch.cuda.synchronize()
+        for s in range(3):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                ops.moe_blockfp8_forward(x, routes[s][0], routes[s][1], E, None, L["wgu_q"],
+                                         L["wgu_s"], L["wd_q"], L["wd_s"], out=outs[s],
+                                         workspace=ws, stream=st, path=path)
+            graphs.append(g)
+        for s in (0, 1, 2, 0, 2, 1, 1, 0):
+            outs[s].zero_()
+            graphs[s].replay()
+            st.synchronize()
+            assert torch.equal(outs[s], eager[s]), f"replay of routing {s} differs"
+    assert ops.device_status() == 0
+    for s in range(3):
+        assert not torch.equal(eager[s], eager[(s + 1) % 3])
