@@ -299,7 +299,6 @@ def run_ours(args):
         arm = layer_graphs(M, pth)  # the graphs write into these tensors: kept alive while replayed
         path_ms[nm] = time_graph_steps(arm[-1], min(args.steps, 200), args.warmup, flush, stream)
         del arm
-        del g_p
 
     # ---- the gate/up GEMM of the staged path alone, events on its stream --------------------
     gemm_ms = time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_use, wgu_s,
