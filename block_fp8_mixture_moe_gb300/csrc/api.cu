@@ -198,6 +198,22 @@ extern "C" const char* moe_last_error_string(void) { return g_err; }
 
 extern "C" int moe_device_supported(void) { return device_is_sm103() ? 1 : 0; }
 
+extern "C" int moe_pointer_device_accessible(const void* p) {
+    if (!p) return 0;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // an unregistered host pointer: clear the error, answer no
+        return 0;
+    }
+    switch (a.type) {
+        case cudaMemoryTypeDevice: return a.device == current_device() ? 1 : 0;
+        case cudaMemoryTypeManaged: return 1;
+        // pinned host memory: usable in kernels only where the device sees it at the same address
+        case cudaMemoryTypeHost: return a.devicePointer == p ? 1 : 0;
+        default: return 0;
+    }
+}
+
 extern "C" int moe_get_device_status(int* status, int reset) {
     clear_error();
     if (!status) { set_error("moe_get_device_status: null status"); return MOE_ERR_ARG; }

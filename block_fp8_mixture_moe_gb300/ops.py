@@ -52,6 +52,7 @@ SIGNATURES = {
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_get_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "moe_device_supported": (_I, []),
+    "moe_pointer_device_accessible": (_I, [_P]),
 }
 
 _lib = None
@@ -84,6 +85,22 @@ def _ptr(t):
         return None
     assert t.is_cuda and t.is_contiguous(), "device tensors must be contiguous CUDA tensors"
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _io_ptr(t):
+    """A forward activation (x, topk_ids, topk_w, out): a CUDA tensor, or a pinned host tensor
+    that the device reaches at the same address (the kernels then move its bytes themselves)."""
+    if t.is_cuda:
+        return _ptr(t)
+    assert t.is_contiguous() and t.is_pinned(), "host activations must be contiguous pinned tensors"
+    p = ctypes.c_void_p(t.data_ptr())
+    if not load().moe_pointer_device_accessible(p):
+        raise MoeError("pinned host tensor is not device-accessible at its host address")
+    return p
+
+
+def pointer_device_accessible(t) -> bool:
+    return bool(load().moe_pointer_device_accessible(ctypes.c_void_p(t.data_ptr())))
 
 
 def _stream(stream=None):
@@ -293,7 +310,9 @@ def moe_blockfp8_plan(M, k, E, E_local, H, N, block_m=0):
 def moe_blockfp8_forward(x, topk_ids, topk_w, E, expert_map, wgu_q, wgu_s, wd_q, wd_s,
                          act=ACT_SILU_MUL, clamp_limit=float("inf"), act_fmt=SCALE_F32,
                          block_m=0, out=None, workspace=None, stream=None, path=FORWARD_AUTO):
-    """The whole layer.  x: bf16 [M, H]; weights as uint8 E4M3 codes + fp32 block scales."""
+    """The whole layer.  x: bf16 [M, H]; weights as uint8 E4M3 codes + fp32 block scales.
+    x, topk_ids, topk_w and out may be pinned host tensors (read and written by the kernels
+    across the host link); the weights, expert_map and workspace are CUDA tensors."""
     L = load()
     assert x.dtype == torch.bfloat16 and topk_ids.dtype == torch.int32 and topk_w.dtype == torch.float32
     assert expert_map is None or expert_map.dtype == torch.int32
@@ -303,13 +322,14 @@ def moe_blockfp8_forward(x, topk_ids, topk_w, E, expert_map, wgu_q, wgu_s, wd_q,
     _, H_d, N, layout_d = _weight_dims(wd_q)
     assert layout == layout_d and H_d == H, "both weight tensors must use the same layout"
     need = L.moe_blockfp8_workspace_bytes(M, k, E, E_local, H, N, block_m)
+    dev = wgu_q.device
     if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     if out is None:
-        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
-    rc = L.moe_blockfp8_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), M, k, E, _ptr(expert_map),
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    rc = L.moe_blockfp8_forward(_io_ptr(x), _io_ptr(topk_ids), _io_ptr(topk_w), M, k, E, _ptr(expert_map),
                                 E_local, H, N, _ptr(wgu_q), _ptr(wgu_s), _ptr(wd_q), _ptr(wd_s), layout, act,
-                                float(clamp_limit), act_fmt, block_m, path, _ptr(out), _ptr(workspace),
+                                float(clamp_limit), act_fmt, block_m, path, _io_ptr(out), _ptr(workspace),
                                 workspace.numel(), _stream(stream))
     _check(rc, "moe_blockfp8_forward")
     return out

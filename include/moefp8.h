@@ -6,7 +6,10 @@
  * ---------------------------------------
  * - All tensor pointers are DEVICE pointers owned by the caller; the library keeps no pointer
  *   after the call returns and allocates no device memory on these paths (scratch space is the
- *   caller's `workspace`).
+ *   caller's `workspace`).  One exception: moe_blockfp8_forward also takes its activations
+ *   (x, topk_ids, topk_w, out) in pinned host memory that the device reaches at the same
+ *   address (moe_pointer_device_accessible); its kernels then read the inputs and write the
+ *   output across the host link themselves, with no separate copy.
  * - Every call only enqueues work on `stream` and never synchronises it.  Routing metadata that
  *   the device produces (num_blocks, ...) stays on the device; the kernels read it there.
  * - Layouts are row-major and dense.  BF16 tensors are passed as `void*` (IEEE bfloat16 bit
@@ -249,6 +252,12 @@ MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* top
  *   moe_forward_path_for.
  * H and N multiples of 128.  All stages run on `stream` with no host synchronisation, so the
  * call can be captured in a CUDA graph.
+ * x, topk_ids, topk_w and out may be device memory or pinned host memory that the device sees
+ * at the same address (cudaHostAlloc / cudaHostRegister under unified addressing; check with
+ * moe_pointer_device_accessible): the input quantisation, route preparation and reduce kernels
+ * read x, topk_ids and topk_w and write out directly there (each byte crosses the host link
+ * once; the call is still asynchronous, so the host reads out after synchronising `stream`).
+ * The weights, expert_map and workspace must be device memory.
  * ------------------------------------------------------------------------------------------ */
 MOEFP8_API size_t moe_blockfp8_workspace_bytes(int M, int k, int E, int E_local, int H, int N, int block_m);
 MOEFP8_API int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, const float* topk_w, int M,
@@ -282,6 +291,10 @@ MOEFP8_API const char* moe_last_error_string(void);
 MOEFP8_API int moe_get_device_status(int* status, int reset);
 /* 1 if the current device is an sm_103 GPU the library was built for, else 0. */
 MOEFP8_API int moe_device_supported(void);
+/* 1 if kernels on the current device can dereference p as it is: device memory of this device,
+ * managed memory, or pinned host memory mapped at the same address; else 0 (also for null and
+ * for pageable host memory).  Host only, no device work. */
+MOEFP8_API int moe_pointer_device_accessible(const void* p);
 
 #ifdef __cplusplus
 }

@@ -79,6 +79,11 @@ def test_calls_without_a_gpu_fail_cleanly(lib_path):
     from block_fp8_mixture_moe_gb300 import ops
     L = ops.load(lib_path)
     assert L.moe_device_supported() == 0
+    # no device: no pointer is device-accessible (null and plain host memory included)
+    import ctypes
+    buf = ctypes.create_string_buffer(64)
+    assert L.moe_pointer_device_accessible(None) == 0
+    assert L.moe_pointer_device_accessible(ctypes.cast(buf, ctypes.c_void_p)) == 0
     rc = L.moe_reduce(None, None, None, None, 1, 1, 1, 8, None, None)
     assert rc == ops.MOE_ERR_UNSUPPORTED
     assert L.moe_last_error_string()

@@ -226,3 +226,30 @@ def test_graphs_with_different_routings_share_a_workspace(ops, path):
     assert ops.device_status() == 0
     for s in range(3):
         assert not torch.equal(eager[s], eager[(s + 1) % 3])
+
+
+@pytest.mark.parametrize("path", [FUSED, STAGED])
+def test_host_activations_zero_copy(ops, path):
+    """x, topk_ids, topk_w and out in pinned host memory: the kernels read and write them across
+    the host link, bit for bit the result of the same call on device copies (decode M=16, and
+    an expert-parallel slice with dropped routes and UE8M0 scales)."""
+    cases = [(dict(wl.CONFIGS["decode"], M=16), 9, {}),
+             (dict(wl.CONFIGS["ep"], M=10), 10, dict(clamp_limit=7.0, act_fmt=1))]
+    for cfg, seed, kw in cases:
+        L = wl.make_layer(**cfg, seed=seed, device="cuda")
+        emap = None if L["expert_map"] is None else to_dev(L["expert_map"])
+        x_d, ids_d, w_d = bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"])
+        args = (L["E"], emap, L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"])
+        ref = ops.moe_blockfp8_forward(x_d, ids_d, w_d, *args, path=path, **kw)
+        x_h, ids_h, w_h = x_d.cpu().pin_memory(), ids_d.cpu().pin_memory(), w_d.cpu().pin_memory()
+        out_h = torch.empty(ref.shape, dtype=torch.bfloat16).pin_memory()
+        for t in (x_h, ids_h, w_h, out_h):
+            assert ops.pointer_device_accessible(t)
+        ops.moe_blockfp8_forward(x_h, ids_h, w_h, *args, out=out_h, path=path, **kw)
+        torch.cuda.synchronize()
+        assert ops.device_status() == 0
+        assert torch.equal(out_h, ref.cpu())
+    # pageable host memory is refused before anything is launched
+    assert not ops.pointer_device_accessible(torch.zeros(4))
+    with pytest.raises(AssertionError):
+        ops.moe_blockfp8_forward(x_d.cpu(), ids_d, w_d, *args, path=path, **kw)
