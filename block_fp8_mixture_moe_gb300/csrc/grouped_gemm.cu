@@ -62,6 +62,7 @@ struct GemmArgs {
     int w_tiled;
     int* status;
     int wait_first;  // wait for the previous launch before anything (its predecessor is not done)
+    int pdl;         // launched with programmatic dependent launch (else nothing to wait for)
 };
 
 template <int BM>
@@ -91,6 +92,9 @@ struct Cfg {
     static constexpr int kCK = 512 / BM < 2 ? 2 : 512 / BM;  // K-blocks per descriptor
     static constexpr int kSwMax = 64;                  // weight-block scales per descriptor
     static constexpr int kRing = 8;                    // descriptors in flight
+    // descriptors published before the previous kernel is done, their token scales deferred:
+    // enough to fill every stage with weight tiles, one ring slot kept for the end marker
+    static constexpr int kDefer = kStages < kRing - 1 ? kStages : kRing - 1;
     static constexpr int kDescHdr = 8;                 // ints: e, b, nt0, ntl, sp, kb0, nck, flags
     static constexpr int kDescInts = kDescHdr + BM + kCK * BM + kSwMax;  // hdr, rows, sa, sw
     static constexpr int kDescBytes = ((kDescInts * 4) + 15) / 16 * 16;
@@ -210,7 +214,42 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         int slot = 0;
         uint32_t ph = 0;
         bool ok = true;
-        bool dep_done = false;
+        bool dep_done = p.wait_first || !p.pdl;
+        // Before the previous kernel is done, up to kDefer descriptors are published without
+        // their token scales (ring slots pend0 .. pend0 + npend - 1), so that the producer can
+        // stream those descriptors' weight tiles meanwhile; the scales follow after the wait.
+        int npend = 0, pend0 = 0;
+        auto fill_sa = [&](int sl, int bb, int cc0, int nn) {
+            const Desc dd = desc_at<BM>(ring, sl);
+            // token scales (written by the previous kernel): lane order (slot j, K-block kk)
+            // with kk fastest, so the loads of one slot row are contiguous
+            float sa_v[C::kCK * BM / 32];
+            const int n_sa = nn * BM;
+#pragma unroll
+            for (int q = 0; q < C::kCK * BM / 32; ++q) {
+                const int i = q * 32 + lane;
+                const int j = i / nn, kk = i - j * nn;
+                sa_v[q] = i < n_sa ? __ldcg(p.a_s + static_cast<long long>(bb * BM + j) * p.KB + cc0 + kk) : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < C::kCK * BM / 32; ++q) {
+                const int i = q * 32 + lane;
+                const int j = i / nn, kk = i - j * nn;
+                if (i < n_sa) dd.sa[kk * BM + j] = sa_v[q];
+            }
+            mbar_arrive(dsa + sl);  // rows, weight and token scales: the epilogue goes ahead
+        };
+        auto flush_pending = [&]() {
+            __syncwarp();  // lane 0's header stores are read by every lane
+            grid_dep_wait();
+            dep_done = true;
+            for (int i = 0; i < npend; ++i) {
+                const int sl = pend0 + i < C::kRing ? pend0 + i : pend0 + i - C::kRing;
+                const int* hdr = desc_at<BM>(ring, sl).hdr;
+                fill_sa(sl, hdr[1], hdr[5], hdr[6]);
+            }
+            npend = 0;
+        };
         int cur_b = -1, e = -1;
         int rows[(BM + 31) / 32];
 #pragma unroll
@@ -275,25 +314,14 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                         const int i = q * 32 + lane;
                         if (i < n_sw) d.sw[i] = sw_v[q];
                     }
-                    if (!dep_done) { grid_dep_wait(); dep_done = true; }
-                    // token scales (written by the previous kernel): lane order (slot j,
-                    // K-block kk) with kk fastest, so the loads of one slot row are contiguous
-                    float sa_v[C::kCK * BM / 32];
-                    const int n_sa = nck * BM;
-#pragma unroll
-                    for (int q = 0; q < C::kCK * BM / 32; ++q) {
-                        const int i = q * 32 + lane;
-                        const int j = i / nck, kk = i - j * nck;
-                        sa_v[q] = i < n_sa ? __ldcg(p.a_s + static_cast<long long>(b * BM + j) * p.KB + c0 + kk) : 0.0f;
+                    if (dep_done) {
+                        fill_sa(slot, b, c0, nck);
+                    } else {
+                        if (npend == 0) pend0 = slot;
+                        ++npend;
                     }
-#pragma unroll
-                    for (int q = 0; q < C::kCK * BM / 32; ++q) {
-                        const int i = q * 32 + lane;
-                        const int j = i / nck, kk = i - j * nck;
-                        if (i < n_sa) d.sa[kk * BM + j] = sa_v[q];
-                    }
-                    mbar_arrive(dsa + slot);  // rows, weight and token scales: the epilogue goes ahead
                     if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
+                    if (npend == C::kDefer) flush_pending();
                 }
             }
             // advance by adv units (never past the end of this block and split's tile run)
@@ -305,21 +333,23 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
             }
         }
         if (ok) {
-            // end marker
+            // end marker (before the deferred token scales, so that the producer stops
+            // waiting for descriptors and issues its deferred activation tiles)
             ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
             if (__all_sync(0xFFFFFFFFu, ok)) {
                 if (lane == 0) desc_at<BM>(ring, slot).hdr[7] = kEnd;
                 mbar_arrive(dfull + slot);
                 mbar_arrive(dsa + slot);
             }
+            if (npend > 0) flush_pending();
         }
     } else if (warp == 0) {
         // ---------------- TMA producer ----------------
         // Until the previous kernel is done (grid_dep_wait) only the weight tiles are loaded; a
         // stage's activation tiles are recorded and issued right after the wait, which happens
-        // when every stage holds weights, or before the second descriptor is read.  Each stage
-        // expects its full byte count from the start, so its barrier completes only when both
-        // halves have landed.
+        // when every stage holds weights, or at the end marker.  Each stage expects its full
+        // byte count from the start, so its barrier completes only when both halves have
+        // landed.
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_a = l2_policy_evict_last();
@@ -327,7 +357,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
             uint32_t ph = 0, dph = 0;
             long long issued = 0;
             bool ok = true;
-            bool dep_done = false;
+            bool dep_done = p.wait_first || !p.pdl;
             int npend = 0;
             int pend_s[C::kStages], pend_kb[C::kStages], pend_nk[C::kStages], pend_b[C::kStages];
             auto load_a = [&](int st_i, int kb, int nk, int b) {
@@ -342,14 +372,11 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                 for (int i = 0; i < npend; ++i) load_a(pend_s[i], pend_kb[i], pend_nk[i], pend_b[i]);
                 npend = 0;
             };
-            long long ndesc = 0;
             while (ok) {
-                if (!dep_done && ndesc > 0) resolve();
                 if (!mbar_wait_fast(dfull + slot, dph, abort_flag, p.status)) break;
                 const Desc d = desc_at<BM>(ring, slot);
                 const int flags = d.hdr[7];
                 if (flags & kEnd) break;
-                ++ndesc;
                 const int e = d.hdr[0], b = d.hdr[1], nt0 = d.hdr[2], ntl = d.hdr[3];
                 const int c0 = d.hdr[5], nck = d.hdr[6];
                 mbar_arrive(dempty + slot);
@@ -362,7 +389,6 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                                                      : static_cast<long long>(e) * p.N_out + nt * 128;
                     for (int kb = c0; kb < c0 + nck; kb += C::kKps) {
                         const int nk = min(C::kKps, c0 + nck - kb);
-                        if (!dep_done && npend == C::kStages) resolve();  // every stage holds weights
                         if (!mbar_wait_fast(empty + s, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                         uint8_t* st = smem + s * C::kStage;
                         mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(nk * (C::kWBytes + C::kABytes)));
@@ -378,7 +404,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                             load_a(s, kb, nk, b);
                         } else {
                             pend_s[npend] = s; pend_kb[npend] = kb; pend_nk[npend] = nk; pend_b[npend] = b;
-                            ++npend;
+                            if (++npend == C::kStages) resolve();  // every stage holds weights
                         }
                         ++issued;
                         if (++s == C::kStages) { s = 0; ph ^= 1u; }
@@ -696,6 +722,7 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
     p.w_tiled = tiled ? 1 : 0;
     p.status = device_status_ptr();
     p.wait_first = wait_first ? 1 : 0;
+    p.pdl = pdl ? 1 : 0;
     const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
     switch (block_m) {
         case 16: return launch_bm<16>(tw, ta, p, max_units, pdl, stream);
