@@ -317,8 +317,8 @@ def run_ours(args):
     def fwd_host(x_, i_, w_, o_):
         return ops.moe_blockfp8_forward(x_, i_, w_, E, None, wgu_use, wgu_s, wd_use, wd_s, out=o_,
                                         workspace=work, stream=stream, path=path)
-    e2e_ms, h2d, d2h = time_e2e_zero_copy(ops, dev, stream, flush, xs, ids, ws, outs, fwd_host,
-                                          args.steps, args.warmup)
+    e2e_ms, h2d, d2h, e2e_wall = time_e2e_zero_copy(ops, dev, stream, flush, xs, ids, ws, outs, fwd_host,
+                                                    args.steps, args.warmup, dev_graphs=graphs)
     e2e_copy_ms, _, _ = time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, args.steps, args.warmup)
     clocks = sampler.stop()
 
@@ -414,7 +414,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h,
                 "transfer": "zero-copy: inputs and output in pinned host memory, read and written by "
                             "the layer's kernels across NVLink-C2C inside the timed graph",
-                "copy_engine_us": round(e2e_copy_ms * 1e3, 3)},
+                "copy_engine_us": round(e2e_copy_ms * 1e3, 3),
+                "host_wall_launch_to_sync_us": e2e_wall},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -736,7 +737,25 @@ def time_e2e(ops, dev, stream, flush, xs, ids, ws, outs, graphs, steps, warmup):
     return statistics.mean(t), h2d, d2h
 
 
-def time_e2e_zero_copy(ops, dev, stream, flush, xs, ids, ws, outs, fwd, steps, warmup):
+def wall_steps(graphs, steps, flush, stream):
+    """Median host wall time (us) from a graph's launch to the end of a stream sync, when its
+    result is visible to the host; L2 flushed and the stream idle before each step."""
+    import time
+    import torch
+    t = []
+    with torch.cuda.stream(stream):
+        for i in range(steps + 3):
+            flush_l2(flush)
+            stream.synchronize()
+            t0 = time.perf_counter()
+            graphs[i % len(graphs)].replay()
+            stream.synchronize()
+            if i >= 3:
+                t.append((time.perf_counter() - t0) * 1e6)
+    return statistics.median(t)
+
+
+def time_e2e_zero_copy(ops, dev, stream, flush, xs, ids, ws, outs, fwd, steps, warmup, dev_graphs=None):
     """Per step: the layer (graph of moe_blockfp8_forward) called on pinned HOST buffers: its
     kernels read x, topk_ids and topk_w from host memory and the reduce writes the output to
     host memory across the host link, so the step starts with the inputs on the host and ends
@@ -770,8 +789,12 @@ def time_e2e_zero_copy(ops, dev, stream, flush, xs, ids, ws, outs, fwd, steps, w
     t = [a.elapsed_time(b) for a, b in evs]
     h2d = hx[0].numel() * 2 + hi[0].numel() * 4 + hw[0].numel() * 4
     d2h = ho[0].numel() * 2
+    # the same steps on the host's clock: launch to sync, zero-copy and device-buffer graphs
+    wall = {"zero_copy": round(wall_steps(graphs, 40, flush, stream), 1)}
+    if dev_graphs is not None:
+        wall["device_buffers"] = round(wall_steps(dev_graphs, 40, flush, stream), 1)
     del graphs
-    return statistics.mean(t), h2d, d2h
+    return statistics.mean(t), h2d, d2h, wall
 
 
 def recorded_traffic(path):
