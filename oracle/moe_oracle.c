@@ -22,7 +22,7 @@
  *   moe_reduce         -- lmdeploy PR #4228 "Moe Reduce kernel", Copilot overview (weighted
  *                         top-k sum moved into a dedicated reduction; fp32 accumulation).
  *
- * Readings where the pages are silent (all listed in the design doc):
+ * Readings where the pages are silent:
  *   E4M3 is OCP e4m3fn (bias 7, max 448, no infinities); encoding rounds to nearest even and
  *   saturates finite values to +-448; the fp32 group scale is max(amax, 1e-10) / 448; UE8M0
  *   rounds that scale up to a power of two; the quantised value is an IEEE fp32 division; the
