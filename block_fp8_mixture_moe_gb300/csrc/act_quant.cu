@@ -178,23 +178,39 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
     const long long item = pair * 2 + half;
     bool active = item < static_cast<long long>(p.rows) * p.G;
     int row = 0, g = 0, in_row = 0;
+    // slot rows with no other filter or map: the slot's route entry is loaded together with
+    // the slot's inputs (one round trip, not two), and a pad slot's values are dropped after
+    const bool slot_walk = p.slot_route && !p.row_expert && !p.row_map;
+    int route = 0;
     if (active) {
         const int w = static_cast<int>(item / p.G);
         g = static_cast<int>(item - static_cast<long long>(w) * p.G);
-        active = row_source(p, w, &in_row, &row, pre_m);
+        if (slot_walk) {
+            in_row = row = w;
+            if (w >= p.in_rows || w >= p.out_rows) {
+                if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                active = false;
+            } else {
+                route = __ldcg(p.slot_route + w);
+            }
+        } else {
+            active = row_source(p, w, &in_row, &row, pre_m);
+        }
     }
     float a[8];
     if (active) {
         const long long col = static_cast<long long>(g) * 128 + l * 8;
         const long long rbase = static_cast<long long>(in_row) * p.W;
-        if (ACT == MOE_ACT_IDENTITY) {
+        float gv[8], uv[8];
+        if (ACT == MOE_ACT_IDENTITY)
             load8<F32IN>(p, rbase + col, a);
-        } else {
-            float gv[8], uv[8];
+        else
             load_gate_up<F32IN, KG>(p, rbase + col, rbase + p.N + col, gv, uv);
-            // INL: inline, so the 8 values' dependent chains (exp, IEEE divide) interleave;
-            // else one out-of-line copy (same arithmetic), less code for many warps to fetch
-            if constexpr (ACT != MOE_ACT_IDENTITY) {
+        if (slot_walk && route < 0) active = false;  // a pad slot
+        // INL: inline, so the 8 values' dependent chains (exp, IEEE divide) interleave;
+        // else one out-of-line copy (same arithmetic), less code for many warps to fetch
+        if constexpr (ACT != MOE_ACT_IDENTITY) {
+            if (active) {
                 if constexpr (INL) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) a[i] = silu_mul_bf16<ACT>(gv[i], uv[i], p.L);
