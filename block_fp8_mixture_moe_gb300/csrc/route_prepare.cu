@@ -233,6 +233,73 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
     warp_scatter(p, loc, p.R, 0, per_warp, row, start, nullptr);
 }
 
+// At most 32 routes: one warp holds a route per lane.  __match_any_sync groups the lanes of
+// equal experts, so a route's stable rank in its expert is the number of same-expert lanes
+// below it; the groups' leaders form a table of at most 32 active experts (local id, count,
+// padded count).  Meanwhile the CTA's other warps write every pad and empty block entry; after
+// the one barrier, each expert's count and padded offset are sums over that table, and the
+// real entries overwrite the pads.
+constexpr int kWarpMaxRoutes = 32;
+constexpr int kWarpThreads = 256;
+
+__global__ void __launch_bounds__(kWarpThreads, 1) k_route_warp(RouteArgs p) {
+    __shared__ int t_e[32], t_cnt[32], t_pad[32];
+    __shared__ int t_n;
+    grid_dep_wait();
+    grid_dep_launch();
+    clear_zero_region(p);
+    const int tid = threadIdx.x, lane = tid & 31;
+    int e = -1, rank = 0;
+    if (tid < 32) {
+        e = lane < p.R ? local_of(p, lane) : -1;
+        const unsigned m = __match_any_sync(kFull, e);
+        rank = __popc(m & lanemask_lt());
+        const bool lead = e >= 0 && rank == 0;
+        const unsigned leads = __ballot_sync(kFull, lead);
+        if (lead) {
+            const int i = __popc(leads & lanemask_lt());
+            const int c = __popc(m);
+            t_e[i] = e;
+            t_cnt[i] = c;
+            t_pad[i] = ((c + p.bm - 1) >> p.bm_shift) << p.bm_shift;
+        }
+        if (lane == 0) t_n = __popc(leads);
+    } else {
+        const int nthr = blockDim.x - 32, t = tid - 32;
+        for (long long sl = t; sl < (static_cast<long long>(p.B_cap) << p.bm_shift); sl += nthr) p.sorted_idx[sl] = -1;
+        for (int b = t; b < p.B_cap; b += nthr) p.block_expert[b] = -1;
+    }
+    __syncthreads();
+    const int n = t_n;
+    // padded offset of local expert x: the padded counts of the active experts below it
+    auto offset_of = [&](int x) {
+        int off = 0;
+        for (int i = 0; i < n; ++i) off += t_e[i] < x ? t_pad[i] : 0;
+        return off;
+    };
+    for (int x = tid; x < p.E_loc; x += blockDim.x) {
+        int c = 0;
+        for (int i = 0; i < n; ++i) c = t_e[i] == x ? t_cnt[i] : c;
+        p.count[x] = c;
+        if (p.offset) p.offset[x] = offset_of(x);
+    }
+    if (tid < n) {
+        const int off = offset_of(t_e[tid]);
+        for (int b = off >> p.bm_shift; b < ((off + t_pad[tid]) >> p.bm_shift); ++b) p.block_expert[b] = t_e[tid];
+    }
+    if (tid == 0) {
+        int total = 0;
+        for (int i = 0; i < n; ++i) total += t_pad[i];
+        *p.num_blocks = total >> p.bm_shift;
+        if (p.offset) p.offset[p.E_loc] = total;
+    }
+    if (tid < 32 && lane < p.R) {
+        const int slot = e >= 0 ? offset_of(e) + rank : -1;
+        if (e >= 0) p.sorted_idx[slot] = lane;
+        if (p.route_slot) p.route_slot[lane] = slot;
+    }
+}
+
 // Multi-CTA kernel 1: chunk histograms; the last CTA to finish builds the metadata.
 __global__ void __launch_bounds__(1024) k_route_count(RouteArgs p) {
     extern __shared__ __align__(16) int sm[];
@@ -378,6 +445,13 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
     p.status = device_status_ptr();
     p.zero_ptr = zero_ptr;
     p.zero_n = zero_ptr ? zero_n : 0;
+    if (path == MOE_ROUTE_AUTO && R > 0 && R <= kWarpMaxRoutes) {
+        // a handful of routes (decode batches of a few tokens): one warp sorts them
+        Launch L(dim3(1), dim3(kWarpThreads), 0, stream, pdl);
+        cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_route_warp, p);
+        if (e != cudaSuccess) { set_error("route warp launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+        return MOE_OK;
+    }
     const bool single = route_single_cta(R, E_local, path) && R > 0;
     if (single) {
         if (R > kSingleMaxRoutes || E_local > kSingleMaxExperts) {

@@ -102,10 +102,11 @@ typedef enum { MOE_FORWARD_AUTO = 0, MOE_FORWARD_FUSED = 1, MOE_FORWARD_STAGED =
  *   route_slot   [M * k]            inverse of sorted_idx: the slot of route r, -1 when the
  *                                   route is dropped; nullable.
  * B_cap = moe_block_capacity(M, k, E_local, block_m) = ceil(M*k/block_m) + min(E_local, M*k).
- * block_m in {16, 32, 64, 128}.  path: AUTO takes the single-CTA sort when M*k <= 8192 and
- * E_local <= 512 (measured faster than the multi-CTA launches there on GB300; the pages switch
- * at 2048) and the multi-CTA count/scan/scatter otherwise; the others force a path
- * (SINGLE_CTA needs M*k <= 8192 and E_local <= 2048).
+ * block_m in {16, 32, 64, 128}.  path: AUTO takes one warp of one CTA for M*k <= 32 (a
+ * match-any rank per route), the single-CTA sort when M*k <= 8192 and E_local <= 512
+ * (measured faster than the multi-CTA launches there on GB300; the pages switch at 2048) and
+ * the multi-CTA count/scan/scatter otherwise; the others force a path (SINGLE_CTA needs
+ * M*k <= 8192 and E_local <= 2048).
  * workspace: moe_route_prepare_workspace_bytes(...) bytes, 256-byte aligned (only the multi-CTA
  * path uses it; the single-CTA path accepts a null workspace).  An expert_map entry outside [-1, E_local) drops that route and sets
  * MOE_DEV_BAD_EXPERT_MAP.
