@@ -87,3 +87,22 @@ def test_calls_without_a_gpu_fail_cleanly(lib_path):
     rc = L.moe_reduce(None, None, None, None, 1, 1, 1, 8, None, None)
     assert rc == ops.MOE_ERR_UNSUPPORTED
     assert L.moe_last_error_string()
+
+
+def test_forward_refuses_pageable_host_activations(lib_path):
+    """Host activations must be pinned (device-accessible at their address); a pageable tensor
+    is refused in the binding, before the library is called."""
+    import torch
+    from block_fp8_mixture_moe_gb300 import ops
+    ops.load(lib_path)
+    M, H, N, E, k = 2, 256, 128, 4, 2
+    x = torch.zeros((M, H), dtype=torch.bfloat16)
+    ids = torch.zeros((M, k), dtype=torch.int32)
+    w = torch.zeros((M, k), dtype=torch.float32)
+    wgu_q = torch.zeros((E, 2 * N, H), dtype=torch.uint8)
+    wgu_s = torch.ones((E, 2 * N // 128, H // 128), dtype=torch.float32)
+    wd_q = torch.zeros((E, H, N), dtype=torch.uint8)
+    wd_s = torch.ones((E, H // 128, N // 128), dtype=torch.float32)
+    with pytest.raises(AssertionError, match="pinned"):
+        ops.moe_blockfp8_forward(x, ids, w, E, None, wgu_q, wgu_s, wd_q, wd_s,
+                                 out=torch.zeros((M, H), dtype=torch.bfloat16))
