@@ -281,19 +281,6 @@ __device__ __forceinline__ void quant_group_codes_compact(const float* a, bool a
     }
 }
 
-// As quant_group_codes, storing the 8 codes at q_dst (one 8-byte store) and, from the
-// half-warp's lane 0 (lead), the scale at s_dst.
-__device__ __forceinline__ void quant_group_store(const float* a, bool active, int fmt,
-                                                  uint8_t* q_dst, float* s_dst, bool lead) {
-    uint2 codes;
-    float s;
-    quant_group_codes(a, active, fmt, &codes, &s);
-    if (active) {
-        *reinterpret_cast<uint2*>(q_dst) = codes;
-        if (lead) *s_dst = s;
-    }
-}
-
 // ---------------------------------------------------------------------------------------------
 // mbarrier / TMA / tcgen05 wrappers (PTX ISA, sm_100-family instructions)
 // ---------------------------------------------------------------------------------------------
@@ -439,44 +426,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
            | (static_cast<uint64_t>(1024 >> 4) << 32)   // stride byte offset: next 8 rows
            | (1ull << 46)                               // descriptor version (sm_100 family)
            | (2ull << 61);                              // swizzle: 128 B
-}
-
-// 32 lanes x 16 columns of fp32 from tensor memory, waited on in the same statement so the
-// registers are never read early.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Two 32-lane x 16-column loads (two accumulator buffers) and one wait, in one statement.
-__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr0, uint32_t taddr1, float* v) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr0), "r"(taddr1)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 32 lanes x 32 columns of fp32 from tensor memory, waited on in the same statement.
