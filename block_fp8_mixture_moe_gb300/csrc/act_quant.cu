@@ -344,10 +344,13 @@ __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __re
     }
 }
 
-// The unfused first half: BF16 SiLU*mul written to memory, 8 outputs per thread.
+// The unfused first half: BF16 SiLU*mul written to memory, 8 outputs per thread.  Rows whose
+// expert the filter drops (row_expert / expert_map, as in k_act_quant) are skipped.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_silu_and_mul(const uint16_t* in, int rows, int N,
-                                                      float L, uint16_t* out) {
+                                                      float L, const int32_t* row_expert,
+                                                      const int32_t* expert_map, int E,
+                                                      uint16_t* out) {
     grid_dep_wait();
     grid_dep_launch();
     const long long chunks = static_cast<long long>(rows) * (N / 8);
@@ -355,6 +358,11 @@ __global__ void __launch_bounds__(256) k_silu_and_mul(const uint16_t* in, int ro
          c += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long row = c / (N / 8);
         const long long col = (c - row * (N / 8)) * 8;
+        if (row_expert) {
+            const int id = __ldg(row_expert + row);
+            if (id < 0 || id >= E) continue;
+            if (expert_map && __ldg(expert_map + id) < 0) continue;
+        }
         uint4 gw = __ldg(reinterpret_cast<const uint4*>(in + row * 2 * N + col));
         uint4 uw = __ldg(reinterpret_cast<const uint4*>(in + row * 2 * N + N + col));
         const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
@@ -519,12 +527,15 @@ int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t*
 }  // namespace moe
 
 extern "C" int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, float clamp_limit,
+                                 const int32_t* row_expert, const int32_t* expert_map, int E,
                                  void* out, cudaStream_t stream) {
     using namespace moe;
     clear_error();
     if (!device_is_sm103()) { set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
     if (!in || !out || !aligned16(in) || !aligned16(out)) { set_error("silu_and_mul_bf16: null or misaligned pointer"); return MOE_ERR_ARG; }
     if (rows < 0 || N <= 0 || N % 8) { set_error("silu_and_mul_bf16: bad shape"); return MOE_ERR_ARG; }
+    if (row_expert && E <= 0) { set_error("silu_and_mul_bf16: row_expert needs E > 0"); return MOE_ERR_ARG; }
+    if (expert_map && !row_expert) { set_error("silu_and_mul_bf16: expert_map needs row_expert"); return MOE_ERR_ARG; }
     if (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SILU_MUL_GATE_UPPER) { set_error("silu_and_mul_bf16: act must be a SiLU*mul"); return MOE_ERR_ARG; }
     const long long chunks = static_cast<long long>(rows) * (N / 8);
     if (chunks == 0) return MOE_OK;
@@ -533,8 +544,10 @@ extern "C" int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, f
     if (blocks > cap) blocks = cap;
     Launch L(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, false);
     cudaError_t e = act == MOE_ACT_SILU_MUL
-        ? cudaLaunchKernelEx(&L.cfg, k_silu_and_mul<MOE_ACT_SILU_MUL>, static_cast<const uint16_t*>(in), rows, N, clamp_limit, static_cast<uint16_t*>(out))
-        : cudaLaunchKernelEx(&L.cfg, k_silu_and_mul<MOE_ACT_SILU_MUL_GATE_UPPER>, static_cast<const uint16_t*>(in), rows, N, clamp_limit, static_cast<uint16_t*>(out));
+        ? cudaLaunchKernelEx(&L.cfg, k_silu_and_mul<MOE_ACT_SILU_MUL>, static_cast<const uint16_t*>(in), rows, N,
+                             clamp_limit, row_expert, expert_map, E, static_cast<uint16_t*>(out))
+        : cudaLaunchKernelEx(&L.cfg, k_silu_and_mul<MOE_ACT_SILU_MUL_GATE_UPPER>, static_cast<const uint16_t*>(in), rows, N,
+                             clamp_limit, row_expert, expert_map, E, static_cast<uint16_t*>(out));
     if (e != cudaSuccess) { set_error("silu_and_mul_bf16 launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     return MOE_OK;
 }

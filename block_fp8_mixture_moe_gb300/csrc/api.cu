@@ -185,7 +185,9 @@ Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int 
 // AUTO forward path: the one measured faster on GB300 for the shape (graph-replayed layer on
 // the decode shapes M = 1..256): the staged launches at every measured size.
 moe_forward_path auto_path(int M, int k, int E, int E_local, int H, int N) {
-    (void)M; (void)k; (void)E; (void)E_local; (void)H; (void)N;
+    (void)M; (void)E; (void)E_local; (void)H; (void)N;
+    // top-k above the separate reduce kernel's limit: only the fused path takes it
+    if (k > kReduceMaxTopk) return MOE_FORWARD_FUSED;
     return MOE_FORWARD_STAGED;
 }
 
@@ -270,6 +272,14 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
         return MOE_ERR_ARG;
     }
     if (k > E) { set_error("moe_blockfp8_forward: k > E"); return MOE_ERR_ARG; }
+    // the staged path's separate reduce kernel takes at most kReduceMaxTopk routes per token;
+    // AUTO sends larger top-k to the fused path (no limit), an explicit STAGED is refused here,
+    // before anything is enqueued
+    if (k > kReduceMaxTopk && path == MOE_FORWARD_STAGED) {
+        set_error("moe_blockfp8_forward: the staged path takes top-k <= %d (got %d); use FUSED or AUTO",
+                  kReduceMaxTopk, k);
+        return MOE_ERR_ARG;
+    }
     if (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SILU_MUL_GATE_UPPER) {
         set_error("moe_blockfp8_forward: act must be SILU_MUL or SILU_MUL_GATE_UPPER");
         return MOE_ERR_ARG;
@@ -357,7 +367,31 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                              block_expert, num_blocks, P.B_cap, P.bm, z, MOE_DTYPE_BF16, P.R, 1,
                              true, stream);
     if (rc) return rc;
-    return launch_moe_reduce(z, topk_w, topk_ids, expert_map, M, k, E, H, out, true, stream);
+    return launch_moe_reduce(z, topk_w, topk_ids, expert_map, M, k, E, E_local, H, out, true, stream);
+}
+
+extern "C" int moe_blockfp8_workspace_layout(int M, int k, int E, int E_local, int H, int N,
+                                             int block_m, size_t* offsets) {
+    clear_error();
+    if (!offsets || M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0 || H % 128 ||
+        N % 128 || (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)) {
+        set_error("moe_blockfp8_workspace_layout: bad sizes or null offsets");
+        return MOE_ERR_ARG;
+    }
+    const Plan P = make_plan(M, k, E, E_local, H, N, block_m, sm_count());
+    offsets[MOE_WS_SORTED_IDX] = P.off_sorted;
+    offsets[MOE_WS_BLOCK_EXPERT] = P.off_bexp;
+    offsets[MOE_WS_NUM_BLOCKS] = P.off_nb;
+    offsets[MOE_WS_EXPERT_COUNT] = P.off_cnt;
+    offsets[MOE_WS_EXPERT_OFFSET] = P.off_off;
+    offsets[MOE_WS_ROUTE_SLOT] = P.off_rslot;
+    offsets[MOE_WS_XQ] = P.off_xq;
+    offsets[MOE_WS_XS] = P.off_xs;
+    offsets[MOE_WS_GU] = P.off_gu;
+    offsets[MOE_WS_AQ] = P.off_aq;
+    offsets[MOE_WS_AS] = P.off_as;
+    offsets[MOE_WS_Z] = P.off_z;
+    return MOE_OK;
 }
 
 extern "C" int moe_forward_path_for(int M, int k, int E, int E_local, int H, int N) {

@@ -59,8 +59,9 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
                         cudaStream_t stream, bool wait_first = false);
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
-                      const int32_t* expert_map, int M, int k, int E, int H, void* out, bool pdl,
-                      cudaStream_t stream);
+                      const int32_t* expert_map, int M, int k, int E, int E_local, int H, void* out,
+                      bool pdl, cudaStream_t stream);
+constexpr int kReduceMaxTopk = 16;  // top-k limit of the separate reduce kernel
 
 // The fused layer kernel (everything after route preparation in one persistent launch).
 struct FusedLaunch {

@@ -15,7 +15,7 @@
 namespace moe {
 namespace {
 
-constexpr int kMaxTopk = 16;
+constexpr int kMaxTopk = kReduceMaxTopk;
 
 // One CTA per (token, 1024-column slice): the token's top-k ids, weights and keep flags are
 // read once into shared memory; each thread then issues all its route loads back to back
@@ -24,7 +24,8 @@ __global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__
                                                     const float* __restrict__ w,
                                                     const int32_t* __restrict__ ids,
                                                     const int32_t* __restrict__ map, int M, int k,
-                                                    int E, int H, uint16_t* __restrict__ out) {
+                                                    int E, int E_local, int H,
+                                                    uint16_t* __restrict__ out) {
     __shared__ float s_w[kMaxTopk];
     __shared__ int s_keep[kMaxTopk];
     grid_dep_launch();
@@ -33,7 +34,12 @@ __global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__
         const int j = threadIdx.x;
         const int id = __ldg(ids + static_cast<long long>(t) * k + j);
         bool keep = id >= 0 && id < E;
-        if (keep && map) keep = __ldg(map + id) >= 0;
+        if (keep && map) {
+            // the route-preparation rule: a map entry outside [0, E_local) gives the route no
+            // slot, so its z row was never written and it adds nothing here either
+            const int le = __ldg(map + id);
+            keep = le >= 0 && le < E_local;
+        }
         s_keep[j] = keep ? 1 : 0;
         s_w[j] = __ldg(w + static_cast<long long>(t) * k + j);
     }
@@ -74,9 +80,16 @@ __global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__
 }  // namespace
 
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
-                      const int32_t* expert_map, int M, int k, int E, int H, void* out, bool pdl,
-                      cudaStream_t stream) {
-    if (M < 0 || k <= 0 || E <= 0 || H <= 0 || H % 8) { set_error("moe_reduce: bad shape (H multiple of 8)"); return MOE_ERR_ARG; }
+                      const int32_t* expert_map, int M, int k, int E, int E_local, int H, void* out,
+                      bool pdl, cudaStream_t stream) {
+    if (M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || H % 8) {
+        set_error("moe_reduce: bad shape (need k, E, E_local > 0 and H a multiple of 8)");
+        return MOE_ERR_ARG;
+    }
+    if (!expert_map && E_local != E) {
+        set_error("moe_reduce: without an expert map E_local must equal E (%d vs %d)", E_local, E);
+        return MOE_ERR_EXPERT_SLICE;
+    }
     const long long total = static_cast<long long>(M) * (H / 8);
     if (total == 0) return MOE_OK;
     if (!z || !topk_w || !topk_ids || !out) { set_error("moe_reduce: null pointer"); return MOE_ERR_ARG; }
@@ -85,7 +98,7 @@ int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_id
     const int slices = (H / 8 + 127) / 128;
     Launch L(dim3(static_cast<unsigned>(M), static_cast<unsigned>(slices)), dim3(128), 0, stream, pdl);
     cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_moe_reduce, static_cast<const uint16_t*>(z),
-                                       topk_w, topk_ids, expert_map, M, k, E, H,
+                                       topk_w, topk_ids, expert_map, M, k, E, E_local, H,
                                        static_cast<uint16_t*>(out));
     if (e != cudaSuccess) { set_error("moe_reduce launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     return MOE_OK;
@@ -94,9 +107,19 @@ int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_id
 }  // namespace moe
 
 extern "C" int moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
-                          const int32_t* expert_map, int M, int k, int E, int H, void* out,
-                          cudaStream_t stream) {
+                          const int32_t* expert_map, int M, int k, int E, int E_local, int H,
+                          void* out, cudaStream_t stream) {
     moe::clear_error();
     if (!moe::device_is_sm103()) { moe::set_error("no sm_103 device is current"); return MOE_ERR_UNSUPPORTED; }
-    return moe::launch_moe_reduce(z, topk_w, topk_ids, expert_map, M, k, E, H, out, false, stream);
+    return moe::launch_moe_reduce(z, topk_w, topk_ids, expert_map, M, k, E, E_local, H, out, false,
+                                  stream);
+}
+
+extern "C" int moe_kernel_binary_version(void) {
+    cudaFuncAttributes a{};
+    if (cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(moe::k_moe_reduce)) != cudaSuccess) {
+        cudaGetLastError();  // no device: clear the error, answer -1
+        return -1;
+    }
+    return a.binaryVersion;
 }

@@ -413,6 +413,7 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
         set_error("moe_route_prepare: block_m must be 16, 32, 64 or 128 (got %d)", block_m);
         return MOE_ERR_ARG;
     }
+    if (k > E) { set_error("moe_route_prepare: top-k %d > E %d", k, E); return MOE_ERR_ARG; }
     if (!expert_map && E_local != E) {
         set_error("moe_route_prepare: without an expert map E_local must equal E (%d vs %d)", E_local, E);
         return MOE_ERR_EXPERT_SLICE;
@@ -495,8 +496,7 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
     p.ws_off = reinterpret_cast<int32_t*>(ws);
     ws += align256(static_cast<size_t>(E_local + 1) * 4);
     p.ws_done = reinterpret_cast<unsigned*>(ws);
-    cudaError_t e = cudaMemsetAsync(p.ws_done, 0, sizeof(unsigned), stream);
-    if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    // shared-memory limits first: a refusal returns before anything is enqueued
     const size_t smem1 = (static_cast<size_t>(E_local) * 2 + 1 + 33) * 4;
     const size_t ints2 = ((static_cast<size_t>(p.chunk) + E_local) + 3) & ~static_cast<size_t>(3);
     const size_t smem2 = ints2 * 4 + static_cast<size_t>(p.warps) * E_local * 2;
@@ -505,6 +505,8 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
         set_error("route multi: shared-memory limit refused");
         return MOE_ERR_LAUNCH;
     }
+    cudaError_t e = cudaMemsetAsync(p.ws_done, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     {
         Launch L(dim3(p.nchunks), dim3(1024), smem1, stream, false);
         e = cudaLaunchKernelEx(&L.cfg, k_route_count, p);
@@ -614,6 +616,7 @@ extern "C" int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, 
         set_error("moe_route_prepare_noalloc: E_local %d > E %d", E_local, E);
         return MOE_ERR_EXPERT_SLICE;
     }
+    if (k > E) { set_error("moe_route_prepare_noalloc: top-k %d > E %d", k, E); return MOE_ERR_ARG; }
     const long long R = static_cast<long long>(M) * k;
     if (R > kNoAllocMaxRoutes || E_local > kNoAllocMaxExperts) {
         set_error("moe_route_prepare_noalloc: at most %d routes (M*k) and %d local experts fit its "
@@ -657,9 +660,7 @@ extern "C" int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, 
     p.ws_cnt = scratch;                                       // [nchunks][E_local]
     p.ws_off = scratch + kNoAllocCntInts;                     // [E_local + 1]
     p.ws_done = reinterpret_cast<unsigned*>(scratch + kNoAllocCntInts + kNoAllocOffInts);
-    // the ticket counter must start at zero (the array keeps the previous call's contents)
-    cudaError_t e = cudaMemsetAsync(p.ws_done, 0, sizeof(unsigned), stream);
-    if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
+    // shared-memory limits first: a refusal returns before anything is enqueued
     const size_t smem1 = (static_cast<size_t>(E_local) * 2 + 1 + 33) * 4;
     const size_t ints2 = ((static_cast<size_t>(p.chunk) + E_local) + 3) & ~static_cast<size_t>(3);
     const size_t smem2 = ints2 * 4 + static_cast<size_t>(p.warps) * E_local * 2;
@@ -668,6 +669,9 @@ extern "C" int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, 
         set_error("moe_route_prepare_noalloc: shared-memory limit refused");
         return MOE_ERR_LAUNCH;
     }
+    // the ticket counter must start at zero (the array keeps the previous call's contents)
+    cudaError_t e = cudaMemsetAsync(p.ws_done, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) { set_error("route memset: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     {
         Launch L(dim3(p.nchunks), dim3(1024), smem1, stream, false);
         e = cudaLaunchKernelEx(&L.cfg, k_route_count, p);

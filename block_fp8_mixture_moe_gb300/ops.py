@@ -40,11 +40,12 @@ SIGNATURES = {
     "moe_blockfp8_pack_weights": (_I, [_P, _I, _I, _I, _P, _P]),
     "silu_mul_quant_fp8": (_I, [_I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _I, _P, _I, _I, _P, _P,
                                 _I, _P]),
-    "silu_and_mul_bf16": (_I, [_I, _P, _I, _I, _F, _P, _P]),
-    "moe_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "silu_and_mul_bf16": (_I, [_I, _P, _I, _I, _F, _P, _P, _I, _P, _P]),
+    "moe_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_blockfp8_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_blockfp8_forward": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I,
                                   _F, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_blockfp8_workspace_layout": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "moe_forward_path_for": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_block_m": (_I, [_I, _I, _I, _I, _I]),
     "moe_blockfp8_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
@@ -52,6 +53,7 @@ SIGNATURES = {
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_get_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "moe_device_supported": (_I, []),
+    "moe_kernel_binary_version": (_I, []),
     "moe_pointer_device_accessible": (_I, [_P]),
 }
 
@@ -221,10 +223,13 @@ def silu_mul_quant_fp8(act, inp, N, rows=None, clamp_limit=float("inf"), fmt=SCA
     return out_q, out_s
 
 
-def silu_and_mul_bf16(act, inp, N, clamp_limit=float("inf"), stream=None):
+def silu_and_mul_bf16(act, inp, N, clamp_limit=float("inf"), row_expert=None, expert_map=None, E=0,
+                      out=None, stream=None):
     L = load()
-    out = torch.empty((inp.shape[0], N), dtype=torch.bfloat16, device=inp.device)
-    rc = L.silu_and_mul_bf16(act, _ptr(inp), inp.shape[0], N, float(clamp_limit), _ptr(out),
+    if out is None:
+        out = torch.empty((inp.shape[0], N), dtype=torch.bfloat16, device=inp.device)
+    rc = L.silu_and_mul_bf16(act, _ptr(inp), inp.shape[0], N, float(clamp_limit),
+                             _ptr(_i32(row_expert)), _ptr(_i32(expert_map)), E, _ptr(out),
                              _stream(stream))
     _check(rc, "silu_and_mul_bf16")
     return out
@@ -275,20 +280,43 @@ def moe_blockfp8_grouped_gemm(proj, a_q, a_s, w_q, w_s, route, block_m, out_dtyp
     return out
 
 
-def moe_reduce(z, topk_w, topk_ids, expert_map, E, H, out=None, stream=None):
+def moe_reduce(z, topk_w, topk_ids, expert_map, E, H, out=None, stream=None, E_local=None):
+    """E_local: number of local experts (the range of the expert map's entries); required
+    with an expert map, E without one."""
     L = load()
     ids = _i32(topk_ids)
     M, k = ids.shape
+    if E_local is None:
+        if expert_map is not None:
+            raise ValueError("moe_reduce: pass E_local with an expert map")
+        E_local = E
     if out is None:
         out = torch.empty((M, H), dtype=torch.bfloat16, device=z.device)
     rc = L.moe_reduce(_ptr(z), _ptr(topk_w.float().contiguous()), _ptr(ids), _ptr(_i32(expert_map)),
-                      M, k, E, H, _ptr(out), _stream(stream))
+                      M, k, E, E_local, H, _ptr(out), _stream(stream))
     _check(rc, "moe_reduce")
     return out
 
 
 def moe_blockfp8_workspace_bytes(M, k, E, E_local, H, N, block_m=0) -> int:
     return load().moe_blockfp8_workspace_bytes(M, k, E, E_local, H, N, block_m)
+
+
+WS_REGIONS = ("sorted_idx", "block_expert", "num_blocks", "expert_count", "expert_offset",
+              "route_slot", "xq", "xs", "gu", "aq", "as", "z")
+
+
+def moe_blockfp8_workspace_layout(M, k, E, E_local, H, N, block_m=0) -> dict:
+    """Byte offsets of the forward's intermediate tensors inside its workspace, by region name
+    (see moe_ws_region in include/moefp8.h for their layouts)."""
+    offs = (ctypes.c_size_t * len(WS_REGIONS))()
+    _check(load().moe_blockfp8_workspace_layout(M, k, E, E_local, H, N, block_m, offs),
+           "moe_blockfp8_workspace_layout")
+    return {name: int(offs[i]) for i, name in enumerate(WS_REGIONS)}
+
+
+def moe_kernel_binary_version() -> int:
+    return load().moe_kernel_binary_version()
 
 
 def moe_forward_path_for(M, k, E, E_local, H, N) -> int:

@@ -156,3 +156,36 @@ def act_rows(rows: int, width: int, std: float, seed: int) -> np.ndarray:
 def act_sweep_rows(tokens: int, k: int = 8, width: int = 1024, seed: int = 0) -> np.ndarray:
     """Fused clamped act-quant sweep: routed rows = tokens * k, gate/up width 2*512."""
     return act_rows(tokens * k, width, 2.0, seed * 7919 + 11 + tokens)
+
+
+def padded_grid_route(sorted_idx, block_expert, num_blocks: int, E_local: int, bm: int):
+    """The schedule that active-expert block scheduling replaces (lmdeploy PR #4956,
+    "Motivation": the dense grid covers every expert): every local expert owns at least one
+    block, max(1, its compact block count), in expert order, so the GEMM streams the weights of
+    every expert whether or not it received routes.  Built on the host from a compact route
+    table (numpy int32 arrays as moe_route_prepare returns them); a table transform only, no
+    arithmetic of the layer.
+
+    Returns dict(sorted_idx, block_expert, num_blocks, B_cap, slot_map): slot_map[s] is the
+    padded-grid slot that holds compact slot s (-1 for slots past the compact blocks)."""
+    sorted_idx = np.asarray(sorted_idx, np.int32)
+    block_expert = np.asarray(block_expert, np.int32)
+    per_expert = [[] for _ in range(E_local)]
+    for b in range(int(num_blocks)):
+        per_expert[int(block_expert[b])].append(b)
+    nb_pad = sum(max(1, len(bl)) for bl in per_expert)
+    si = np.full(nb_pad * bm, -1, np.int32)
+    be = np.empty(nb_pad, np.int32)
+    slot_map = np.full(sorted_idx.size, -1, np.int32)
+    nb = 0
+    for e, blocks in enumerate(per_expert):
+        if not blocks:
+            be[nb] = e
+            nb += 1
+            continue
+        for b in blocks:
+            be[nb] = e
+            si[nb * bm:(nb + 1) * bm] = sorted_idx[b * bm:(b + 1) * bm]
+            slot_map[b * bm:(b + 1) * bm] = np.arange(nb * bm, (nb + 1) * bm, dtype=np.int32)
+            nb += 1
+    return dict(sorted_idx=si, block_expert=be, num_blocks=nb, B_cap=nb, slot_map=slot_map)

@@ -102,6 +102,7 @@ typedef enum { MOE_FORWARD_AUTO = 0, MOE_FORWARD_FUSED = 1, MOE_FORWARD_STAGED =
  *   route_slot   [M * k]            inverse of sorted_idx: the slot of route r, -1 when the
  *                                   route is dropped; nullable.
  * B_cap = moe_block_capacity(M, k, E_local, block_m) = ceil(M*k/block_m) + min(E_local, M*k).
+ * k <= E (MOE_ERR_ARG otherwise).
  * block_m in {16, 32, 64, 128}.  path: AUTO takes one warp of one CTA for M*k <= 32 (a
  * match-any rank per route), the single-CTA sort when M*k <= 8192 and E_local <= 512
  * (measured faster than the multi-CTA launches there on GB300; the pages switch at 2048) and
@@ -155,6 +156,12 @@ MOEFP8_API int moe_route_prepare_noalloc(const int32_t* topk_ids, int M, int k, 
  *   y[s, n] = sum_kb ( sum_{i in kb} a_q[s, i] * w_q[e, n, i] ) * a_s[s, kb] * w_s[e, n/128, kb]
  * accumulated in fp32.  Work is launched for real blocks only (num_blocks is read on the
  * device); pad slots are neither read for output nor written.
+ * The activation rows are in SLOT order for both projections, not in token order: row s of
+ * a_q is the input of the route in slot s.  The pages' kernels read token rows t = route / k
+ * through the sorted indices inside the GEMM; here the gather happens before the GEMM (the
+ * layer's input quantisation writes each token's codes to its routes' slots, e.g.
+ * silu_mul_quant_fp8(IDENTITY, row_map = route_slot, row_div = k)), so that every GEMM operand
+ * is a plain 2-D tensor tile.  A caller with token-ordered activations must gather them first.
  *   a_q  [a_rows, K] E4M3, rows in SLOT order (a_rows >= B_cap*block_m); a_s [a_rows, K/128] f32.
  *   w_q  [E_local, N_out, K] E4M3 (K contiguous) for MOE_WEIGHTS_ROW_MAJOR, or the tiled
  *        regrouping of it for MOE_WEIGHTS_TILED; w_s [E_local, N_out/128, K/128] f32.
@@ -213,21 +220,27 @@ MOEFP8_API int silu_mul_quant_fp8(moe_act act, const void* in, moe_dtype in_dtyp
 
 /* The unfused first half of the two-kernel path (lmdeploy PR #4956, "Motivation"): writes the
  * BF16 SiLU*mul result out [rows, N] from in [rows, 2N].  act must not be IDENTITY.  Used as
- * the separate-kernel arm that the fused kernel is compared with. */
-MOEFP8_API int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, float clamp_limit, void* out,
-                      cudaStream_t stream);
+ * the separate-kernel arm that the fused kernel is compared with.  The expert filter
+ * (row_expert nullable [rows] global ids, expert_map nullable [E]) skips the same rows as in
+ * silu_mul_quant_fp8 and leaves their output rows untouched (vLLM PR #53875, "Kernel
+ * microbenchmarks": the filter applies in both arms). */
+MOEFP8_API int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, float clamp_limit,
+                                 const int32_t* row_expert, const int32_t* expert_map, int E,
+                                 void* out, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * moe_reduce (lmdeploy PR #4228 "Moe Reduce kernel"): weighted top-k sum back to one row per
  * token, out[t, h] = bf16( sum_j w[t, j] * z[t*k + j, h] ) over the kept routes in j order,
- * fp32 accumulation with one fused multiply-add per term.  Dropped routes (id < 0, >= E, or
- * mapped to -1) contribute nothing and their z rows are never read.
+ * fp32 accumulation with one fused multiply-add per term.  Dropped routes contribute nothing
+ * and their z rows are never read.  A route is dropped by the same rule as in route
+ * preparation: id < 0, id >= E, or an expert_map entry outside [0, E_local) (-1, or an invalid
+ * entry for which route preparation gave the route no slot).
  *   z [M*k, H] bf16 (route order); topk_w [M, k] f32; topk_ids [M, k] int32;
- *   expert_map nullable [E]; out [M, H] bf16.  H multiple of 8, k <= 16; pointers 16-byte
- *   aligned.
+ *   expert_map nullable [E] (without it E_local must equal E); out [M, H] bf16.  H multiple
+ *   of 8, k <= 16; pointers 16-byte aligned.
  * ------------------------------------------------------------------------------------------ */
 MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
-               const int32_t* expert_map, int M, int k, int E, int H, void* out,
+               const int32_t* expert_map, int M, int k, int E, int E_local, int H, void* out,
                cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
@@ -251,8 +264,10 @@ MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* top
  *   so the fp32 summation order of the gate/up partial sums (not the arithmetic of any stage)
  *   depends on the SM count.  path STAGED: one launch per stage.  AUTO: see
  *   moe_forward_path_for.
- * H and N multiples of 128.  All stages run on `stream` with no host synchronisation, so the
- * call can be captured in a CUDA graph.
+ * H and N multiples of 128; k <= E.  The staged path's reduce takes k <= 16: STAGED with a
+ * larger k is refused (MOE_ERR_ARG, nothing enqueued) and AUTO then takes FUSED, which has no
+ * top-k limit.  All stages run on `stream` with no host synchronisation, so the call can be
+ * captured in a CUDA graph.
  * x, topk_ids, topk_w and out may be device memory or pinned host memory that the device sees
  * at the same address (cudaHostAlloc / cudaHostRegister under unified addressing; check with
  * moe_pointer_device_accessible): the input quantisation, route preparation and reduce kernels
@@ -268,6 +283,32 @@ MOEFP8_API int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                          float clamp_limit, moe_scale_fmt act_fmt, int block_m,
                          moe_forward_path path, void* out, void* workspace, size_t ws_bytes,
                          cudaStream_t stream);
+/* Where the forward keeps its intermediate tensors inside the workspace: offsets[i] is the
+ * byte offset of region i (moe_ws_region) for these sizes and block_m (0 = the forward's own
+ * choice).  For inspecting a finished forward (the tests compare these tensors with the
+ * oracle); the regions are rewritten by every forward.  Host only.  Regions and layouts
+ * (slots = B_cap * block_m, KB = H/128, GN = N/128, S = the gate/up split count of
+ * moe_blockfp8_plan):
+ *   SORTED_IDX int32 [slots], BLOCK_EXPERT int32 [B_cap], NUM_BLOCKS int32 [1],
+ *   EXPERT_COUNT int32 [E_local], EXPERT_OFFSET int32 [E_local + 1], ROUTE_SLOT int32 [M*k]:
+ *     the outputs of moe_route_prepare;
+ *   XQ  E4M3 [slots, H]: the quantised input, row = slot of a kept route;
+ *   XS  f32 scales of XQ: STAGED [slots, KB]; FUSED K-block major [KB, slots];
+ *   GU  f32 gate/up partial sums: STAGED [S, slots, 2N] (split p covers K-blocks
+ *       [p*KB/S, (p+1)*KB/S)); FUSED [pieces, num_blocks * block_m, 2N], piece q of a
+ *       128-column tile is its q-th stream-K range (see moe_blockfp8_forward);
+ *   AQ  E4M3 [slots, N]: the quantised SiLU*mul activation; AS its scales: STAGED
+ *       [slots, GN]; FUSED [GN, slots];
+ *   Z   bf16 [M*k, H]: the down projection's output, route order.
+ * Returns MOE_OK or MOE_ERR_ARG. */
+typedef enum {
+    MOE_WS_SORTED_IDX = 0, MOE_WS_BLOCK_EXPERT = 1, MOE_WS_NUM_BLOCKS = 2, MOE_WS_EXPERT_COUNT = 3,
+    MOE_WS_EXPERT_OFFSET = 4, MOE_WS_ROUTE_SLOT = 5, MOE_WS_XQ = 6, MOE_WS_XS = 7, MOE_WS_GU = 8,
+    MOE_WS_AQ = 9, MOE_WS_AS = 10, MOE_WS_Z = 11, MOE_WS_REGIONS = 12
+} moe_ws_region;
+MOEFP8_API int moe_blockfp8_workspace_layout(int M, int k, int E, int E_local, int H, int N,
+                                             int block_m, size_t* offsets /*[MOE_WS_REGIONS]*/);
+
 /* The path moe_blockfp8_forward takes for path = AUTO at these sizes (FUSED or STAGED). */
 MOEFP8_API int moe_forward_path_for(int M, int k, int E, int E_local, int H, int N);
 
@@ -292,6 +333,10 @@ MOEFP8_API const char* moe_last_error_string(void);
 MOEFP8_API int moe_get_device_status(int* status, int reset);
 /* 1 if the current device is an sm_103 GPU the library was built for, else 0. */
 MOEFP8_API int moe_device_supported(void);
+/* The binary architecture version of the library's kernels as the CUDA runtime reports it for
+ * the current device (cudaFuncGetAttributes binaryVersion, 103 for sm_103a code), or -1 when
+ * it cannot be queried (no device). */
+MOEFP8_API int moe_kernel_binary_version(void);
 /* 1 if kernels on the current device can dereference p as it is: device memory of this device,
  * managed memory, or pinned host memory mapped at the same address; else 0 (also for null and
  * for pageable host memory).  Host only, no device work. */

@@ -146,3 +146,58 @@ def test_pack_weights_is_the_tile_regrouping(ops):
     torch.cuda.synchronize()
     ref = wq.view(3, 3, 128, 5, 128).permute(0, 1, 3, 2, 4).contiguous()
     assert torch.equal(t, ref)
+
+
+@pytest.mark.parametrize("proj", [0, 1])
+@pytest.mark.parametrize("M,k,E,bm,K,N_out,hot", [
+    (1, 8, 256, 16, 7168, 512, False),    # decode M=1: 8 active experts, 248 empty blocks
+    (32, 8, 256, 16, 7168, 512, False),   # decode M=32: ~165 active experts
+    (48, 4, 16, 16, 1024, 256, True),     # hot experts: several blocks per expert, 8 empty
+])
+def test_padded_grid_arm_vs_oracle(ops, proj, M, k, E, bm, K, N_out, hot):
+    """The padded-grid schedule (every expert owns a block, empty ones included), run through
+    the same grouped GEMM, computes the rows of the kept routes exactly as the compact schedule
+    does (oracle, within the GEMM tolerance) and writes nothing else -- so the active-block
+    comparison of the bench times a checked arm (lmdeploy PR #4956, "Motivation")."""
+    seed = M + K + (7 if hot else 0)
+    if hot:
+        r = np.random.default_rng(seed)
+        ids = np.stack([r.choice(8, k, replace=False) for _ in range(M)]).astype(np.int32)
+    else:
+        ids, _ = wl.routing_topk(M, E, k, seed=seed, kind="uniform")
+    rr = oracle.route_prepare(ids, E, None, E, bm)
+    pg = wl.padded_grid_route(rr["sorted_idx"], rr["block_expert"], rr["num_blocks"], E, bm)
+    assert pg["num_blocks"] == sum(max(1, int(np.ceil(c / bm))) for c in rr["expert_count"])
+    slots_p = pg["B_cap"] * bm
+    # activations in padded-grid slot order; every slot without a route holds NaN codes
+    x = wl.act_rows(slots_p, K, 1.0, seed=seed + 2)
+    aq, a_s = oracle.act_quant(0, x, K)
+    aq[pg["sorted_idx"] < 0] = 0x7F
+    a_s[pg["sorted_idx"] < 0] = np.nan
+    wq, ws = wl.quantized_weights(E, N_out, K, seed=seed + 3, device="cuda")
+    route = dict(sorted_idx=to_dev(pg["sorted_idx"]), block_expert=to_dev(pg["block_expert"]),
+                 num_blocks=to_dev(np.array([pg["num_blocks"]], np.int32)), B_cap=pg["B_cap"])
+    R = M * k
+    out_rows = slots_p if proj == 0 else R
+    sentinel = torch.full((out_rows, N_out), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = ops.moe_blockfp8_grouped_gemm(proj, to_dev(aq), to_dev(a_s), wq, ws, route, bm,
+                                        out_dtype=ops.DTYPE_BF16, out_rows=out_rows, out=sentinel)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    used = np.unique(pg["block_expert"][np.nonzero(pg["sorted_idx"] >= 0)[0] // bm])
+    used_d = torch.from_numpy(used.astype(np.int64)).cuda()
+    wq_h = np.zeros(tuple(wq.shape), np.uint8)
+    ws_h = np.ones(tuple(ws.shape), np.float32)
+    wq_h[used] = wq[used_d].cpu().numpy()
+    ws_h[used] = ws[used_d].cpu().numpy()
+    valid = np.nonzero(pg["sorted_idx"] >= 0)[0].astype(np.int32)
+    rexp = pg["block_expert"][valid // bm].astype(np.int32)
+    ref = oracle.route_gemm(aq, a_s, wq_h, ws_h, valid, rexp)
+    got = bf16_host(out)
+    rows = valid if proj == 0 else pg["sorted_idx"][valid]
+    assert_bf16_close(got[rows], ref, f"padded grid proj {proj}")
+    untouched = np.setdiff1d(np.arange(out_rows), rows)
+    assert (got[untouched] == bf16_host(torch.tensor([-7.0], dtype=torch.bfloat16))[0]).all()
+    # the compact slots map onto the padded grid one to one, routes unchanged
+    cs = np.nonzero(rr["sorted_idx"] >= 0)[0]
+    assert (pg["sorted_idx"][pg["slot_map"][cs]] == rr["sorted_idx"][cs]).all()

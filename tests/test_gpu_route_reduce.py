@@ -108,7 +108,30 @@ def test_moe_reduce_bitwise(ops, M, k, E, H, inv, use_map):
         ids = np.where(r.random(ids.shape) < inv, -1, ids).astype(np.int32)
     emap = wl.expert_map_random(E, max(1, E // 4), seed=2) if use_map else None
     z = wl.act_rows(M * k, H, 1.0, seed=H)
-    out = ops.moe_reduce(bf16_to_dev(z), to_dev(w), to_dev(ids), None if emap is None else to_dev(emap), E, H)
+    out = ops.moe_reduce(bf16_to_dev(z), to_dev(w), to_dev(ids), None if emap is None else to_dev(emap), E, H,
+                         E_local=None if emap is None else max(1, E // 4))
     torch.cuda.synchronize()
     ref = oracle.moe_reduce(z, w, ids, emap, E, H)
     assert (bf16_host(out) == ref).all()
+
+
+def test_moe_reduce_drops_routes_with_out_of_range_map_entries(ops):
+    """A map entry outside [0, E_local) drops the route in the reduce exactly as in route
+    preparation (which gives such a route no slot, so its expert output is never written): the
+    result equals the oracle's for the map with that entry set to -1."""
+    M, k, E, E_loc, H = 16, 6, 64, 16, 512
+    ids, w = wl.routing_topk(M, E, k, seed=77)
+    emap = wl.expert_map_random(E, E_loc, seed=78)
+    local_used = [g for g in np.unique(ids) if emap[g] >= 0]
+    bad = emap.copy()
+    bad[local_used[0]] = E_loc
+    bad[local_used[1]] = E_loc + 100
+    z = wl.act_rows(M * k, H, 1.0, seed=79)
+    out = ops.moe_reduce(bf16_to_dev(z), to_dev(w), to_dev(ids), to_dev(bad), E, H, E_local=E_loc)
+    torch.cuda.synchronize()
+    ok = emap.copy()
+    ok[local_used[0]] = -1
+    ok[local_used[1]] = -1
+    assert (bf16_host(out) == oracle.moe_reduce(z, w, ids, ok, E, H)).all()
+    with pytest.raises(ValueError):
+        ops.moe_reduce(bf16_to_dev(z), to_dev(w), to_dev(ids), to_dev(bad), E, H)  # E_local missing

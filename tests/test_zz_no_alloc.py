@@ -40,6 +40,15 @@ def test_noalloc_matches_workspace_route_prepare_twice_in_a_row(ops):
     assert ops.device_status() == 0
 
 
+def test_noalloc_at_its_maximum_size_then_a_smaller_call(ops):
+    """Every part of the fixed scratch in use: 65,536 routes (64 chunk histograms) over 1,024
+    local experts of 2,048 through an expert map, block_m 128; then a small call that reuses the
+    array (its ticket counter and offsets from the large call are still there)."""
+    _compare(ops, 8192, 8, 2048, 1024, 128, "uniform", seed=13)
+    _compare(ops, 37, 3, 64, 64, 16, "zipf", seed=14)
+    assert ops.device_status() == 0
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(ops):
     ids = to_dev(np.zeros((8193, 8), np.int32))  # 65,544 routes > 65,536
     with pytest.raises(ops.MoeError, match="at most 65536 routes"):
@@ -47,3 +56,6 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(ops):
     ids = to_dev(np.zeros((4, 2), np.int32))
     with pytest.raises(ops.MoeError, match="1024 local experts"):
         ops.moe_route_prepare_noalloc(ids, 2048, None, 2048, 16)
+    ids = to_dev(np.zeros((2, 5), np.int32))
+    with pytest.raises(ops.MoeError, match="top-k 5 > E 4"):
+        ops.moe_route_prepare_noalloc(ids, 4, None, 4, 16)
