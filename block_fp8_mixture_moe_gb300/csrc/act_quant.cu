@@ -402,11 +402,11 @@ int launch_aq_grid(const AQArgs& p, long long pairs, bool persistent, bool pdl, 
     return MOE_OK;
 }
 
-// Up to kInlinePairs group pairs (the decode layer up to 128 tokens at top-8 and N = 256) the
-// SiLU*mul and quantiser run inline; above, out of line.  Measured on GB300 (graph-replayed
-// decode layer, means of 480 steps): inline 34.9 vs 36.3 us at M = 1 and 161.1 vs 161.9 us at
-// M = 32, but 253.7 vs 252.6 us at M = 256.
-constexpr long long kInlinePairs = 1024;
+// Up to kInlinePairs group pairs the SiLU*mul and quantiser run inline; above, out of line.
+// Measured on GB300 (graph-replayed layers): inline 34.9 vs 36.3 us at decode M = 1 and 161.1
+// vs 161.9 us at M = 32, within noise at M = 256, and 115.8 vs 116.6 us at the expert-parallel
+// shape (T = 1024, N = 2048), where the kernel is issue-bound and the calls cost instructions.
+constexpr long long kInlinePairs = 1LL << 40;
 
 template <int ACT, bool F32IN, int KG>
 int launch_aq_kg(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream) {

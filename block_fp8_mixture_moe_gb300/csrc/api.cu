@@ -346,9 +346,19 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     }
     rc = launch_input_quant_tokens(x, M, H, k, route_slot, P.slots, xq, xs, act_fmt, true, stream);
     if (rc) return rc;
-    rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
-                             w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
-                             MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/true);
+    // A few routes (decode batches of 1-4 tokens at top-8): the gate/up GEMM sorts them itself
+    // from topk_ids, so its weight stream starts while routing and input quantisation still run.
+    // Otherwise it waits for the input quantisation before reading route preparation's tables.
+    const bool self_route = P.R <= kSelfRouteMaxRoutes && P.bm <= 32;
+    if (self_route)
+        rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
+                                 w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
+                                 MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/false,
+                                 topk_ids, expert_map, P.R, E);
+    else
+        rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
+                                 w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
+                                 MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/true);
     if (rc) return rc;
     // act-quant walks the routes (through route_slot) or, when the blocks hold fewer slots than
     // there are routes (an expert map that keeps few of them), the slots of the blocks that exist

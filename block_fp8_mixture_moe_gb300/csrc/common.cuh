@@ -57,11 +57,15 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         moe_weight_layout w_layout, const int32_t* sorted_idx, const int32_t* block_expert,
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
-                        cudaStream_t stream, bool wait_first = false);
+                        cudaStream_t stream, bool wait_first = false,
+                        const int32_t* self_ids = nullptr, const int32_t* self_map = nullptr,
+                        int self_R = 0, int self_E = 0);
+// Largest route count for which the gate/up GEMM derives its block table itself.
+constexpr int kSelfRouteMaxRoutes = 32;
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
                       const int32_t* expert_map, int M, int k, int E, int E_local, int H, void* out,
                       bool pdl, cudaStream_t stream);
-constexpr int kReduceMaxTopk = 16;  // top-k limit of the separate reduce kernel
+constexpr int kReduceMaxTopk = 32;  // top-k limit of the separate reduce kernel (a route per lane)
 
 // The fused layer kernel (everything after route preparation in one persistent launch).
 struct FusedLaunch {

@@ -63,6 +63,15 @@ struct GemmArgs {
     int* status;
     int wait_first;  // wait for the previous launch before anything (its predecessor is not done)
     int pdl;         // launched with programmatic dependent launch (else nothing to wait for)
+    // Self-routing (GATE_UP, at most 32 routes, block_m <= 32): the metadata warp derives the
+    // block table from the caller's top-k ids itself -- the same stable counting sort as route
+    // preparation's one-warp path, so the blocks, slots and rows are identical -- instead of
+    // reading route preparation's outputs.  The ids are an input of the layer, not an output of
+    // an earlier kernel, so the weight stream starts before routing and input quantisation are
+    // done; only the activation tiles and token scales wait for them.
+    const int32_t* self_ids;  // [self_R] global expert ids, or null
+    const int32_t* self_map;  // nullable [self_E]
+    int self_R, self_E;
 };
 
 template <int BM>
@@ -192,7 +201,12 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     // waits for it, and the next launch is released only after that wait, so that it may read
     // the routing early too.
     if (p.wait_first) grid_dep_wait();
-    grid_dep_launch();
+    // The next launch (the activation kernel) reads route preparation's outputs before it waits.
+    // A self-routing launch may begin before route preparation is complete, so it releases the
+    // next launch only after a thread of the CTA has waited for its own predecessor (whose
+    // completion implies route preparation's); the first release of a CTA counts.
+    const bool self_route = p.self_ids != nullptr;
+    if (!self_route) grid_dep_launch();
 
     if (warp == 6) {
         // ---------------- metadata warp ----------------
@@ -202,7 +216,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         // up to kSwMax / (K-blocks per unit) tiles; a unit longer than kCK K-blocks is cut into
         // one descriptor per kCK K-blocks.  All loads of a descriptor are issued before any of
         // its shared-memory stores.
-        int nblk = __ldcg(p.num_blocks);
+        int nblk = self_route ? 0 : __ldcg(p.num_blocks);
         nblk = max(0, min(nblk, p.B_cap));
         const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
         const long long u_lo = units * blockIdx.x / gridDim.x;
@@ -242,6 +256,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         auto flush_pending = [&]() {
             __syncwarp();  // lane 0's header stores are read by every lane
             grid_dep_wait();
+            if (self_route) grid_dep_launch();
             dep_done = true;
             for (int i = 0; i < npend; ++i) {
                 const int sl = pend0 + i < C::kRing ? pend0 + i : pend0 + i - C::kRing;
@@ -254,8 +269,64 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         int rows[(BM + 31) / 32];
 #pragma unroll
         for (int t = 0; t < (BM + 31) / 32; ++t) rows[t] = -1;
+        // self-routing: lane r holds route r; match-any groups the routes of one expert, so a
+        // route's rank in its expert is the number of same-expert lanes below it, and an
+        // expert's padded offset is the sum of the padded counts of the active experts below it
+        int sr_e = -1, sr_off = 0, sr_pad = 0, sr_cnt = 0;
+        bool sr_lead = false;
+        if constexpr (BM <= 32) {
+            if (self_route) {
+                int er = -1;
+                if (lane < p.self_R) {
+                    const int id = __ldg(p.self_ids + lane);
+                    if (id >= 0 && id < p.self_E) {
+                        const int le = p.self_map ? __ldg(p.self_map + id) : id;
+                        er = (le >= 0 && le < p.E_local) ? le : -1;
+                    }
+                }
+                const unsigned m = __match_any_sync(0xFFFFFFFFu, er);
+                unsigned lt;
+                asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+                sr_lead = er >= 0 && (m & lt) == 0;
+                sr_e = er;
+                sr_cnt = __popc(m);
+                sr_pad = sr_lead ? (sr_cnt + BM - 1) / BM * BM : 0;
+                int total = 0;
+                for (int j = 0; j < 32; ++j) {
+                    const int ej = __shfl_sync(0xFFFFFFFFu, er, j);
+                    const int pj = __shfl_sync(0xFFFFFFFFu, sr_pad, j);
+                    total += pj;
+                    sr_off += ej < er ? pj : 0;  // pj > 0 only for an active expert's leader
+                }
+                nblk = min(total / BM, p.B_cap);
+                const long long units_s = static_cast<long long>(nblk) * p.NT * p.splits;
+                const long long lo_s = units_s * blockIdx.x / gridDim.x;
+                nt = static_cast<int>(lo_s % p.NT);
+                sp = static_cast<int>((lo_s / p.NT) % p.splits);
+                b = static_cast<int>(lo_s / (static_cast<long long>(p.NT) * p.splits));
+                left = units_s * (blockIdx.x + 1) / gridDim.x - lo_s;
+            }
+        }
         while (left > 0 && ok) {
-            if (b != cur_b) {
+            if (self_route && b != cur_b) {
+                if constexpr (BM <= 32) {
+                    // block b belongs to the active expert whose padded run holds slot b*BM
+                    const unsigned own = __ballot_sync(0xFFFFFFFFu, sr_lead && sr_off <= b * BM &&
+                                                                        b * BM < sr_off + sr_pad);
+                    const int src = own ? __ffs(own) - 1 : 0;
+                    const int e_b = __shfl_sync(0xFFFFFFFFu, sr_e, src);
+                    const int off_b = __shfl_sync(0xFFFFFFFFu, sr_off, src);
+                    const int cnt_b = __shfl_sync(0xFFFFFFFFu, sr_cnt, src);
+                    e = own ? e_b : -1;
+                    int row = (lane < BM && e >= 0 && b * BM + lane - off_b < cnt_b) ? b * BM + lane : -1;
+                    if (row >= p.out_rows) {
+                        if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                        row = -1;
+                    }
+                    rows[0] = row;
+                }
+                cur_b = b;
+            } else if (b != cur_b) {
                 // the block's expert and its slot rows, loaded together
                 const int e_raw = __ldcg(p.block_expert + b);
                 int rr[(BM + 31) / 32];
@@ -368,6 +439,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
             };
             auto resolve = [&]() {
                 grid_dep_wait();
+                if (self_route) grid_dep_launch();
                 dep_done = true;
                 for (int i = 0; i < npend; ++i) load_a(pend_s[i], pend_kb[i], pend_nk[i], pend_b[i]);
                 npend = 0;
@@ -404,7 +476,11 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                             load_a(s, kb, nk, b);
                         } else {
                             pend_s[npend] = s; pend_kb[npend] = kb; pend_nk[npend] = nk; pend_b[npend] = b;
-                            if (++npend == C::kStages) resolve();  // every stage holds weights
+                            // wait when every stage holds weights -- or, self-routing, after the
+                            // first: the launch began only shortly before its predecessor ends, so
+                            // the wait is short, and the first stages' activation tiles then do
+                            // not queue behind all the other stages' weight tiles
+                            if (++npend == (self_route ? 1 : C::kStages)) resolve();
                         }
                         ++issued;
                         if (++s == C::kStages) { s = 0; ph ^= 1u; }
@@ -490,6 +566,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < C::kCpw; ++j) acc[j] = 0.0f;
         grid_dep_wait();  // (returns at once: the activations it consumes come after it)
+        if (self_route) grid_dep_launch();
         for (;;) {
             bool ok = mbar_wait_fast(dsa + slot, dph, abort_flag, p.status);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -655,7 +732,8 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         moe_weight_layout w_layout, const int32_t* sorted_idx, const int32_t* block_expert,
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
-                        cudaStream_t stream, bool wait_first) {
+                        cudaStream_t stream, bool wait_first, const int32_t* self_ids,
+                        const int32_t* self_map, int self_R, int self_E) {
     if (proj != MOE_PROJ_GATE_UP && proj != MOE_PROJ_DOWN) { set_error("grouped_gemm: bad proj"); return MOE_ERR_ARG; }
     if (!a_q || !a_s || !w_q || !w_s || !sorted_idx || !block_expert || !num_blocks || !out) {
         set_error("grouped_gemm: null pointer");
@@ -723,6 +801,17 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
     p.status = device_status_ptr();
     p.wait_first = wait_first ? 1 : 0;
     p.pdl = pdl ? 1 : 0;
+    if (self_ids) {
+        if (proj != MOE_PROJ_GATE_UP || block_m > 32 || self_R < 1 || self_R > 32 || self_E < 1 ||
+            !pdl || wait_first) {
+            set_error("grouped_gemm: self-routing needs GATE_UP, block_m <= 32, 1..32 routes and PDL");
+            return MOE_ERR_ARG;
+        }
+        p.self_ids = self_ids;
+        p.self_map = self_map;
+        p.self_R = self_R;
+        p.self_E = self_E;
+    }
     const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
     switch (block_m) {
         case 16: return launch_bm<16>(tw, ta, p, max_units, pdl, stream);

@@ -7,74 +7,120 @@
 // thread on fp32_acc); the terms are added in top-k order with one fused multiply-add each, so
 // the result does not depend on the launch shape.
 //
-// One thread produces 8 consecutive outputs of one token: per kept route one 16-byte load of 8
-// BF16 values (a warp reads 512 contiguous bytes), 8 FMAs, and one 16-byte store at the end.
-// HBM traffic is the kept routes' rows once plus the output once.  top-k is at most 16.
+// One warp produces 256 consecutive outputs of one token, 8 per lane.  Lane j < k holds route
+// j's id, weight and keep flag, so the kept routes form a warp-uniform bit mask that the warp
+// walks in top-k order: no shared memory, no barrier, no per-route predicate.  For each group
+// of up to eight kept routes a lane issues its 16-byte loads of 8 BF16 values together, then the
+// fused multiply-adds run in route order.  HBM traffic is the kept routes' rows once plus the
+// output once.  A grid of one wave walks the (token, 256-column chunk) items; the first item's
+// ids, weights and expert-map entries are caller inputs, read before the wait for the previous
+// kernel.  top-k is at most 32 (one route per lane).
 #include "common.cuh"
+
+#include <algorithm>
 
 namespace moe {
 namespace {
 
 constexpr int kMaxTopk = kReduceMaxTopk;
+constexpr int kThreads = 256;
+constexpr int kGroup = 8;  // kept routes whose loads are in flight together (top-8 in one round)
+static_assert(kMaxTopk <= 32, "one route per lane");
 
-// One CTA per (token, 1024-column slice): the token's top-k ids, weights and keep flags are
-// read once into shared memory; each thread then issues all its route loads back to back
-// before the fused multiply-adds, so the loads overlap instead of running one after another.
-__global__ void __launch_bounds__(128) k_moe_reduce(const uint16_t* __restrict__ z,
-                                                    const float* __restrict__ w,
-                                                    const int32_t* __restrict__ ids,
-                                                    const int32_t* __restrict__ map, int M, int k,
-                                                    int E, int E_local, int H,
-                                                    uint16_t* __restrict__ out) {
-    __shared__ float s_w[kMaxTopk];
-    __shared__ int s_keep[kMaxTopk];
-    grid_dep_launch();
-    const int t = blockIdx.x;
-    if (threadIdx.x < k) {
-        const int j = threadIdx.x;
-        const int id = __ldg(ids + static_cast<long long>(t) * k + j);
-        bool keep = id >= 0 && id < E;
+// The kept routes of token t as a bit mask (bit j: route j is kept); *wl = this lane's weight.
+__device__ __forceinline__ unsigned token_routes(const int32_t* __restrict__ ids,
+                                                 const float* __restrict__ w,
+                                                 const int32_t* __restrict__ map, int t, int k,
+                                                 int E, int E_local, int lane, float* wl) {
+    bool keep = false;
+    *wl = 0.0f;
+    if (lane < k) {
+        const long long r = static_cast<long long>(t) * k + lane;
+        const int id = __ldg(ids + r);
+        *wl = __ldg(w + r);
+        keep = id >= 0 && id < E;
         if (keep && map) {
             // the route-preparation rule: a map entry outside [0, E_local) gives the route no
             // slot, so its z row was never written and it adds nothing here either
             const int le = __ldg(map + id);
             keep = le >= 0 && le < E_local;
         }
-        s_keep[j] = keep ? 1 : 0;
-        s_w[j] = __ldg(w + static_cast<long long>(t) * k + j);
     }
-    // ids, weights and the expert map are the caller's inputs, not the previous kernel's
-    // outputs: they are read above; the expert outputs z are read after the wait
-    grid_dep_wait();
-    __syncthreads();
-    const int col = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
-    if (col >= H) return;
-    uint4 v[kMaxTopk];
+    return __ballot_sync(0xFFFFFFFFu, keep);
+}
+
+__global__ void __launch_bounds__(kThreads) k_moe_reduce(const uint16_t* __restrict__ z,
+                                                         const float* __restrict__ w,
+                                                         const int32_t* __restrict__ ids,
+                                                         const int32_t* __restrict__ map, int M,
+                                                         int k, int E, int E_local, int H,
+                                                         uint16_t* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = (H + 255) / 256;
+    const long long items = static_cast<long long>(M) * chunks;
+    const int wpb = blockDim.x >> 5;
+    const long long stride = static_cast<long long>(gridDim.x) * wpb;
+    long long it = static_cast<long long>(blockIdx.x) * wpb + (threadIdx.x >> 5);
+    grid_dep_launch();
+    float wl = 0.0f;
+    unsigned keep = 0;
+    int t = -1;
+    if (it < items) {
+        t = static_cast<int>(it / chunks);
+        keep = token_routes(ids, w, map, t, k, E, E_local, lane, &wl);
+    }
+    grid_dep_wait();  // the expert outputs z are the previous kernel's
+    for (; it < items; it += stride) {
+        const int tt = static_cast<int>(it / chunks);
+        if (tt != t) {
+            t = tt;
+            keep = token_routes(ids, w, map, t, k, E, E_local, lane, &wl);
+        }
+        const int col = static_cast<int>(it - static_cast<long long>(t) * chunks) * 256 + lane * 8;
+        const bool act = col < H;
+        const uint16_t* zt = z + static_cast<long long>(t) * k * H + col;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        unsigned rest = keep;
+        while (rest) {
+            int jg[kGroup];
+            uint4 vg[kGroup];
+            int n = 0;
 #pragma unroll
-    for (int j = 0; j < kMaxTopk; ++j)
-        if (j < k && s_keep[j])
-            v[j] = __ldcg(reinterpret_cast<const uint4*>(z + (static_cast<long long>(t) * k + j) * H + col));
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < kGroup; ++q) {
+                jg[q] = rest ? __ffs(rest) - 1 : 0;
+                if (rest) { rest &= rest - 1; ++n; }
+            }
 #pragma unroll
-    for (int j = 0; j < kMaxTopk; ++j) {
-        if (j < k && s_keep[j]) {
-            const float wj = s_w[j];
-            acc[0] = __fmaf_rn(wj, bf16_lo(v[j].x), acc[0]);
-            acc[1] = __fmaf_rn(wj, bf16_hi(v[j].x), acc[1]);
-            acc[2] = __fmaf_rn(wj, bf16_lo(v[j].y), acc[2]);
-            acc[3] = __fmaf_rn(wj, bf16_hi(v[j].y), acc[3]);
-            acc[4] = __fmaf_rn(wj, bf16_lo(v[j].z), acc[4]);
-            acc[5] = __fmaf_rn(wj, bf16_hi(v[j].z), acc[5]);
-            acc[6] = __fmaf_rn(wj, bf16_lo(v[j].w), acc[6]);
-            acc[7] = __fmaf_rn(wj, bf16_hi(v[j].w), acc[7]);
+            for (int q = 0; q < kGroup; ++q)
+                if (q < n && act)
+                    vg[q] = __ldcg(reinterpret_cast<const uint4*>(zt + static_cast<long long>(jg[q]) * H));
+#pragma unroll
+            for (int q = 0; q < kGroup; ++q) {
+                if (q < n) {
+                    const float wj = __shfl_sync(0xFFFFFFFFu, wl, jg[q]);
+                    if (act) {
+                        const uint4 v = vg[q];
+                        acc[0] = __fmaf_rn(wj, bf16_lo(v.x), acc[0]);
+                        acc[1] = __fmaf_rn(wj, bf16_hi(v.x), acc[1]);
+                        acc[2] = __fmaf_rn(wj, bf16_lo(v.y), acc[2]);
+                        acc[3] = __fmaf_rn(wj, bf16_hi(v.y), acc[3]);
+                        acc[4] = __fmaf_rn(wj, bf16_lo(v.z), acc[4]);
+                        acc[5] = __fmaf_rn(wj, bf16_hi(v.z), acc[5]);
+                        acc[6] = __fmaf_rn(wj, bf16_lo(v.w), acc[6]);
+                        acc[7] = __fmaf_rn(wj, bf16_hi(v.w), acc[7]);
+                    }
+                }
+            }
+        }
+        if (act) {
+            uint4 o;
+            o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
+            o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
+            o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
+            o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
+            *reinterpret_cast<uint4*>(out + static_cast<long long>(t) * H + col) = o;
         }
     }
-    uint4 o;
-    o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
-    o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
-    o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
-    o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
-    *reinterpret_cast<uint4*>(out + static_cast<long long>(t) * H + col) = o;
 }
 
 }  // namespace
@@ -90,13 +136,29 @@ int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_id
         set_error("moe_reduce: without an expert map E_local must equal E (%d vs %d)", E_local, E);
         return MOE_ERR_EXPERT_SLICE;
     }
-    const long long total = static_cast<long long>(M) * (H / 8);
-    if (total == 0) return MOE_OK;
+    if (k > kMaxTopk) { set_error("moe_reduce: top-k above %d is not supported", kMaxTopk); return MOE_ERR_ARG; }
+    const long long items = static_cast<long long>(M) * ((H + 255) / 256);
+    if (items == 0) return MOE_OK;
     if (!z || !topk_w || !topk_ids || !out) { set_error("moe_reduce: null pointer"); return MOE_ERR_ARG; }
     if (!aligned16(z) || !aligned16(out)) { set_error("moe_reduce: z and out must be 16-byte aligned"); return MOE_ERR_ARG; }
-    if (k > kMaxTopk) { set_error("moe_reduce: top-k above %d is not supported", kMaxTopk); return MOE_ERR_ARG; }
-    const int slices = (H / 8 + 127) / 128;
-    Launch L(dim3(static_cast<unsigned>(M), static_cast<unsigned>(slices)), dim3(128), 0, stream, pdl);
+    // Few items (decode batches of a few tokens): one item per warp in CTAs of two warps, one
+    // CTA per SM -- small enough in registers to become resident beside a grouped-GEMM CTA, so
+    // the CTAs launched early by programmatic dependent launch wait on the SMs while the down
+    // GEMM finishes.  Otherwise one wave of full CTAs, as many as are resident at once.
+    const int sms = sm_count();
+    int threads = kThreads;
+    long long blocks;
+    if (items <= 2LL * sms) {
+        threads = 64;
+        blocks = (items + 1) / 2;
+    } else {
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_moe_reduce, kThreads, 0) != cudaSuccess || occ < 1)
+            occ = 1;
+        const long long need = (items + kThreads / 32 - 1) / (kThreads / 32);
+        blocks = std::min<long long>(need, static_cast<long long>(sms) * occ);
+    }
+    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, pdl);
     cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_moe_reduce, static_cast<const uint16_t*>(z),
                                        topk_w, topk_ids, expert_map, M, k, E, E_local, H,
                                        static_cast<uint16_t*>(out));

@@ -56,6 +56,7 @@ struct RouteArgs {
     // optional: words the next kernel needs at zero (its phase counters), cleared here
     uint32_t* zero_ptr;
     int zero_n;
+    int compact;  // single CTA with an expert map: compact the kept routes first
 };
 
 // Clears the caller's zero region (grid-stride over the launch).
@@ -150,24 +151,26 @@ __device__ __forceinline__ void column_scan(uint16_t* wcnt, int nw, int E_loc, i
     }
 }
 
-// Stable scatter of this CTA's routes (local ids in `loc`, global route id = first + i).
+// Stable scatter of this CTA's routes (local ids in `loc`, global route id = first + i, or
+// ridx[i] for a compacted list of kept routes).
 // slot = start[e] + chunk_base(e) + warp rank + rank in the 32-group.
 __device__ __forceinline__ void warp_scatter(const RouteArgs& p, const int* loc, int n, int first,
                                              int per_warp, uint16_t* row, const int* start,
-                                             const int32_t* chunk_base) {
+                                             const int32_t* chunk_base, const int* ridx = nullptr) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int lo = w * per_warp, hi = min(n, lo + per_warp);
     for (int base = lo; base < hi; base += 32) {
         const int r = base + lane;
         const int e = r < hi ? loc[r] : -1;
         const unsigned m = __match_any_sync(kFull, e);
+        const int route = ridx ? (r < hi ? ridx[r] : -1) : first + r;
         if (e >= 0) {
             int slot = start[e] + row[e] + __popc(m & lanemask_lt());
             if (chunk_base) slot += chunk_base[e];
-            p.sorted_idx[slot] = first + r;
-            if (p.route_slot) p.route_slot[first + r] = slot;
+            p.sorted_idx[slot] = route;
+            if (p.route_slot) p.route_slot[route] = slot;
         } else if (r < hi && p.route_slot) {
-            p.route_slot[first + r] = -1;
+            p.route_slot[route] = -1;
         }
         __syncwarp();
         if (e >= 0 && lane == __ffs(m) - 1) row[e] = static_cast<uint16_t>(row[e] + __popc(m));
@@ -195,11 +198,15 @@ __device__ void write_metadata(const RouteArgs& p, const int* tot, const int* st
     }
 }
 
-// shared memory of the single-CTA kernel: loc[R] | start[E_loc+1] | tot[E_loc] | tmp[33] | wcnt
-size_t single_smem_bytes(int R, int E_loc) {
-    size_t ints = static_cast<size_t>(R) + (E_loc + 1) + E_loc + 33;
-    ints = (ints + 3) & ~static_cast<size_t>(3);
-    return ints * 4 + static_cast<size_t>(kSingleWarps) * E_loc * 2;
+// Shared memory of the single-CTA kernel: loc[R] | start[E_loc+1] | tot[E_loc] | tmp[33] |
+// wcnt[32][E_loc] (uint16), and with an expert map also smap[E] | kloc[R] | kidx[R].
+__host__ __device__ inline size_t single_ints(int R, int E_loc) {
+    const size_t ints = static_cast<size_t>(R) + (E_loc + 1) + E_loc + 33;
+    return (ints + 3) & ~static_cast<size_t>(3);
+}
+size_t single_smem_bytes(int R, int E, int E_loc, bool map) {
+    const size_t base = single_ints(R, E_loc) * 4 + static_cast<size_t>(kSingleWarps) * E_loc * 2;
+    return map ? ((base + 15) & ~static_cast<size_t>(15)) + (static_cast<size_t>(E) + 2 * R) * 4 : base;
 }
 
 __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
@@ -208,18 +215,81 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
     int* start = loc + p.R;
     int* tot = start + p.E_loc + 1;
     int* tmp = tot + p.E_loc;
-    size_t ints = static_cast<size_t>(p.R) + (p.E_loc + 1) + p.E_loc + 33;
-    ints = (ints + 3) & ~static_cast<size_t>(3);
+    const size_t ints = single_ints(p.R, p.E_loc);
     uint16_t* wcnt = reinterpret_cast<uint16_t*>(sm + ints);
     grid_dep_wait();
     grid_dep_launch();
     clear_zero_region(p);
-    for (int r = threadIdx.x; r < p.R; r += blockDim.x) loc[r] = local_of(p, r);
-    for (int i = threadIdx.x; i < kSingleWarps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
-    __syncthreads();
-    const int per_warp = (p.R + kSingleWarps - 1) / kSingleWarps;
+    int n = p.R;         // routes the sort walks
+    const int* key = loc;
+    const int* ridx = nullptr;
+    if (p.compact) {
+        // With an expert map most routes are usually dropped (an expert-parallel slice keeps
+        // about 1/8): the map is staged in shared memory next to the ids, so a route's local
+        // expert costs no second dependent global load, and the kept routes are compacted in
+        // route order (a block scan) before the sort, which then walks only them.
+        int* smap = reinterpret_cast<int*>(
+            (reinterpret_cast<uintptr_t>(wcnt + kSingleWarps * p.E_loc) + 15) & ~static_cast<uintptr_t>(15));
+        int* kloc = smap + p.E;
+        int* kidx = kloc + p.R;
+        for (int i = threadIdx.x; i < p.E; i += blockDim.x) smap[i] = __ldg(p.map + i);
+        for (int r = threadIdx.x; r < p.R; r += blockDim.x) loc[r] = __ldg(p.ids + r);
+        for (int i = threadIdx.x; i < kSingleWarps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
+        __syncthreads();
+        for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
+            const int id = loc[r];
+            int e = (id < 0 || id >= p.E) ? -1 : smap[id];
+            if (e < -1 || e >= p.E_loc) {
+                if (p.status) atomicOr(p.status, MOE_DEV_BAD_EXPERT_MAP);
+                e = -1;
+            }
+            loc[r] = e;
+            if (e < 0 && p.route_slot) p.route_slot[r] = -1;
+        }
+        __syncthreads();
+        // stable compaction: thread t owns routes [t*per, (t+1)*per)
+        const int per = (p.R + blockDim.x - 1) / blockDim.x;
+        const int lo = min(p.R, static_cast<int>(threadIdx.x) * per), hi = min(p.R, lo + per);
+        int cnt = 0;
+        for (int r = lo; r < hi; ++r) cnt += loc[r] >= 0;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) tmp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int nw = blockDim.x >> 5;
+            const int v = lane < nw ? tmp[lane] : 0;
+            int sc = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(kFull, sc, o);
+                if (lane >= o) sc += u;
+            }
+            if (lane < nw) tmp[lane] = sc - v;
+            if (lane == 31) tmp[32] = sc;
+        }
+        __syncthreads();
+        int pos = tmp[warp] + incl - cnt;
+        for (int r = lo; r < hi; ++r) {
+            if (loc[r] >= 0) { kloc[pos] = loc[r]; kidx[pos] = r; ++pos; }
+        }
+        n = tmp[32];
+        key = kloc;
+        ridx = kidx;
+        __syncthreads();
+    } else {
+        for (int r = threadIdx.x; r < p.R; r += blockDim.x) loc[r] = local_of(p, r);
+        for (int i = threadIdx.x; i < kSingleWarps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
+        __syncthreads();
+    }
+    const int per_warp = (n + kSingleWarps - 1) / kSingleWarps;
     uint16_t* row = wcnt + (threadIdx.x >> 5) * p.E_loc;
-    warp_histogram(loc, p.R, per_warp, row);
+    warp_histogram(key, n, per_warp, row);
     __syncthreads();
     column_scan(wcnt, kSingleWarps, p.E_loc, tot);
     __syncthreads();
@@ -230,7 +300,7 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
     if (threadIdx.x == 0) start[p.E_loc] = total;
     __syncthreads();
     write_metadata(p, tot, start);
-    warp_scatter(p, loc, p.R, 0, per_warp, row, start, nullptr);
+    warp_scatter(p, key, n, 0, per_warp, row, start, nullptr, ridx);
 }
 
 // At most 32 routes: one warp holds a route per lane.  __match_any_sync groups the lanes of
@@ -460,7 +530,9 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
                       kSingleMaxRoutes, kSingleMaxExperts);
             return MOE_ERR_ARG;
         }
-        const size_t smem = single_smem_bytes(R, E_local);
+        // with an expert map, the compacting variant when its shared memory fits comfortably
+        p.compact = expert_map && single_smem_bytes(R, E, E_local, true) <= 200 * 1024 ? 1 : 0;
+        const size_t smem = single_smem_bytes(R, E, E_local, p.compact != 0);
         if (!ensure_smem(reinterpret_cast<const void*>(k_route_single), static_cast<int>(smem))) {
             set_error("route single: shared-memory limit %zu refused", smem);
             return MOE_ERR_LAUNCH;

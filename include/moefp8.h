@@ -237,7 +237,7 @@ MOEFP8_API int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, f
  * entry for which route preparation gave the route no slot).
  *   z [M*k, H] bf16 (route order); topk_w [M, k] f32; topk_ids [M, k] int32;
  *   expert_map nullable [E] (without it E_local must equal E); out [M, H] bf16.  H multiple
- *   of 8, k <= 16; pointers 16-byte aligned.
+ *   of 8, k <= 32; pointers 16-byte aligned.
  * ------------------------------------------------------------------------------------------ */
 MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
                const int32_t* expert_map, int M, int k, int E, int E_local, int H, void* out,
@@ -264,7 +264,7 @@ MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* top
  *   so the fp32 summation order of the gate/up partial sums (not the arithmetic of any stage)
  *   depends on the SM count.  path STAGED: one launch per stage.  AUTO: see
  *   moe_forward_path_for.
- * H and N multiples of 128; k <= E.  The staged path's reduce takes k <= 16: STAGED with a
+ * H and N multiples of 128; k <= E.  The staged path's reduce takes k <= 32: STAGED with a
  * larger k is refused (MOE_ERR_ARG, nothing enqueued) and AUTO then takes FUSED, which has no
  * top-k limit.  All stages run on `stream` with no host synchronisation, so the call can be
  * captured in a CUDA graph.

@@ -186,13 +186,15 @@ def test_decode_hot_experts(ops, path):
 
 
 @pytest.mark.parametrize("path", [FUSED, STAGED])
-def test_graphs_with_different_routings_share_a_workspace(ops, path):
+@pytest.mark.parametrize("M", [16, 3])
+def test_graphs_with_different_routings_share_a_workspace(ops, path, M):
     """Three captured forwards with different routings on one workspace, replayed in a mixed
     order: every replay reproduces its own eager output bit for bit, so no state (counters,
-    block tables, cleared regions) carries over from the previous call."""
-    cfg = dict(wl.CONFIGS["decode"], M=16)
+    block tables, cleared regions) carries over from the previous call.  M = 3 (24 routes)
+    runs the self-routed gate/up GEMM."""
+    cfg = dict(wl.CONFIGS["decode"], M=M)
     L = wl.make_layer(**cfg, seed=8, device="cuda")
-    M, H, E, k = 16, cfg["H"], cfg["E"], cfg["k"]
+    H, E, k = cfg["H"], cfg["E"], cfg["k"]
     x = bf16_to_dev(L["x"])
     routes = []
     for s in range(3):
@@ -234,6 +236,7 @@ def test_host_activations_zero_copy(ops, path):
     the host link, bit for bit the result of the same call on device copies (decode M=16, and
     an expert-parallel slice with dropped routes and UE8M0 scales)."""
     cases = [(dict(wl.CONFIGS["decode"], M=16), 9, {}),
+             (dict(wl.CONFIGS["decode"], M=4), 11, {}),  # 32 routes: the self-routed gate/up GEMM
              (dict(wl.CONFIGS["ep"], M=10), 10, dict(clamp_limit=7.0, act_fmt=1))]
     for cfg, seed, kw in cases:
         L = wl.make_layer(**cfg, seed=seed, device="cuda")

@@ -155,12 +155,14 @@ def test_layer_intermediates_vs_oracle(ops, name, cfg, seed, opt, path):
 
 
 @pytest.mark.parametrize("path", [FUSED, STAGED])
-def test_out_of_range_map_entry_drops_the_route(ops, path):
+@pytest.mark.parametrize("M", [10, 5])
+def test_out_of_range_map_entry_drops_the_route(ops, path, M):
     """An expert map entry outside [-1, E_local) is an invalid slice: route preparation gives
     the route no slot and flags MOE_DEV_BAD_EXPERT_MAP, and every later stage -- the reduce
     included -- drops the route.  Both paths give the oracle's output for the map with that
-    entry set to -1 (lmdeploy PR #4857 review: validate the local-expert slice)."""
-    cfg = dict(wl.CONFIGS["ep"], M=10)
+    entry set to -1 (lmdeploy PR #4857 review: validate the local-expert slice).  M = 5 (30
+    routes) runs the self-routed gate/up GEMM, which must drop the route in the same way."""
+    cfg = dict(wl.CONFIGS["ep"], M=M)
     L = wl.make_layer(**cfg, seed=25, device="cuda")
     emap = L["expert_map"].copy()
     used = np.unique(L["topk_ids"])
@@ -183,17 +185,26 @@ def test_out_of_range_map_entry_drops_the_route(ops, path):
     assert ops.device_status() == 0
 
 
-def test_staged_path_refuses_topk_above_16(ops):
-    """The staged reduce takes top-k <= 16: an explicit STAGED call with k = 17 is refused
-    before anything is enqueued, and AUTO takes the fused path, which matches the oracle."""
-    L = wl.make_layer(M=3, H=256, N=128, E=20, k=17, seed=26, device="cuda")
+def test_staged_path_refuses_topk_above_32(ops):
+    """The staged reduce takes top-k <= 32 (one route per lane): an explicit STAGED call with
+    k = 33 is refused before anything is enqueued, and AUTO takes the fused path, which matches
+    the oracle; k = 32 runs staged and matches too."""
+    L = wl.make_layer(M=3, H=256, N=128, E=40, k=33, seed=26, device="cuda")
     args = (bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"]), L["E"], None,
             L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"])
-    with pytest.raises(ops.MoeError, match="top-k <= 16"):
+    with pytest.raises(ops.MoeError, match="top-k <= 32"):
         ops.moe_blockfp8_forward(*args, path=STAGED)
-    assert ops.moe_forward_path_for(3, 17, 20, 20, 256, 128) == FUSED
+    assert ops.moe_forward_path_for(3, 33, 40, 40, 256, 128) == FUSED
     out = ops.moe_blockfp8_forward(*args)
     torch.cuda.synchronize()
     assert ops.device_status() == 0
     ref = oracle.moe_forward(wl.layer_numpy(L))
-    assert_bf16_close(out.view(torch.int16).cpu().numpy().view(np.uint16), ref, "top-k 17")
+    assert_bf16_close(out.view(torch.int16).cpu().numpy().view(np.uint16), ref, "top-k 33")
+    L32 = wl.make_layer(M=3, H=256, N=128, E=40, k=32, seed=27, device="cuda")
+    out = ops.moe_blockfp8_forward(bf16_to_dev(L32["x"]), to_dev(L32["topk_ids"]), to_dev(L32["topk_w"]),
+                                   L32["E"], None, L32["wgu_q"], L32["wgu_s"], L32["wd_q"], L32["wd_s"],
+                                   path=STAGED)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    ref = oracle.moe_forward(wl.layer_numpy(L32))
+    assert_bf16_close(out.view(torch.int16).cpu().numpy().view(np.uint16), ref, "top-k 32")

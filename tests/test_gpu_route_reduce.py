@@ -99,6 +99,9 @@ def test_route_prepare_empty(ops):
 @pytest.mark.parametrize("M,k,E,H,inv,use_map", [
     (1, 8, 256, 7168, 0.0, False), (32, 8, 256, 7168, 0.1, False), (7, 6, 256, 2048, 0.2, True),
     (512, 8, 512, 4096, 0.0, False), (3, 1, 4, 8, 0.0, False), (0, 8, 16, 512, 0.0, False),
+    (1024, 6, 256, 2048, 0.0, True),   # expert-parallel shape: most routes dropped
+    (5, 32, 64, 264, 0.3, False),      # the largest top-k, a ragged last 256-column chunk
+    (9, 17, 40, 136, 0.0, True),
 ])
 def test_moe_reduce_bitwise(ops, M, k, E, H, inv, use_map):
     """fp32 fused multiply-adds in top-k order on both sides: bit-exact."""
