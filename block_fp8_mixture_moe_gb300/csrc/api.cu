@@ -326,12 +326,13 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     const bool fused = path == MOE_FORWARD_FUSED;
     unsigned* sync = reinterpret_cast<unsigned*>(ws + P.off_sync);
 
-    int rc = launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, P.bm, MOE_ROUTE_AUTO,
-                                  sorted_idx, block_expert, num_blocks, counts, offsets,
-                                  route_slot, ws + P.off_rws, rws_bytes, false, stream,
-                                  fused ? sync : nullptr, fused ? fused_counter_words(P.B_cap) : 0);
-    if (rc) return rc;
+    int rc;
     if (fused) {
+        rc = launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, P.bm, MOE_ROUTE_AUTO,
+                                  sorted_idx, block_expert, num_blocks, counts, offsets,
+                                  route_slot, ws + P.off_rws, rws_bytes, false, stream, sync,
+                                  fused_counter_words(P.B_cap));
+        if (rc) return rc;
         FusedLaunch f{};
         f.x = x; f.topk_ids = topk_ids; f.topk_w = topk_w; f.expert_map = expert_map;
         f.M = M; f.k = k; f.E = E; f.E_local = E_local; f.H = H; f.N = N; f.bm = P.bm;
@@ -344,6 +345,10 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
         f.sync = sync;
         return launch_fused_layer(f, stream);
     }
+    rc = launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, P.bm, MOE_ROUTE_AUTO,
+                              sorted_idx, block_expert, num_blocks, counts, offsets, route_slot,
+                              ws + P.off_rws, rws_bytes, false, stream);
+    if (rc) return rc;
     rc = launch_input_quant_tokens(x, M, H, k, route_slot, P.slots, xq, xs, act_fmt, true, stream);
     if (rc) return rc;
     // A few routes (decode batches of 1-4 tokens at top-8): the gate/up GEMM sorts them itself

@@ -312,62 +312,89 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
 constexpr int kWarpMaxRoutes = 32;
 constexpr int kWarpThreads = 256;
 
-__global__ void __launch_bounds__(kWarpThreads, 1) k_route_warp(RouteArgs p) {
-    __shared__ int t_e[32], t_cnt[32], t_pad[32];
-    __shared__ int t_n;
-    grid_dep_wait();
-    grid_dep_launch();
-    clear_zero_region(p);
+// The one-warp sort's table: the active experts of at most 32 routes (local id, route count,
+// padded count), in the order of their leading lanes.
+struct WarpTable {
+    int e[32], cnt[32], pad[32];
+    int n;
+};
+
+// Before a CTA barrier: lane r of warp 0 takes route r (its local expert in *e, its stable rank
+// among the same-expert lanes in *rank) and fills the table; with `pads`, the CTA's other warps
+// meanwhile write every -1 pad of sorted_idx and block_expert.
+__device__ __forceinline__ void warp_table_build(const RouteArgs& p, WarpTable& t, bool pads,
+                                                 int* e, int* rank) {
     const int tid = threadIdx.x, lane = tid & 31;
-    int e = -1, rank = 0;
+    *e = -1;
+    *rank = 0;
     if (tid < 32) {
-        e = lane < p.R ? local_of(p, lane) : -1;
-        const unsigned m = __match_any_sync(kFull, e);
-        rank = __popc(m & lanemask_lt());
-        const bool lead = e >= 0 && rank == 0;
+        const int er = lane < p.R ? local_of(p, lane) : -1;
+        const unsigned m = __match_any_sync(kFull, er);
+        const int rk = __popc(m & lanemask_lt());
+        const bool lead = er >= 0 && rk == 0;
         const unsigned leads = __ballot_sync(kFull, lead);
         if (lead) {
             const int i = __popc(leads & lanemask_lt());
             const int c = __popc(m);
-            t_e[i] = e;
-            t_cnt[i] = c;
-            t_pad[i] = ((c + p.bm - 1) >> p.bm_shift) << p.bm_shift;
+            t.e[i] = er;
+            t.cnt[i] = c;
+            t.pad[i] = ((c + p.bm - 1) >> p.bm_shift) << p.bm_shift;
         }
-        if (lane == 0) t_n = __popc(leads);
-    } else {
-        const int nthr = blockDim.x - 32, t = tid - 32;
-        for (long long sl = t; sl < (static_cast<long long>(p.B_cap) << p.bm_shift); sl += nthr) p.sorted_idx[sl] = -1;
-        for (int b = t; b < p.B_cap; b += nthr) p.block_expert[b] = -1;
+        if (lane == 0) t.n = __popc(leads);
+        *e = er;
+        *rank = rk;
+    } else if (pads) {
+        const int nthr = blockDim.x - 32, u = tid - 32;
+        for (long long sl = u; sl < (static_cast<long long>(p.B_cap) << p.bm_shift); sl += nthr) p.sorted_idx[sl] = -1;
+        for (int b = u; b < p.B_cap; b += nthr) p.block_expert[b] = -1;
     }
-    __syncthreads();
-    const int n = t_n;
-    // padded offset of local expert x: the padded counts of the active experts below it
-    auto offset_of = [&](int x) {
-        int off = 0;
-        for (int i = 0; i < n; ++i) off += t_e[i] < x ? t_pad[i] : 0;
-        return off;
-    };
+}
+
+// After the barrier: the padded offset of local expert x (the padded counts of the active
+// experts below it).
+__device__ __forceinline__ int warp_table_offset(const WarpTable& t, int x) {
+    int off = 0;
+    for (int i = 0; i < t.n; ++i) off += t.e[i] < x ? t.pad[i] : 0;
+    return off;
+}
+
+// After the barrier: counts, offsets, block table, block count and the real sorted_idx and
+// route_slot entries (over the pads written before it).
+__device__ __forceinline__ void warp_table_write(const RouteArgs& p, const WarpTable& t, int e, int rank) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int n = t.n;
     for (int x = tid; x < p.E_loc; x += blockDim.x) {
         int c = 0;
-        for (int i = 0; i < n; ++i) c = t_e[i] == x ? t_cnt[i] : c;
+        for (int i = 0; i < n; ++i) c = t.e[i] == x ? t.cnt[i] : c;
         p.count[x] = c;
-        if (p.offset) p.offset[x] = offset_of(x);
+        if (p.offset) p.offset[x] = warp_table_offset(t, x);
     }
     if (tid < n) {
-        const int off = offset_of(t_e[tid]);
-        for (int b = off >> p.bm_shift; b < ((off + t_pad[tid]) >> p.bm_shift); ++b) p.block_expert[b] = t_e[tid];
+        const int off = warp_table_offset(t, t.e[tid]);
+        for (int b = off >> p.bm_shift; b < ((off + t.pad[tid]) >> p.bm_shift); ++b) p.block_expert[b] = t.e[tid];
     }
     if (tid == 0) {
         int total = 0;
-        for (int i = 0; i < n; ++i) total += t_pad[i];
+        for (int i = 0; i < n; ++i) total += t.pad[i];
         *p.num_blocks = total >> p.bm_shift;
         if (p.offset) p.offset[p.E_loc] = total;
     }
     if (tid < 32 && lane < p.R) {
-        const int slot = e >= 0 ? offset_of(e) + rank : -1;
+        const int slot = e >= 0 ? warp_table_offset(t, e) + rank : -1;
         if (e >= 0) p.sorted_idx[slot] = lane;
         if (p.route_slot) p.route_slot[lane] = slot;
     }
+}
+
+__global__ void __launch_bounds__(kWarpThreads, 1) k_route_warp(RouteArgs p) {
+    __shared__ WarpTable t;
+    grid_dep_wait();
+    grid_dep_launch();
+    clear_zero_region(p);
+    int e, rank;
+    warp_table_build(p, t, true, &e, &rank);
+    __syncthreads();
+    warp_table_write(p, t, e, rank);
 }
 
 // Multi-CTA kernel 1: chunk histograms; the last CTA to finish builds the metadata.
