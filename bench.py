@@ -66,6 +66,15 @@ def parse():
     return ap.parse_args()
 
 
+def workload_config(M, seed):
+    """The workload both arms (the library and the CPU oracle) report, as the same dict."""
+    H, N, E, k = DECODE["H"], DECODE["N"], DECODE["E"], DECODE["k"]
+    return {"workload": f"decode MoE layer M={M} H={H} N={N} E={E} top-k={k}, block-FP8 128x128",
+            "M": M, "H": H, "N": N, "E": E, "topk": k, "routing": "uniform (softmax top-k of N(0,1) logits)",
+            "weights": "E4M3, fp32 scale per 128x128 block, ~N(0, 0.02)", "activations": "BF16 ~N(0,1)",
+            "seed": seed, "routing_batches": NROT}
+
+
 def dist_setup(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -337,9 +346,15 @@ def run_ours(args):
             "stages_decode": dict(M=M, **stage_times(ops, dev, stream, flush, xs, ids, ws, wgu_use, wgu_s, wd_use,
                                                      wd_s, M, H, N, E, k, act, hbm_peak)),
             "act_quant": act_quant_arms(ops, dev, stream, flush),
+            "act_quant_expert_filtered": act_quant_ep_arms(ops, dev, stream, flush),
             "route_prepare_us": route_prep_arms(ops, dev, stream, flush),
+            "tiny": layer_arm(ops, dev, stream, flush, wl.CONFIGS["tiny"], 0, hbm_peak, fp8_peak, steps=50,
+                              warmup=5, clamp=7.0, fmt=1),
             "expert_parallel": layer_arm(ops, dev, stream, flush, dict(wl.CONFIGS["ep"], M=1024), 2, hbm_peak,
                                          fp8_peak, clamp=7.0, fmt=1),
+            "expert_parallel_tokens": {str(T): layer_arm(ops, dev, stream, flush, dict(wl.CONFIGS["ep"], M=T), 2,
+                                                         hbm_peak, fp8_peak, steps=50, warmup=5, clamp=7.0, fmt=1)
+                                       for T in wl.EP_TOKENS},
             "prefill": layer_arm(ops, dev, stream, flush, wl.CONFIGS["prefill"], 3, hbm_peak, fp8_peak),
             "fp8_peak_source": "measured bf16 GEMM peak x 2 (nominal fp8/bf16 ratio)" if "bf16_tflops" in peaks
                               else "fallback bf16 1.9 PFLOP/s x 2",
@@ -371,7 +386,8 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(M, ids_host[0], xs[0], wgu_q, wgu_s, wd_q, wd_s, H, N, E, k)
+        host = oracle_layer(M, ids_host[0], ws[0].cpu().numpy(), xs[0], wgu_q, wgu_s, wd_q, wd_s, H, N, E, k)
+        cpu = cpu_baseline(host, M)
 
     route_launches = 1 if M * k <= 2048 else 2
     launches_per_step = route_launches + (1 if path == ops.FORWARD_FUSED else 5)
@@ -395,11 +411,10 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic (seeded; random weights, uniform random routing)",
-        "config": {"workload": f"decode MoE layer M={M} H={H} N={N} E={E} top-k={k}, block-FP8 128x128",
-                   "M": M, "H": H, "N": N, "E": E, "topk": k, "block_m": bm, "path": path_name,
-                   "weights": args.weights,
-                   "l2": "256 MiB buffer written then read back between timed steps (outside the events); 8 rotating routing batches",
-                   "timing": "CUDA graph replay per step, CUDA events per step", "parallelism": f"replicas x{world}"},
+        "config": workload_config(M, args.seed),
+        "setup": {"block_m": bm, "path": path_name, "weight_layout": args.weights,
+                  "l2": "256 MiB buffer written then read back between timed steps (outside the events); 8 rotating routing batches",
+                  "timing": "CUDA graph replay per step, CUDA events per step", "parallelism": f"replicas x{world}"},
         "layer_hbm": {"GBps": round(achieved, 1), "frac": round(achieved / hbm_peak, 4),
                       "active_bytes": int(mean_bytes), "peak": hbm_peak, "peak_source": peak_src,
                       "us_median": round(statistics.median(step_ms) * 1e3, 2),
@@ -545,6 +560,41 @@ def act_quant_arms(ops, dev, stream, flush, steps=50, warmup=5):
     return out
 
 
+def act_quant_ep_arms(ops, dev, stream, flush, steps=50, warmup=5):
+    """The expert-filtered act-quant sweep (vLLM PR #53875, "Kernel microbenchmarks": top-k 6,
+    width 2048, 32 of 256 experts local, the filter in both arms): routed rows 6T for T in
+    {1, 10, 100, 1024}, clamp +-7, UE8M0 scales.  Fused: one silu_mul_quant_fp8 that skips the
+    non-local rows.  Two kernels: silu_and_mul_bf16 (same filter, BF16 written) then the
+    identity quantisation (same filter)."""
+    import torch
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    E, k, El, n = 256, 6, 32, 2048
+    emap = torch.from_numpy(wl.expert_map_random(E, El, 4242)).to(dev)
+    out = {}
+    for T in wl.EP_TOKENS:
+        rows = k * T
+        ids, _ = wl.routing_topk(T, E, k, seed=51 + T, kind="uniform")
+        re = torch.from_numpy(ids.reshape(-1)).to(dev)
+        x = torch.from_numpy(wl.act_rows(rows, 2 * n, 1.0, 61 + T).view(np.int16)).view(torch.bfloat16).to(dev)
+        q = torch.zeros((rows, n), dtype=torch.uint8, device=dev)
+        sc = torch.zeros((rows, n // 128), dtype=torch.float32, device=dev)
+        mid = torch.zeros((rows, n), dtype=torch.bfloat16, device=dev)
+        kept = int((emap[re.long()] >= 0).sum().item())
+        fused = lambda i: ops.silu_mul_quant_fp8(1, x, n, clamp_limit=7.0, fmt=ops.SCALE_UE8M0, row_expert=re,
+                                                expert_map=emap, E=E, out_q=q, out_s=sc, stream=stream)
+
+        def separate(i):
+            ops.silu_and_mul_bf16(1, x, n, clamp_limit=7.0, row_expert=re, expert_map=emap, E=E, out=mid,
+                                  stream=stream)
+            ops.silu_mul_quant_fp8(0, mid, n, fmt=ops.SCALE_UE8M0, row_expert=re, expert_map=emap, E=E,
+                                   out_q=q, out_s=sc, stream=stream)
+        tf = statistics.mean(time_events(fused, steps, warmup, flush, stream)) * 1e3
+        ts = statistics.mean(time_events(separate, steps, warmup, flush, stream)) * 1e3
+        out[str(rows)] = {"tokens": T, "kept_rows": kept, "fused_us": round(tf, 2), "separate_us": round(ts, 2),
+                          "speedup": round(ts / tf, 2)}
+    return out
+
+
 def route_prep_arms(ops, dev, stream, flush, steps=50, warmup=5):
     """Route preparation alone: 512 routes over 256 experts (single CTA), and 2048 and 4096 (the
     prefill's) routes over 512 experts on both paths."""
@@ -642,22 +692,17 @@ def layer_arm(ops, dev, stream, flush, cfg, seed, hbm_peak, fp8_peak_tflops, ste
 
 
 def padded_grid_route(route, E, bm, dev):
-    """The schedule before active-expert dispatch: one block per expert, every expert's weights
-    streamed whether or not it received routes (lmdeploy PR #4956, "Motivation").  Built from
-    the compact route table with torch ops at setup time."""
+    """The schedule before active-expert dispatch: every expert owns a block, so every expert's
+    weights are streamed whether or not it received routes (lmdeploy PR #4956, "Motivation");
+    the route table comes from workloads.padded_grid_route, the builder the GEMM parity tests
+    check, at setup time."""
     import torch
-    si = route["sorted_idx"].cpu()
-    be = route["block_expert"].cpu()
-    nb = int(route["num_blocks"].item())
-    assert nb <= E, "padded-grid arm assumes at most block_m routes per expert"
-    B_cap = E
-    sorted_idx = torch.full((B_cap * bm,), -1, dtype=torch.int32)
-    for b in range(nb):
-        e = int(be[b])
-        sorted_idx[e * bm:(e + 1) * bm] = si[b * bm:(b + 1) * bm]
-    return dict(sorted_idx=sorted_idx.to(dev), block_expert=torch.arange(E, dtype=torch.int32, device=dev),
-                num_blocks=torch.tensor([E], dtype=torch.int32, device=dev), B_cap=B_cap,
-                route_slot=None, moved=True)
+    from block_fp8_mixture_moe_gb300 import workloads as wl
+    pg = wl.padded_grid_route(route["sorted_idx"].cpu().numpy(), route["block_expert"].cpu().numpy(),
+                              int(route["num_blocks"].item()), E, bm)
+    return dict(sorted_idx=torch.from_numpy(pg["sorted_idx"]).to(dev),
+                block_expert=torch.from_numpy(pg["block_expert"]).to(dev),
+                num_blocks=torch.tensor([pg["num_blocks"]], dtype=torch.int32, device=dev), B_cap=pg["B_cap"])
 
 
 def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, M, H, N,
@@ -678,12 +723,13 @@ def time_gate_up_kernel(ops, dev, stream, flush, xs, ids, ws, wgu_q, wgu_s, M, H
             routes.append(route)
         torch.cuda.synchronize()
     if padded:
-        # the padded grid reads activations from slot e*bm + i: scatter the quantised rows there
-        slots_p = E * bm
+        # the padded grid reads activations from its own slots (the values do not change the
+        # time: the same bytes are read)
+        proutes = [padded_grid_route(rt, E, bm, dev) for rt in routes]
+        slots_p = max(pr["B_cap"] for pr in proutes) * bm
         xq_p = torch.zeros((max(slots, slots_p), H), dtype=torch.uint8, device=dev)
         xs_p = torch.ones((max(slots, slots_p), H // 128), dtype=torch.float32, device=dev)
         gu_p = torch.empty((splits, max(slots, slots_p), 2 * N), dtype=torch.float32, device=dev)
-        proutes = [padded_grid_route(rt, E, bm, dev) for rt in routes]
     times = []
     with torch.cuda.stream(stream):
         for i in range(warmup + steps):
@@ -815,37 +861,54 @@ def recorded_traffic(path):
         return None
 
 
-def cpu_baseline(M, ids0, x0, wgu_q, wgu_s, wd_q, wd_s, H, N, E, k, sample_tokens=4):
-    """The oracle's sparse layer on a 4-token sample of the first routing batch (weights of the
-    sample's experts copied to the host), timed on all host cores and scaled to M tokens."""
-    import torch
-    import oracle
+def oracle_layer(M, ids0, w0, x0, wgu_q, wgu_s, wd_q, wd_s, H, N, E, k):
+    """Host (numpy) copy of routing batch 0's whole layer for the oracle: the batch's routing,
+    weights and activations, and the weights of its active experts (the same bytes the library
+    reads; the other experts are zero, and no route reaches them)."""
     from block_fp8_mixture_moe_gb300 import workloads as wl
-    toks = list(range(min(sample_tokens, M)))
-    used = np.unique(ids0[toks])
-    layer = dict(x=x0.view(torch.int16).cpu().numpy().view(np.uint16), topk_ids=ids0,
-                 topk_w=np.full(ids0.shape, 1.0 / k, np.float32), expert_map=None,
-                 wgu_q=wgu_q, wgu_s=wgu_s, wd_q=wd_q, wd_s=wd_s, E=E, M=M, H=H, N=N, k=k)
-    host = wl.layer_numpy(layer, experts=used)
-    threads = oracle.set_threads(0)
-    oracle.moe_forward(host, tokens=toks)  # warm (page-in)
+    import torch
+    layer = dict(x=x0.view(torch.int16).cpu().numpy().view(np.uint16), topk_ids=ids0, topk_w=w0,
+                 expert_map=None, wgu_q=wgu_q, wgu_s=wgu_s, wd_q=wd_q, wd_s=wd_s, E=E, M=M, H=H, N=N, k=k)
+    return wl.layer_numpy(layer, experts=np.unique(ids0))
+
+
+def time_oracle(host, threads, min_runs, budget_s):
+    """Median wall time (us) of the oracle's whole layer with `threads` OpenMP threads (0 = all
+    host cores), at least min_runs runs and at most about budget_s seconds; returns (us, runs,
+    threads used)."""
+    import oracle
+    used = oracle.set_threads(threads)
     runs = []
-    t_end = time.time() + 10.0
-    while time.time() < t_end or len(runs) < 3:
+    t_end = time.time() + budget_s
+    while len(runs) < min_runs or (time.time() < t_end and len(runs) < 20):
         t0 = time.perf_counter()
-        oracle.moe_forward(host, tokens=toks)
+        oracle.moe_forward(host)
         runs.append(time.perf_counter() - t0)
-        if len(runs) >= 50:
-            break
-    per_layer_us = statistics.median(runs) * (M / len(toks)) * 1e6
-    return {"value": round(per_layer_us, 1), "unit": "us", "cores": threads, "kind": "oracle",
-            "sample": f"{len(toks)} of {M} tokens (their {len(used)} experts), median of {len(runs)} runs, scaled x{M / len(toks):g}"}
+    oracle.set_threads(0)
+    return statistics.median(runs) * 1e6, len(runs), used
+
+
+def cpu_baseline(host, M):
+    """The oracle's whole layer (all M tokens of routing batch 0, the bench's own inputs) on the
+    host cores: all cores, and one thread."""
+    import oracle
+    oracle.build()
+    oracle.moe_forward(host)  # warm (page-in)
+    us_all, n_all, threads = time_oracle(host, 0, 3, 8.0)
+    us_one, n_one, _ = time_oracle(host, 1, 1, 4.0)
+    return {"value": round(us_all, 1), "unit": "us", "cores": threads, "kind": "oracle",
+            "sample": f"the whole layer (all {M} tokens of routing batch 0, the timed inputs), median of {n_all} runs on {threads} threads",
+            "single_thread": {"value": round(us_one, 1), "unit": "us", "cores": 1, "runs": n_one}}
 
 
 # ---------------------------------------------------------------------------------------------
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------------------------
 def run_reference(args):
+    """The CPU oracle on the library arm's own workload: the same seeds give the same routing,
+    activations and weights (generated with torch's CUDA generator when a GPU is present, as the
+    library arm does; only input generation touches the GPU), and each step is one whole layer
+    of routing batch 0 on all host cores."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -856,36 +919,32 @@ def run_reference(args):
     oracle.build()
     H, N, E, k = DECODE["H"], DECODE["N"], DECODE["E"], DECODE["k"]
     M = args.M
-    ids, w = wl.routing_topk(M, E, k, seed=args.seed * 1000, kind="uniform")
-    x = wl.bf16_normal((M, H), 1.0, args.seed * 1000 + 500).view(torch.int16).numpy().view(np.uint16)
-    # one token per step; only the experts of the sampled tokens need weights on the host
-    sample = list(range(min(M, 4)))
-    used = np.unique(ids[sample])
-    remap = {int(g): i for i, g in enumerate(used)}
-    ids_s = np.array([[remap.get(int(g), -1) for g in row] for row in ids], np.int32)
-    wgu_q, wgu_s = wl.quantized_weights(len(used), 2 * N, H, seed=5)
-    wd_q, wd_s = wl.quantized_weights(len(used), H, N, seed=6)
-    layer = dict(x=x, topk_ids=ids_s, topk_w=w, expert_map=None, wgu_q=wgu_q.numpy(),
-                 wgu_s=wgu_s.numpy(), wd_q=wd_q.numpy(), wd_s=wd_s.numpy(), E=len(used), M=M,
-                 H=H, N=N, k=k)
+    gen_dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    wgu_q, wgu_s = wl.quantized_weights(E, 2 * N, H, seed=args.seed * 7919 + 5, device=gen_dev)
+    wd_q, wd_s = wl.quantized_weights(E, H, N, seed=args.seed * 7919 + 6, device=gen_dev)
+    ids0, w0 = wl.routing_topk(M, E, k, seed=args.seed * 1000, kind="uniform")
+    x0 = wl.bf16_normal((M, H), 1.0, args.seed * 1000 + 500)
+    host = oracle_layer(M, ids0, w0, x0, wgu_q, wgu_s, wd_q, wd_s, H, N, E, k)
+    del wgu_q, wgu_s, wd_q, wd_s
     threads = oracle.set_threads(0)
-    for i in range(args.warmup):
-        oracle.moe_forward(layer, tokens=[sample[i % len(sample)]])
+    for _ in range(args.warmup):
+        oracle.moe_forward(host)
     t = []
-    for i in range(args.steps):
+    for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.moe_forward(layer, tokens=[sample[i % len(sample)]])
+        oracle.moe_forward(host)
         t.append(time.perf_counter() - t0)
-    per_layer_us = statistics.mean(t) * M * 1e6
+    per_layer_us = statistics.mean(t) * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": round(per_layer_us, 1), "unit": "us",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(statistics.mean(t) * 1e3, 4), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": f"decode MoE layer M={M} H={H} N={N} E={E} top-k={k}, block-FP8 128x128",
-                   "M": M, "H": H, "N": N, "E": E, "topk": k},
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded; random weights, uniform random routing)",
+        "config": workload_config(M, args.seed),
         "cpu_baseline": {"value": round(per_layer_us, 1), "unit": "us", "kind": "oracle", "cores": threads,
-                         "sample": f"1 token per step (of {M}), scaled x{M}"},
+                         "sample": f"the whole layer (all {M} tokens of routing batch 0) per step, "
+                                   f"inputs generated on {gen_dev.type}"},
         "e2e": {"value": round(per_layer_us, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

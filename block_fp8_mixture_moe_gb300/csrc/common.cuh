@@ -328,18 +328,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after ~2 s (global timer) or as soon as another role of the CTA has
-// given up (*abort != 0); on a timeout it records MOE_DEV_TIMEOUT in the status word.
+// Bounded wait: gives up after `limit` ns (global timer; ~2 s by default) or as soon as another
+// role of the CTA has given up (*abort != 0); on a timeout it records MOE_DEV_TIMEOUT in the
+// status word.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                       int* status) {
+                                       int* status, uint64_t limit = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit) {
                 if (status) atomicOr(status, MOE_DEV_TIMEOUT);
                 *abort = 1;
                 return false;

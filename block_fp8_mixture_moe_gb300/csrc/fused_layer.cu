@@ -79,6 +79,10 @@ struct FusedArgs {
     unsigned* blk_ready;  // [B_cap] act-quant items (slot, group) done per block, pads included
     unsigned* ready_list; // [B_cap] 1 + block id, in the order the blocks became ready
     int* status;
+    // limit of the counter waits (ns), and a test hook: block stall_block's act-quant items wait
+    // for one gate/up piece more than exist, so that wait can only run out (-1: none)
+    unsigned long long wait_limit_ns;
+    int stall_block;
 };
 
 template <int BM>
@@ -140,9 +144,9 @@ __device__ __forceinline__ void epi_sync() {
     asm volatile("barrier.sync %0, 128;" ::"n"(kEpiBar) : "memory");
 }
 
-// Waits (bounded, like mbar_wait) until the counter reaches `target`.
+// Waits (bounded, like mbar_wait, after `limit` ns) until the counter reaches `target`.
 __device__ __noinline__ bool wait_counter(const unsigned* ctr, unsigned target, volatile int* abort,
-                                          int* status) {
+                                          int* status, unsigned long long limit) {
     if (ld_acquire_gpu(ctr) >= target) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
@@ -150,7 +154,7 @@ __device__ __noinline__ bool wait_counter(const unsigned* ctr, unsigned target, 
         if (ld_acquire_gpu(ctr) >= target) return true;
         if ((i & 15u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit) {
                 if (status) atomicOr(status, MOE_DEV_TIMEOUT);
                 *abort = 1;
                 return false;
@@ -164,12 +168,13 @@ __device__ __noinline__ bool wait_counter(const unsigned* ctr, unsigned target, 
 // same; the second named barrier releases the group.  Every epilogue thread executes both
 // barriers, also after an abort, so the group never waits on a thread that left.
 __device__ __forceinline__ void epi_phase_barrier(unsigned* ctr, unsigned G, int etid,
-                                                  volatile int* abort, int* status) {
+                                                  volatile int* abort, int* status,
+                                                  unsigned long long limit) {
     epi_sync();
     if (etid == 0 && !*abort) {
         __threadfence();
         atomicAdd(ctr, 1u);
-        wait_counter(ctr, G, abort, status);
+        wait_counter(ctr, G, abort, status, limit);
     }
     epi_sync();
 }
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(256, 1)
                     bool late = false;
                     while (static_cast<long long>(*w_taken) + kAhead < base_desc) {
                         if (*abort_flag) { late = true; break; }
-                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        if (globaltimer_ns() - t0 > p.wait_limit_ns) {
                             if (lane == 0) {
                                 if (p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
                                 *abort_flag = 1;
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(256, 1)
                         bool okw = true;
                         unsigned v = 0;
                         if (lane == 0) {
-                            okw = wait_counter(p.ready_list + bi, 1u, abort_flag, p.status);
+                            okw = wait_counter(p.ready_list + bi, 1u, abort_flag, p.status, p.wait_limit_ns);
                             v = ld_acquire_gpu(p.ready_list + bi);
                         }
                         okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(256, 1)
             int ready_b = -1;
             if (!wprod) {
                 // the quantised input rows of every CTA must be in memory before they are read
-                ok = wait_counter(p.sync + 0, G, abort_flag, p.status);
+                ok = wait_counter(p.sync + 0, G, abort_flag, p.status, p.wait_limit_ns);
                 fence_proxy_async_global();
             }
             while (ok) {
@@ -521,12 +526,16 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
             if (*abort_flag) {
-                // never leave a TMA write in flight: wait (bounded) for the last load of every stage
+                // never leave a TMA write in flight: wait (bounded) for the last load of every
+                // stage.  A stage completes only when both producers have arrived, and the other
+                // producer may have left on the abort first; its own loads land within
+                // microseconds, so the kernel's wait limit bounds this wait
                 for (int i = 0; i < C::kStages; ++i) {
                     if (issued <= i) break;
                     const long long n_i = (issued - 1 - i) / C::kStages + 1;
                     volatile int no_abort = 0;
-                    mbar_wait(full + i, static_cast<uint32_t>((n_i - 1) & 1), &no_abort, p.status);
+                    mbar_wait(full + i, static_cast<uint32_t>((n_i - 1) & 1), &no_abort, p.status,
+                              p.wait_limit_ns);
                 }
             }
         }
@@ -570,7 +579,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             mma_commit(mma_done);
             volatile int no_abort = 0;
-            mbar_wait(mma_done, 0, &no_abort, p.status);
+            mbar_wait(mma_done, 0, &no_abort, p.status, p.wait_limit_ns);
         }
     } else {
         // ---------------- epilogue group (warps 2..5) ----------------
@@ -653,7 +662,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             fence_proxy_async_global();  // the quantised rows are read by TMA
         }
-        epi_phase_barrier(p.sync + 0, G, etid, abort_flag, p.status);
+        epi_phase_barrier(p.sync + 0, G, etid, abort_flag, p.status, p.wait_limit_ns);
 
         int ts = 0, slot = 0;
         uint32_t tph = 0, dph = 0;
@@ -829,13 +838,14 @@ __global__ void __launch_bounds__(256, 1)
                     const int b = m / BM;
                     {
                         // wait (bounded, the whole warp) until every active item's block is stored
-                        const unsigned tgt = active ? 4u * block_pieces(b, p.NT1, p.KB1, W1, G1) : 0u;
+                        const unsigned tgt = active ? 4u * block_pieces(b, p.NT1, p.KB1, W1, G1) +
+                                                          (b == p.stall_block ? 1u : 0u) : 0u;
                         const uint64_t t0 = globaltimer_ns();
                         for (;;) {
                             const bool rdy = !active || ld_acquire_gpu(p.blk_done + b) >= tgt;
                             if (__all_sync(0xFFFFFFFFu, rdy)) break;
                             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
-                            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            if (globaltimer_ns() - t0 > p.wait_limit_ns) {
                                 if (lane == 0) {
                                     if (p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
                                     *abort_flag = 1;
@@ -982,7 +992,8 @@ __global__ void __launch_bounds__(256, 1)
     long long it4 = lo4 + threadIdx.x;
     if (it4 < hi4) load_routes(static_cast<int>(it4 / C8), 0);
     if (warp >= 2 && warp <= 5)
-        epi_phase_barrier(p.sync + 3, G, static_cast<int>(threadIdx.x) - 64, abort_flag, p.status);
+        epi_phase_barrier(p.sync + 3, G, static_cast<int>(threadIdx.x) - 64, abort_flag, p.status,
+                          p.wait_limit_ns);
     __syncthreads();  // every role is done; the epilogue group has passed the last counter
     if (!*abort_flag) {
         bool first = true;
@@ -1062,6 +1073,21 @@ size_t fused_partial_bytes(int B_cap, int bm, int H, int N, int G) {
 // list per block.
 int fused_counter_words(int B_cap) { return 4 + 3 * B_cap; }
 
+namespace {
+// Test hook (moe_debug_inject_stall): one-shot settings for the calling thread's next launch.
+thread_local int t_stall_block = -1;
+thread_local unsigned long long t_stall_limit_ns = 0;
+
+void take_stall_injection(int* block, unsigned long long* limit_ns) {
+    if (t_stall_limit_ns) {
+        *block = t_stall_block;
+        *limit_ns = t_stall_limit_ns;
+    }
+    t_stall_block = -1;
+    t_stall_limit_ns = 0;
+}
+}  // namespace
+
 int launch_fused_layer(const FusedLaunch& f, cudaStream_t stream) {
     const int bm = f.bm;
     const int G = sm_count();
@@ -1093,6 +1119,9 @@ int launch_fused_layer(const FusedLaunch& f, cudaStream_t stream) {
     a.sync = f.sync; a.blk_done = f.sync + 4; a.blk_ready = f.sync + 4 + f.B_cap;
     a.ready_list = f.sync + 4 + 2 * f.B_cap;
     a.status = device_status_ptr();
+    a.wait_limit_ns = kWaitLimitNs;
+    a.stall_block = -1;
+    take_stall_injection(&a.stall_block, &a.wait_limit_ns);
     const void* fn;
     int smem;
     switch (bm) {
@@ -1115,3 +1144,15 @@ int launch_fused_layer(const FusedLaunch& f, cudaStream_t stream) {
 }
 
 }  // namespace moe
+
+extern "C" int moe_debug_inject_stall(int block, unsigned long long wait_limit_ns) {
+    moe::clear_error();
+    if (block < 0 || wait_limit_ns == 0 || wait_limit_ns > moe::kWaitLimitNs) {
+        moe::set_error("moe_debug_inject_stall: need block >= 0 and 0 < wait_limit_ns <= %llu",
+                       static_cast<unsigned long long>(moe::kWaitLimitNs));
+        return MOE_ERR_ARG;
+    }
+    moe::t_stall_block = block;
+    moe::t_stall_limit_ns = wait_limit_ns;
+    return MOE_OK;
+}

@@ -54,6 +54,7 @@ SIGNATURES = {
     "moe_get_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "moe_device_supported": (_I, []),
     "moe_kernel_binary_version": (_I, []),
+    "moe_debug_inject_stall": (_I, [_I, ctypes.c_ulonglong]),
     "moe_pointer_device_accessible": (_I, [_P]),
 }
 
@@ -313,6 +314,12 @@ def moe_blockfp8_workspace_layout(M, k, E, E_local, H, N, block_m=0) -> dict:
     _check(load().moe_blockfp8_workspace_layout(M, k, E, E_local, H, N, block_m, offs),
            "moe_blockfp8_workspace_layout")
     return {name: int(offs[i]) for i, name in enumerate(WS_REGIONS)}
+
+
+def moe_debug_inject_stall(block: int, wait_limit_ns: int) -> None:
+    """Test hook: the calling thread's next path-FUSED forward waits for block `block` until
+    wait_limit_ns runs out (see include/moefp8.h)."""
+    _check(load().moe_debug_inject_stall(block, wait_limit_ns), "moe_debug_inject_stall")
 
 
 def moe_kernel_binary_version() -> int:

@@ -333,6 +333,16 @@ MOEFP8_API const char* moe_last_error_string(void);
 MOEFP8_API int moe_get_device_status(int* status, int reset);
 /* 1 if the current device is an sm_103 GPU the library was built for, else 0. */
 MOEFP8_API int moe_device_supported(void);
+/* Test hook for the bounded waits (no counterpart in the pages).  The next path-FUSED forward
+ * launched from the calling thread treats block `block` of the layer as one gate/up piece
+ * short, so the activation step's wait for that block can never complete, and uses
+ * wait_limit_ns (at most the default 2 s) as the limit of its counter waits.  Every index and
+ * address stays valid: the wait runs out, MOE_DEV_TIMEOUT is set in the device status word,
+ * the kernel drains its copies and tensor-core work, frees its tensor memory and returns, and
+ * the output of that call is undefined.  The setting applies to one launch and is then
+ * cleared.  Returns MOE_OK, or MOE_ERR_ARG for block < 0 or a limit outside (0, 2 s]. */
+MOEFP8_API int moe_debug_inject_stall(int block, unsigned long long wait_limit_ns);
+
 /* The binary architecture version of the library's kernels as the CUDA runtime reports it for
  * the current device (cudaFuncGetAttributes binaryVersion, 103 for sm_103a code), or -1 when
  * it cannot be queried (no device). */
