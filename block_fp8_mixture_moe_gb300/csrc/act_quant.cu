@@ -44,6 +44,7 @@ struct AQArgs {
     float* out_s;
     int in_splits;
     int map_early;  // row_map was written two or more launches back: read it before the wait
+    int map_smem;   // stage expert_map ([E] ints) in shared memory (persistent launches)
     // slot rows: row w is produced iff slot_route[w] >= 0 (input and output row w), and only
     // rows below n_blocks[0] * bm exist (n_blocks read on the device)
     const int32_t* slot_route;
@@ -147,18 +148,20 @@ __device__ __forceinline__ void load_gate_up(const AQArgs& p, long long off_g, l
     for (int i = 0; i < 8; ++i) { g[i] = bf16_round_f32(g[i]); u[i] = bf16_round_f32(u[i]); }
 }
 
-// Decides whether work row `w` is produced, and its input and output rows.
+// Decides whether work row `w` is produced, and its input and output rows.  `pre` is the row's
+// entry of its first selector (row_expert if given, else row_map) when it was loaded ahead
+// (-2: not loaded); smap is the expert map staged in shared memory (or null).
 __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, int* out_row,
-                                           int pre_m = -2) {
+                                           int pre = -2, const int* smap = nullptr) {
     int src = w, dst = w;
     if (p.slot_route && __ldcg(p.slot_route + w) < 0) return false;
     if (p.row_expert) {
-        int id = __ldg(p.row_expert + w);
+        const int id = pre != -2 ? pre : __ldg(p.row_expert + w);
         if (id < 0 || id >= p.E) return false;
-        if (p.expert_map && __ldg(p.expert_map + id) < 0) return false;
+        if (p.expert_map && (smap ? smap[id] : __ldg(p.expert_map + id)) < 0) return false;
     }
     if (p.row_map) {
-        int m = pre_m != -2 ? pre_m : __ldg(p.row_map + w);
+        const int m = (pre != -2 && !p.row_expert) ? pre : __ldg(p.row_map + w);
         if (m < 0) return false;
         dst = m;
         src = p.row_div > 0 ? w / p.row_div : m;
@@ -173,7 +176,8 @@ __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, 
 }
 
 template <int ACT, bool F32IN, int KG, bool INL>
-__device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int lane, int pre_m = -2) {
+__device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int lane, int pre = -2,
+                                           const int* smap = nullptr) {
     const int half = lane >> 4, l = lane & 15;
     const long long item = pair * 2 + half;
     bool active = item < static_cast<long long>(p.rows) * p.G;
@@ -194,7 +198,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
                 route = __ldcg(p.slot_route + w);
             }
         } else {
-            active = row_source(p, w, &in_row, &row, pre_m);
+            active = row_source(p, w, &in_row, &row, pre, smap);
         }
     }
     float a[8];
@@ -236,6 +240,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
 
 template <int ACT, bool F32IN, bool PERSISTENT, int KG, bool INL>
 __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
+    extern __shared__ int aq_smap[];  // the expert map, when p.map_smem
     const int lane = threadIdx.x & 31;
     const long long warps_per_block = blockDim.x >> 5;
     if (p.n_blocks) {
@@ -246,32 +251,39 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     }
     const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
     long long pair = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
-    // the first pair's row map entry, when it was written two or more launches back
-    int pre_m = -2;
-    if (p.map_early && p.row_map && !p.row_expert && pair < pairs) {
-        const long long item = pair * 2 + (lane >> 4);
-        if (item < static_cast<long long>(p.rows) * p.G) pre_m = __ldcg(p.row_map + item / p.G);
+    // a row's first selector: its expert id (a caller input) or its row-map entry
+    const int32_t* sel = p.row_expert ? p.row_expert : p.row_map;
+    const long long items = static_cast<long long>(p.rows) * p.G;
+    auto sel_of = [&](long long pr) -> int {
+        const long long item = pr * 2 + (lane >> 4);
+        return (pr < pairs && item < items) ? __ldcg(sel + item / p.G) : -1;
+    };
+    // the first pair's selector before the wait, when it is an input or was written two or
+    // more launches back; with an expert filter the (caller's) expert map is staged in shared
+    // memory, so a row's filter costs one global load
+    int pre = -2;
+    if (sel && (p.row_expert || p.map_early) && pair < pairs) pre = sel_of(pair);
+    const int* smap = nullptr;
+    if (PERSISTENT && p.map_smem) {
+        for (int i = threadIdx.x; i < p.E; i += blockDim.x) aq_smap[i] = __ldg(p.expert_map + i);
+        __syncthreads();
+        smap = aq_smap;
     }
     grid_dep_wait();
     grid_dep_launch();
     if (!PERSISTENT) {
-        if (pair < pairs) quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, pre_m);
+        if (pair < pairs) quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, pre);
         return;
     }
     const long long stride = static_cast<long long>(gridDim.x) * warps_per_block;
-    // with a row map, each pair's map entry is loaded one pair ahead, so a pair whose route is
-    // dropped (most of them at expert-parallel shapes) costs no round trip of its own
-    const bool ahead = p.row_map && !p.row_expert;
-    const long long items = static_cast<long long>(p.rows) * p.G;
-    auto map_of = [&](long long pr) -> int {
-        const long long item = pr * 2 + (lane >> 4);
-        return (pr < pairs && item < items) ? __ldcg(p.row_map + item / p.G) : -1;
-    };
-    int cur = pre_m;
-    if (ahead && cur == -2) cur = map_of(pair);
+    // each pair's selector is loaded one pair ahead, so a pair whose row is dropped (most of
+    // them at expert-parallel shapes) costs no round trip of its own
+    const bool ahead = sel != nullptr;
+    int cur = pre;
+    if (ahead && cur == -2) cur = sel_of(pair);
     for (; pair < pairs; pair += stride) {
-        const int nxt = ahead ? map_of(pair + stride) : -2;
-        quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, ahead ? cur : -2);
+        const int nxt = ahead ? sel_of(pair + stride) : -2;
+        quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, ahead ? cur : -2, smap);
         cur = nxt;
     }
 }
@@ -382,17 +394,18 @@ template <int ACT, bool F32IN, int KG, bool INL>
 int launch_aq_grid(const AQArgs& p, long long pairs, bool persistent, bool pdl, cudaStream_t stream) {
     const int threads = 256, wpb = threads / 32;
     long long blocks = (pairs + wpb - 1) / wpb;
+    const size_t smem = persistent && p.map_smem ? static_cast<size_t>(p.E) * 4 : 0;
     if (persistent) {
         // as many CTAs as are resident at once, so the grid runs in one wave
         int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_act_quant<ACT, F32IN, true, KG, INL>, threads, 0) !=
-                cudaSuccess || occ < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_act_quant<ACT, F32IN, true, KG, INL>, threads,
+                                                          smem) != cudaSuccess || occ < 1)
             occ = 1;
         long long cap = static_cast<long long>(sm_count()) * occ;
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7FFFFFFFLL) { set_error("act_quant: too many groups"); return MOE_ERR_ARG; }
-    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, pdl);
+    Launch L(dim3(static_cast<unsigned>(blocks)), dim3(threads), smem, stream, pdl);
     cudaError_t e = persistent ? cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, true, KG, INL>, p)
                                : cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, false, KG, INL>, p);
     if (e != cudaSuccess) {
@@ -483,6 +496,8 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
     p.out_q = out_q;
     p.out_s = out_s;
     p.map_early = map_early ? 1 : 0;
+    // an expert filter's map, staged in shared memory by persistent launches (up to 8192 ids)
+    p.map_smem = (row_expert && expert_map && E <= 8192) ? 1 : 0;
     if (n_blocks && (!slot_route || bm <= 0 || row_map)) {
         set_error("silu_mul_quant_fp8: slot rows need slot_route, bm > 0 and no row map");
         return MOE_ERR_ARG;

@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     uint64_t* mma_done = dsa + C::kRing;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // set by an epilogue thread once its wait for the previous launch has returned
+    volatile int* dep_seen = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -176,6 +178,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
+        *dep_seen = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -476,11 +479,12 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                             load_a(s, kb, nk, b);
                         } else {
                             pend_s[npend] = s; pend_kb[npend] = kb; pend_nk[npend] = nk; pend_b[npend] = b;
-                            // wait when every stage holds weights -- or, self-routing, after the
-                            // first: the launch began only shortly before its predecessor ends, so
-                            // the wait is short, and the first stages' activation tiles then do
-                            // not queue behind all the other stages' weight tiles
-                            if (++npend == (self_route ? 1 : C::kStages)) resolve();
+                            // the wait blocks this thread, so it waits only when every stage
+                            // holds weights -- or as soon as the previous launch is known to be
+                            // done (an epilogue thread has passed its own wait), so that the
+                            // pending activation tiles go out at once instead of queueing behind
+                            // the weight tiles of every remaining stage
+                            if (++npend == C::kStages || *dep_seen) resolve();
                         }
                         ++issued;
                         if (++s == C::kStages) { s = 0; ph ^= 1u; }
@@ -566,6 +570,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < C::kCpw; ++j) acc[j] = 0.0f;
         grid_dep_wait();  // (returns at once: the activations it consumes come after it)
+        if (warp == 2 && lane == 0) *dep_seen = 1;
         if (self_route) grid_dep_launch();
         for (;;) {
             bool ok = mbar_wait_fast(dsa + slot, dph, abort_flag, p.status);
