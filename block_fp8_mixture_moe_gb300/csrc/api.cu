@@ -151,7 +151,7 @@ int gate_up_splits(int M, int k, int E, int E_local, int H, int N, int bm, int s
 struct Plan {
     int bm, B_cap, slots, R, splits;
     size_t off_sorted, off_bexp, off_nb, off_cnt, off_off, off_rslot, off_rws, off_xq, off_xs,
-        off_gu, off_aq, off_as, off_z, off_sync, total;
+        off_gu, off_aq, off_as, off_z, off_sync, off_rcnt, total;
 };
 
 Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int sms) {
@@ -178,12 +178,15 @@ Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int 
     P.off_as = take(sizeof(float) * static_cast<size_t>(P.slots) * (N / 128));
     P.off_z = take(sizeof(uint16_t) * static_cast<size_t>(P.R) * H);
     P.off_sync = take(sizeof(unsigned) * static_cast<size_t>(fused_counter_words(P.B_cap)));
+    P.off_rcnt = take(sizeof(unsigned) * static_cast<size_t>(M) * (H / 128));  // epilogue-reduce counters
     P.total = o;
     return P;
 }
 
 // AUTO forward path: the one measured faster on GB300 for the shape (graph-replayed layer on
-// the decode shapes M = 1..256): the staged launches at every measured size.
+// the decode shapes M = 1..256 and the expert-parallel shape): the staged launches at every
+// measured size.  The fused persistent kernel and the reduce in the down GEMM's epilogue were
+// slower everywhere (e.g. M = 32: 177 and 250 us against 162 us staged).
 moe_forward_path auto_path(int M, int k, int E, int E_local, int H, int N) {
     (void)M; (void)E; (void)E_local; (void)H; (void)N;
     // top-k above the separate reduce kernel's limit: only the fused path takes it
@@ -275,7 +278,7 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     // the staged path's separate reduce kernel takes at most kReduceMaxTopk routes per token;
     // AUTO sends larger top-k to the fused path (no limit), an explicit STAGED is refused here,
     // before anything is enqueued
-    if (k > kReduceMaxTopk && path == MOE_FORWARD_STAGED) {
+    if (k > kReduceMaxTopk && (path == MOE_FORWARD_STAGED || path == MOE_FORWARD_STAGED_EPILOGUE_REDUCE)) {
         set_error("moe_blockfp8_forward: the staged path takes top-k <= %d (got %d); use FUSED or AUTO",
                   kReduceMaxTopk, k);
         return MOE_ERR_ARG;
@@ -288,7 +291,8 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
         set_error("moe_blockfp8_forward: block_m must be 0 (auto), 16, 32, 64 or 128");
         return MOE_ERR_ARG;
     }
-    if (path != MOE_FORWARD_AUTO && path != MOE_FORWARD_FUSED && path != MOE_FORWARD_STAGED) {
+    if (path != MOE_FORWARD_AUTO && path != MOE_FORWARD_FUSED && path != MOE_FORWARD_STAGED &&
+        path != MOE_FORWARD_STAGED_EPILOGUE_REDUCE) {
         set_error("moe_blockfp8_forward: unknown path %d", static_cast<int>(path));
         return MOE_ERR_ARG;
     }
@@ -324,6 +328,9 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     const size_t rws_bytes = P.off_xq - P.off_rws;
     if (path == MOE_FORWARD_AUTO) path = auto_path(M, k, E, E_local, H, N);
     const bool fused = path == MOE_FORWARD_FUSED;
+    // the weighted sum in the down GEMM's epilogue (block_m <= 32; otherwise the reduce kernel)
+    const bool epi_reduce = path == MOE_FORWARD_STAGED_EPILOGUE_REDUCE && P.bm <= 32;
+    unsigned* rcnt = reinterpret_cast<unsigned*>(ws + P.off_rcnt);
     unsigned* sync = reinterpret_cast<unsigned*>(ws + P.off_sync);
 
     int rc;
@@ -347,7 +354,8 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     }
     rc = launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, P.bm, MOE_ROUTE_AUTO,
                               sorted_idx, block_expert, num_blocks, counts, offsets, route_slot,
-                              ws + P.off_rws, rws_bytes, false, stream);
+                              ws + P.off_rws, rws_bytes, false, stream, epi_reduce ? rcnt : nullptr,
+                              epi_reduce ? M * (H / 128) : 0);
     if (rc) return rc;
     rc = launch_input_quant_tokens(x, M, H, k, route_slot, P.slots, xq, xs, act_fmt, true, stream);
     if (rc) return rc;
@@ -377,6 +385,13 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                               nullptr, nullptr, 0, route_slot, 0, P.slots, aq, as,
                               MOE_QUANT_PERSISTENT, true, stream, /*map_early=*/true);
     if (rc) return rc;
+    if (epi_reduce) {
+        const EpilogueReduce red{out, rcnt, topk_w, route_slot, k, M};
+        return launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, w_layout,
+                                   sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, z,
+                                   MOE_DTYPE_BF16, P.R, 1, true, stream, false, nullptr, nullptr, 0, 0,
+                                   &red);
+    }
     rc = launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, w_layout,
                              sorted_idx,
                              block_expert, num_blocks, P.B_cap, P.bm, z, MOE_DTYPE_BF16, P.R, 1,

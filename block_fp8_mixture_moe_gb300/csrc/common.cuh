@@ -52,6 +52,14 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
                          uint32_t* zero_ptr = nullptr, int zero_n = 0);
 size_t route_workspace_bytes(int R, int E_local, int block_m);
 bool route_single_cta(int R, int E_local, moe_route_path path);
+// The weighted top-k sum done in the down GEMM's epilogue (see GemmArgs in grouped_gemm.cu).
+struct EpilogueReduce {
+    void* out;            // [M, N_out] bf16
+    unsigned* cnt;        // [M, N_out/128] arrival counters, zero before the launch
+    const float* w;       // [M, k]
+    const int32_t* slot;  // route_slot [M*k]
+    int k, M;
+};
 int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int a_rows, int K,
                         const uint8_t* w_q, const float* w_s, int E_local, int N_out,
                         moe_weight_layout w_layout, const int32_t* sorted_idx, const int32_t* block_expert,
@@ -59,7 +67,7 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
                         cudaStream_t stream, bool wait_first = false,
                         const int32_t* self_ids = nullptr, const int32_t* self_map = nullptr,
-                        int self_R = 0, int self_E = 0);
+                        int self_R = 0, int self_E = 0, const EpilogueReduce* red = nullptr);
 // Largest route count for which the gate/up GEMM derives its block table itself.
 constexpr int kSelfRouteMaxRoutes = 32;
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,

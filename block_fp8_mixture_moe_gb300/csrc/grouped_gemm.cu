@@ -72,6 +72,17 @@ struct GemmArgs {
     const int32_t* self_ids;  // [self_R] global expert ids, or null
     const int32_t* self_map;  // nullable [self_E]
     int self_R, self_E;
+    // Epilogue reduce (DOWN, block_m <= 32; red_out == nullptr: none): the weighted top-k sum
+    // out[t] = bf16(sum_j w[t,j] z[t*k+j]) over the kept routes in top-k order.  After a unit's
+    // z rows are stored, each row counts itself in its (token, 128-column tile) counter; the
+    // arrival that completes a token's kept routes sums that token's 128 columns, so the order
+    // of the fp32 fused multiply-adds is the same whichever CTA does it.  Tokens with no kept
+    // route get zero rows.
+    uint16_t* red_out;        // [red_M, N_out] bf16
+    unsigned* red_cnt;        // [red_M, NT] arrivals, zero at launch
+    const float* red_w;       // [red_M, red_k] routing weights
+    const int32_t* red_slot;  // [red_M * red_k] route_slot: >= 0 for a kept route
+    int red_k, red_M;
 };
 
 template <int BM>
@@ -105,7 +116,7 @@ struct Cfg {
     // enough to fill every stage with weight tiles, one ring slot kept for the end marker
     static constexpr int kDefer = kStages < kRing - 1 ? kStages : kRing - 1;
     static constexpr int kDescHdr = 8;                 // ints: e, b, nt0, ntl, sp, kb0, nck, flags
-    static constexpr int kDescInts = kDescHdr + BM + kCK * BM + kSwMax;  // hdr, rows, sa, sw
+    static constexpr int kDescInts = kDescHdr + 2 * BM + kCK * BM + kSwMax;  // hdr, rows, kept, sa, sw
     static constexpr int kDescBytes = ((kDescInts * 4) + 15) / 16 * 16;
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmem = kStages * kStage + kRing * kDescBytes + kBarBytes + 1024;
@@ -113,7 +124,7 @@ struct Cfg {
     static_assert(kTSlots * kSlotCols <= 512, "tensor memory holds 512 fp32 columns");
     static_assert(kCK % kKps == 0, "descriptors hold whole stages");
     static_assert(kCK * BM == 512, "token-scale area of a descriptor is 512 values");
-    static_assert(((kDescHdr + BM) * 4) % 16 == 0, "token scales stay 16-byte aligned");
+    static_assert(((kDescHdr + 2 * BM) * 4) % 16 == 0, "token scales stay 16-byte aligned");
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -129,6 +140,7 @@ constexpr int kFirst = 1, kLast = 2, kEnd = 4;
 struct Desc {
     int* hdr;
     int* rows;
+    int* kept;  // epilogue reduce: kept routes of the token of row j
     float* sa;
     float* sw;
 };
@@ -140,7 +152,8 @@ __device__ __forceinline__ Desc desc_at(uint8_t* ring, int slot) {
     Desc d;
     d.hdr = base;
     d.rows = base + C::kDescHdr;
-    d.sa = reinterpret_cast<float*>(d.rows + BM);
+    d.kept = d.rows + BM;
+    d.sa = reinterpret_cast<float*>(d.kept + BM);
     d.sw = d.sa + C::kCK * BM;
     return d;
 }
@@ -167,8 +180,15 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     // set by an epilogue thread once its wait for the previous launch has returned
     volatile int* dep_seen = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
+    // epilogue reduce: per warpgroup, the tokens whose last unit the warpgroup just finished
+    // (double-buffered by unit parity) and two barriers of its 128 threads
+    __shared__ int red_list[2][2][32];
+    __shared__ int red_n[2][2];
+    __shared__ __align__(8) uint64_t rbar[4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        red_n[0][0] = red_n[0][1] = red_n[1][0] = red_n[1][1] = 0;
+        for (int i = 0; i < 4; ++i) mbar_init(rbar + i, 128);
         for (int i = 0; i < C::kStages; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
         for (int i = 0; i < C::kTSlots; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, C::kTemptyArrivals); }
         for (int i = 0; i < C::kRing; ++i) {
@@ -269,9 +289,9 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
             npend = 0;
         };
         int cur_b = -1, e = -1;
-        int rows[(BM + 31) / 32];
+        int rows[(BM + 31) / 32], kept[(BM + 31) / 32];
 #pragma unroll
-        for (int t = 0; t < (BM + 31) / 32; ++t) rows[t] = -1;
+        for (int t = 0; t < (BM + 31) / 32; ++t) { rows[t] = -1; kept[t] = 0; }
         // self-routing: lane r holds route r; match-any groups the routes of one expert, so a
         // route's rank in its expert is the number of same-expert lanes below it, and an
         // expert's padded offset is the sum of the padded counts of the active experts below it
@@ -350,6 +370,25 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                         }
                         rows[t] = row;
                     }
+                    if (p.red_out) {
+                        // epilogue reduce: the number of kept routes of each row's token
+#pragma unroll
+                        for (int t = 0; t < (BM + 31) / 32; ++t) {
+                            int cnt = 0;
+                            if (rows[t] >= 0) {
+                                const long long rb = static_cast<long long>(rows[t] / p.red_k) * p.red_k;
+                                for (int j0 = 0; j0 < p.red_k; j0 += 8) {
+                                    int sl[8];
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj)
+                                        sl[jj] = j0 + jj < p.red_k ? __ldcg(p.red_slot + rb + j0 + jj) : -1;
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj) cnt += sl[jj] >= 0 ? 1 : 0;
+                                }
+                            }
+                            kept[t] = cnt;
+                        }
+                    }
                 }
                 cur_b = b;
             }
@@ -382,7 +421,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                     mbar_arrive(dfull + slot);  // the header: the producer and the MMA go ahead
 #pragma unroll
                     for (int t = 0; t < (BM + 31) / 32; ++t)
-                        if (t * 32 + lane < BM) d.rows[t * 32 + lane] = rows[t];
+                        if (t * 32 + lane < BM) { d.rows[t * 32 + lane] = rows[t]; d.kept[t * 32 + lane] = kept[t]; }
 #pragma unroll
                     for (int q = 0; q < C::kSwMax / 32; ++q) {
                         const int i = q * 32 + lane;
@@ -416,6 +455,15 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                 mbar_arrive(dsa + slot);
             }
             if (npend > 0) flush_pending();
+        }
+        if (p.red_out && ok) {
+            // epilogue reduce: a token with no kept route gets a zero row (no unit sums it)
+            for (int tok = blockIdx.x; tok < p.red_M; tok += gridDim.x) {
+                const int sl = lane < p.red_k ? __ldcg(p.red_slot + static_cast<long long>(tok) * p.red_k + lane) : -1;
+                if (__any_sync(0xFFFFFFFFu, sl >= 0)) continue;
+                uint4* o = reinterpret_cast<uint4*>(p.red_out + static_cast<long long>(tok) * p.N_out);
+                for (int c = lane; c < p.N_out / 8; c += 32) o[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     } else if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -566,6 +614,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         const int c0 = C::kColSplit ? wg * C::kCpw : 0;  // this thread's first token column
         int unit = 0;
         bool mine = false;
+        uint32_t red_par = 0;  // epilogue reduce: phase of this warpgroup's rbar pair
         float acc[C::kCpw];
 #pragma unroll
         for (int j = 0; j < C::kCpw; ++j) acc[j] = 0.0f;
@@ -663,6 +712,69 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                             }
                         }
                     }
+                    if constexpr (!C::kColSplit) {
+                        if (p.red_out) {
+                            // Epilogue reduce.  All 128 threads arrive on rbar[0] after their z
+                            // stores of the unit; row j's thread then publishes them (fence, count)
+                            // and, if its arrival completes the token, lists the token; after
+                            // rbar[1] the warpgroup sums the listed tokens' columns.  The list is
+                            // double-buffered by unit parity; thread 0 clears the other buffer once
+                            // every thread has arrived for this unit (so it has finished the last
+                            // one).  Every wait is bounded.
+                            const int buf = red_par & 1;
+                            mbar_arrive(rbar + wg * 2 + 0);
+                            bool okr = true;
+                            if (r_in_tile < BM) {
+                                okr = mbar_wait_fast(rbar + wg * 2 + 0, red_par, abort_flag, p.status);
+                                if (okr) {
+                                    if (r_in_tile == 0) red_n[wg][buf ^ 1] = 0;
+                                    const int row = d.rows[r_in_tile];
+                                    if (row >= 0) {
+                                        const int tok = row / p.red_k;
+                                        __threadfence();
+                                        const unsigned old = atomicAdd(p.red_cnt + static_cast<long long>(tok) * p.NT + nt0 + t, 1u);
+                                        if (old + 1u == static_cast<unsigned>(d.kept[r_in_tile])) {
+                                            __threadfence();  // the token's other rows, stored by other units
+                                            red_list[wg][buf][atomicAdd(&red_n[wg][buf], 1)] = tok;
+                                        }
+                                    }
+                                }
+                            }
+                            mbar_arrive(rbar + wg * 2 + 1);
+                            okr = mbar_wait_fast(rbar + wg * 2 + 1, red_par, abort_flag, p.status) && okr;
+                            red_par ^= 1u;
+                            if (!__all_sync(0xFFFFFFFFu, okr)) goto epi_done;
+                            const int nd = red_n[wg][buf];
+                            for (int i = 0; i < nd; ++i) {
+                                // out[tok, n] = bf16(sum_j w[tok, j] z[tok*k + j, n]) over the
+                                // kept routes in top-k order (k_moe_reduce's arithmetic)
+                                const int tok = red_list[wg][buf][i];
+                                const long long rb = static_cast<long long>(tok) * p.red_k;
+                                const uint16_t* z = static_cast<const uint16_t*>(p.out);
+                                float sum = 0.0f;
+                                for (int j0 = 0; j0 < p.red_k; j0 += 8) {
+                                    int sl[8];
+                                    float wv[8];
+                                    uint16_t zv[8];
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj) {
+                                        const bool in = j0 + jj < p.red_k;
+                                        sl[jj] = in ? __ldcg(p.red_slot + rb + j0 + jj) : -1;
+                                        wv[jj] = in ? __ldg(p.red_w + rb + j0 + jj) : 0.0f;
+                                    }
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj)
+                                        zv[jj] = sl[jj] >= 0 ? __ldcg(z + (rb + j0 + jj) * p.N_out + n) : 0;
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj)
+                                        if (sl[jj] >= 0)
+                                            sum = __fmaf_rn(wv[jj], __uint_as_float(static_cast<uint32_t>(zv[jj]) << 16), sum);
+                                }
+                                p.red_out[static_cast<long long>(tok) * p.N_out + n] =
+                                    static_cast<uint16_t>(f32_to_bf16_bits(sum));
+                            }
+                        }
+                    }
                 }
             }
             mbar_arrive_relaxed(dempty + slot);
@@ -738,7 +850,7 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
                         cudaStream_t stream, bool wait_first, const int32_t* self_ids,
-                        const int32_t* self_map, int self_R, int self_E) {
+                        const int32_t* self_map, int self_R, int self_E, const EpilogueReduce* red) {
     if (proj != MOE_PROJ_GATE_UP && proj != MOE_PROJ_DOWN) { set_error("grouped_gemm: bad proj"); return MOE_ERR_ARG; }
     if (!a_q || !a_s || !w_q || !w_s || !sorted_idx || !block_expert || !num_blocks || !out) {
         set_error("grouped_gemm: null pointer");
@@ -816,6 +928,21 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
         p.self_map = self_map;
         p.self_R = self_R;
         p.self_E = self_E;
+    }
+    if (red) {
+        if (proj != MOE_PROJ_DOWN || block_m > 32 || out_dtype != MOE_DTYPE_BF16 || !red->out ||
+            !red->cnt || !red->w || !red->slot || red->k < 1 || red->k > kReduceMaxTopk ||
+            red->M < 1 || !aligned16(red->out)) {
+            set_error("grouped_gemm: the epilogue reduce needs DOWN, block_m <= 32, BF16 output and k <= %d",
+                      kReduceMaxTopk);
+            return MOE_ERR_ARG;
+        }
+        p.red_out = static_cast<uint16_t*>(red->out);
+        p.red_cnt = red->cnt;
+        p.red_w = red->w;
+        p.red_slot = red->slot;
+        p.red_k = red->k;
+        p.red_M = red->M;
     }
     const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
     switch (block_m) {

@@ -26,7 +26,7 @@ ROUTE_AUTO, ROUTE_SINGLE_CTA, ROUTE_MULTI_CTA = 0, 1, 2
 QUANT_AUTO, QUANT_PER_GROUP, QUANT_PERSISTENT = 0, 1, 2
 DEV_TIMEOUT, DEV_BAD_EXPERT_MAP, DEV_BAD_INDEX = 1, 2, 4
 WEIGHTS_ROW_MAJOR, WEIGHTS_TILED = 0, 1
-FORWARD_AUTO, FORWARD_FUSED, FORWARD_STAGED = 0, 1, 2
+FORWARD_AUTO, FORWARD_FUSED, FORWARD_STAGED, FORWARD_STAGED_EPILOGUE_REDUCE = 0, 1, 2, 3
 
 # every entry point of include/moefp8.h with its ctypes signature
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t

@@ -70,8 +70,15 @@ typedef enum { MOE_QUANT_AUTO = 0, MOE_QUANT_PER_GROUP = 1, MOE_QUANT_PERSISTENT
 typedef enum { MOE_WEIGHTS_ROW_MAJOR = 0, MOE_WEIGHTS_TILED = 1 } moe_weight_layout;
 /* FUSED: route preparation, then one persistent kernel for everything else (see
  * moe_blockfp8_forward).  STAGED: one launch per stage through the same kernels as the per-stage
- * entry points.  AUTO: the path this library measured to be faster for the shape. */
-typedef enum { MOE_FORWARD_AUTO = 0, MOE_FORWARD_FUSED = 1, MOE_FORWARD_STAGED = 2 } moe_forward_path;
+ * entry points.  STAGED_EPILOGUE_REDUCE: as STAGED, but the weighted top-k sum runs in the down
+ * GEMM's epilogue instead of a separate reduce launch (block_m <= 32; with a larger block_m it
+ * is STAGED).  AUTO: the path this library measured to be faster for the shape. */
+typedef enum {
+    MOE_FORWARD_AUTO = 0,
+    MOE_FORWARD_FUSED = 1,
+    MOE_FORWARD_STAGED = 2,
+    MOE_FORWARD_STAGED_EPILOGUE_REDUCE = 3
+} moe_forward_path;
 
 /* device status bits */
 #define MOE_DEV_TIMEOUT 1
@@ -262,8 +269,12 @@ MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* top
  *   whole duration (every wait is bounded; such a run ends with MOE_DEV_TIMEOUT in the device
  *   status word instead of hanging).  The gate/up K range is dealt to the SMs in equal pieces,
  *   so the fp32 summation order of the gate/up partial sums (not the arithmetic of any stage)
- *   depends on the SM count.  path STAGED: one launch per stage.  AUTO: see
- *   moe_forward_path_for.
+ *   depends on the SM count.  path STAGED: one launch per stage.  path STAGED_EPILOGUE_REDUCE:
+ *   the down GEMM also does the weighted top-k sum (lmdeploy PR #4228's reduce, with per-token
+ *   ownership): once a unit has stored its z rows, each row counts itself in a counter of its
+ *   (token, 128-column tile); the arrival that completes a token's kept routes sums that
+ *   token's 128 columns in top-k order with the same fp32 fused multiply-adds as moe_reduce,
+ *   so the output is bitwise the STAGED output.  AUTO: see moe_forward_path_for.
  * H and N multiples of 128; k <= E.  The staged path's reduce takes k <= 32: STAGED with a
  * larger k is refused (MOE_ERR_ARG, nothing enqueued) and AUTO then takes FUSED, which has no
  * top-k limit.  All stages run on `stream` with no host synchronisation, so the call can be

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 INF = float("inf")
 
 
-FUSED, STAGED = 1, 2  # moe_forward_path
+FUSED, STAGED, EPI = 1, 2, 3  # moe_forward_path (EPI: staged, reduce in the down epilogue)
 
 
 def _run(ops, L, act=1, clamp=INF, fmt=0, block_m=0, tiled=False, path=FUSED):
@@ -44,7 +44,7 @@ def _host(L, tokens=None):
     return wl.layer_numpy(L, experts=loc[loc >= 0])
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 @pytest.mark.parametrize("tiled", [False, True])
 @pytest.mark.parametrize("act,clamp,fmt", [(1, INF, 0), (1, INF, 1), (1, 7.0, 1), (2, 1.0, 0)])
 @pytest.mark.parametrize("block_m", [0, 16, 32, 64, 128])
@@ -55,7 +55,7 @@ def test_tiny_layer(ops, act, clamp, fmt, block_m, tiled, path):
     assert_bf16_close(got, ref, "tiny")
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 @pytest.mark.parametrize("M", wl.DECODE_M)
 def test_decode_full_size(ops, M, path):
     cfg = dict(wl.CONFIGS["decode"], M=M)
@@ -65,7 +65,7 @@ def test_decode_full_size(ops, M, path):
     assert_bf16_close(got, ref, f"decode M={M}")
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 @pytest.mark.parametrize("T", wl.EP_TOKENS)
 def test_expert_parallel_slice(ops, T, path):
     """k=6 of E=256 with 32 local experts through an expert map; non-local routes are dropped
@@ -88,7 +88,7 @@ def test_expert_parallel_slice(ops, T, path):
             assert (oracle.bf16_to_f32(got[none_local]) == 0).all()
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 def test_prefill_zipf_sampled(ops, path):
     cfg = wl.CONFIGS["prefill"]
     L = wl.make_layer(**cfg, seed=3, device="cuda")
@@ -102,7 +102,7 @@ def test_prefill_zipf_sampled(ops, path):
     assert_bf16_close(got[toks], ref[toks], "prefill sample")
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 def test_invalid_routes_and_empty(ops, path):
     L = wl.make_layer(M=9, H=256, N=128, E=12, k=3, seed=4, device="cuda", invalid_frac=0.3)
     got = _run(ops, L, path=path)
@@ -126,7 +126,7 @@ def test_invalid_routes_and_empty(ops, path):
     assert out.shape == (0, 256)
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 def test_forward_is_deterministic_and_graph_capturable(ops, path):
     cfg = dict(wl.CONFIGS["decode"], M=4)
     L = wl.make_layer(**cfg, seed=5, device="cuda")
@@ -153,7 +153,7 @@ def test_forward_is_deterministic_and_graph_capturable(ops, path):
     assert torch.equal(out, first)
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 @pytest.mark.parametrize("M", (64, 128, 256))
 def test_decode_large_m_sampled(ops, M, path):
     """The decode sweep's larger batches (H=7168, N=256, E=256, k=8), compared on a token
@@ -167,7 +167,7 @@ def test_decode_large_m_sampled(ops, M, path):
     assert_bf16_close(got[toks], ref[toks], f"decode M={M} sample")
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 def test_decode_hot_experts(ops, path):
     """Decode shape with every route on 12 hot experts (64 routes each, so several block_m=16
     blocks per expert and 244 idle experts)."""
@@ -185,7 +185,7 @@ def test_decode_hot_experts(ops, path):
     assert_bf16_close(got[toks], ref[toks], "hot experts sample")
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 @pytest.mark.parametrize("M", [16, 3])
 def test_graphs_with_different_routings_share_a_workspace(ops, path, M):
     """Three captured forwards with different routings on one workspace, replayed in a mixed
@@ -230,7 +230,7 @@ def test_graphs_with_different_routings_share_a_workspace(ops, path, M):
         assert not torch.equal(eager[s], eager[(s + 1) % 3])
 
 
-@pytest.mark.parametrize("path", [FUSED, STAGED])
+@pytest.mark.parametrize("path", [FUSED, STAGED, EPI])
 def test_host_activations_zero_copy(ops, path):
     """x, topk_ids, topk_w and out in pinned host memory: the kernels read and write them across
     the host link, bit for bit the result of the same call on device copies (decode M=16, and
@@ -256,3 +256,31 @@ def test_host_activations_zero_copy(ops, path):
     assert not ops.pointer_device_accessible(torch.zeros(4))
     with pytest.raises(AssertionError):
         ops.moe_blockfp8_forward(x_d.cpu(), ids_d, w_d, *args, path=path, **kw)
+
+
+@pytest.mark.parametrize("case", ["decode1", "decode4", "decode32", "decode64", "ep_t1", "ep_t100",
+                                  "dropped", "topk32", "bm32"])
+def test_epilogue_reduce_is_bitwise_the_staged_output(ops, case):
+    """The weighted top-k sum done in the down GEMM's epilogue (per-token ownership: the arrival
+    that completes a token's kept routes sums it, in top-k order) gives bit for bit the separate
+    reduce kernel's output, including zero rows for tokens with no kept route."""
+    kw, block_m = {}, 0
+    if case.startswith("decode"):
+        cfg, seed = dict(wl.CONFIGS["decode"], M=int(case[6:])), 40
+    elif case.startswith("ep_t"):
+        cfg, seed, kw = dict(wl.CONFIGS["ep"], M=int(case[4:])), 41, dict(clamp_limit=7.0, act_fmt=1)
+    elif case == "dropped":
+        cfg, seed = dict(M=9, H=256, N=128, E=12, k=3, invalid_frac=0.4), 42
+    elif case == "topk32":
+        cfg, seed = dict(M=5, H=384, N=128, E=40, k=32), 43
+    else:
+        cfg, seed, block_m = dict(wl.CONFIGS["decode"], M=16), 44, 32
+    L = wl.make_layer(**cfg, seed=seed, device="cuda")
+    emap = None if L["expert_map"] is None else to_dev(L["expert_map"])
+    args = (bf16_to_dev(L["x"]), to_dev(L["topk_ids"]), to_dev(L["topk_w"]), L["E"], emap,
+            L["wgu_q"], L["wgu_s"], L["wd_q"], L["wd_s"])
+    ref = ops.moe_blockfp8_forward(*args, path=STAGED, block_m=block_m, **kw)
+    got = ops.moe_blockfp8_forward(*args, path=EPI, block_m=block_m, **kw)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    assert torch.equal(got, ref)
