@@ -145,13 +145,34 @@ int gate_up_splits(int M, int k, int E, int E_local, int H, int N, int bm, int s
     return best;
 }
 
+// The grouped GEMMs' dynamic-tail counters: one 64-bit counter per projection in one
+// 256-byte region.
+constexpr size_t kSchedBytes = 256;
+
+// A GEMM takes the dynamic tail when its expected weight stream is at least this many bytes per
+// SM.  Measured on GB300 (graph-replayed layer, interleaved A/B): the Zipf prefill shape (about
+// 21 and 10 MB per SM for gate/up and down) went from 778 to 764 us, while at decode sizes
+// (at most ~6 MB per SM) and the expert-parallel shape the atomic round trips and, for the
+// self-routed gate/up GEMM, the earlier dependency wait cost more than the tail saves
+// (decode M=1: 33.4 -> 41.4 us).
+constexpr double kDynTailMinBytesPerSm = 8.0 * 1024 * 1024;
+
+// Whether a GEMM of N_out x K weights per expert takes the dynamic tail (see
+// kDynTailMinBytesPerSm): its expected active-expert weight bytes per SM.
+bool dyn_tail(int M, int k, int E, int E_local, int N_out, int K, int bm) {
+    if (bm > 32) return false;  // built for the plan's block sizes, 16 and 32
+    const double bytes = expected_blocks(M, k, E, E_local, bm) * (N_out / 128) * (K / 128) * 128.0 * 128.0;
+    return bytes / std::max(1, sm_count()) >= kDynTailMinBytesPerSm;
+}
+
 // One workspace layout serves both forward paths: the token-scale and partial-sum regions are
 // sized for the larger of the two uses (the fused kernel stores its token scales K-block major
-// and its gate/up partial sums per stream-K piece); the counters are the fused path's only.
+// and its gate/up partial sums per stream-K piece).  The counters: the fused kernel's, the
+// GEMMs' dynamic-tail counters and the epilogue-reduce counters.
 struct Plan {
     int bm, B_cap, slots, R, splits;
     size_t off_sorted, off_bexp, off_nb, off_cnt, off_off, off_rslot, off_rws, off_xq, off_xs,
-        off_gu, off_aq, off_as, off_z, off_sync, off_rcnt, total;
+        off_gu, off_aq, off_as, off_z, off_sync, off_sched, off_rcnt, total;
 };
 
 Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int sms) {
@@ -178,7 +199,10 @@ Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int 
     P.off_as = take(sizeof(float) * static_cast<size_t>(P.slots) * (N / 128));
     P.off_z = take(sizeof(uint16_t) * static_cast<size_t>(P.R) * H);
     P.off_sync = take(sizeof(unsigned) * static_cast<size_t>(fused_counter_words(P.B_cap)));
-    P.off_rcnt = take(sizeof(unsigned) * static_cast<size_t>(M) * (H / 128));  // epilogue-reduce counters
+    // the GEMMs' dynamic-tail counters (gate/up, down), directly followed by the epilogue-reduce
+    // counters, so that route preparation zeroes both as one range
+    P.off_sched = take(kSchedBytes);
+    P.off_rcnt = take(sizeof(unsigned) * static_cast<size_t>(M) * (H / 128));
     P.total = o;
     return P;
 }
@@ -247,6 +271,21 @@ extern "C" int moe_blockfp8_plan(int M, int k, int E, int E_local, int H, int N,
     if (out_block_m) *out_block_m = P.bm;
     if (out_B_cap) *out_B_cap = P.B_cap;
     if (out_splits) *out_splits = P.splits;
+    return MOE_OK;
+}
+
+extern "C" int moe_blockfp8_dynamic_tail(int M, int k, int E, int E_local, int H, int N, int block_m,
+                                         int* gate_up, int* down) {
+    clear_error();
+    if (!gate_up || !down || M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0 ||
+        H % 128 || N % 128 ||
+        (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)) {
+        set_error("moe_blockfp8_dynamic_tail: bad sizes or null outputs");
+        return MOE_ERR_ARG;
+    }
+    const int bm = block_m > 0 ? block_m : forward_block_m(M, k, E_local, H, N);
+    *gate_up = dyn_tail(M, k, E, E_local, 2 * N, H, bm) ? 1 : 0;
+    *down = dyn_tail(M, k, E, E_local, H, N, bm) ? 1 : 0;
     return MOE_OK;
 }
 
@@ -332,6 +371,9 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     const bool epi_reduce = path == MOE_FORWARD_STAGED_EPILOGUE_REDUCE && P.bm <= 32;
     unsigned* rcnt = reinterpret_cast<unsigned*>(ws + P.off_rcnt);
     unsigned* sync = reinterpret_cast<unsigned*>(ws + P.off_sync);
+    unsigned long long* sched = reinterpret_cast<unsigned long long*>(ws + P.off_sched);
+    const bool dyn_gu = dyn_tail(M, k, E, E_local, 2 * N, H, P.bm);
+    const bool dyn_dn = dyn_tail(M, k, E, E_local, H, N, P.bm);
 
     int rc;
     if (fused) {
@@ -354,8 +396,9 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     }
     rc = launch_route_prepare(topk_ids, M, k, E, expert_map, E_local, P.bm, MOE_ROUTE_AUTO,
                               sorted_idx, block_expert, num_blocks, counts, offsets, route_slot,
-                              ws + P.off_rws, rws_bytes, false, stream, epi_reduce ? rcnt : nullptr,
-                              epi_reduce ? M * (H / 128) : 0);
+                              ws + P.off_rws, rws_bytes, false, stream,
+                              reinterpret_cast<uint32_t*>(sched),
+                              static_cast<int>(kSchedBytes / 4) + (epi_reduce ? M * (H / 128) : 0));
     if (rc) return rc;
     rc = launch_input_quant_tokens(x, M, H, k, route_slot, P.slots, xq, xs, act_fmt, true, stream);
     if (rc) return rc;
@@ -367,11 +410,12 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
         rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
                                  w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
                                  MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/false,
-                                 topk_ids, expert_map, P.R, E);
+                                 topk_ids, expert_map, P.R, E, nullptr, dyn_gu ? sched : nullptr);
     else
         rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
                                  w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
-                                 MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/true);
+                                 MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/true,
+                                 nullptr, nullptr, 0, 0, nullptr, dyn_gu ? sched : nullptr);
     if (rc) return rc;
     // act-quant walks the routes (through route_slot) or, when the blocks hold fewer slots than
     // there are routes (an expert map that keeps few of them), the slots of the blocks that exist
@@ -390,12 +434,13 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
         return launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, w_layout,
                                    sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, z,
                                    MOE_DTYPE_BF16, P.R, 1, true, stream, false, nullptr, nullptr, 0, 0,
-                                   &red);
+                                   &red, dyn_dn ? sched + 1 : nullptr);
     }
     rc = launch_grouped_gemm(MOE_PROJ_DOWN, aq, as, P.slots, N, wd_q, wd_s, E_local, H, w_layout,
                              sorted_idx,
                              block_expert, num_blocks, P.B_cap, P.bm, z, MOE_DTYPE_BF16, P.R, 1,
-                             true, stream);
+                             true, stream, false, nullptr, nullptr, 0, 0, nullptr,
+                             dyn_dn ? sched + 1 : nullptr);
     if (rc) return rc;
     return launch_moe_reduce(z, topk_w, topk_ids, expert_map, M, k, E, E_local, H, out, true, stream);
 }

@@ -67,7 +67,8 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
                         cudaStream_t stream, bool wait_first = false,
                         const int32_t* self_ids = nullptr, const int32_t* self_map = nullptr,
-                        int self_R = 0, int self_E = 0, const EpilogueReduce* red = nullptr);
+                        int self_R = 0, int self_E = 0, const EpilogueReduce* red = nullptr,
+                        unsigned long long* sched = nullptr);
 // Largest route count for which the gate/up GEMM derives its block table itself.
 constexpr int kSelfRouteMaxRoutes = 32;
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,

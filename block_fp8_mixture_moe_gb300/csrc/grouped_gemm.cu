@@ -83,7 +83,15 @@ struct GemmArgs {
     const float* red_w;       // [red_M, red_k] routing weights
     const int32_t* red_slot;  // [red_M * red_k] route_slot: >= 0 for a kept route
     int red_k, red_M;
+    // Dynamic tail (sched == nullptr: none).  The CTAs first walk equal static shares of three
+    // quarters of the units, then take the rest sched_chunk units at a time from this counter
+    // (zero at launch), so the SMs that stream faster or start later even out at the end.
+    unsigned long long* sched;
+    int sched_chunk;
 };
+
+// Weight bytes of one chunk of the dynamic tail.
+constexpr long long kSchedChunkBytes = 64 * 1024;
 
 template <int BM>
 struct Cfg {
@@ -158,7 +166,9 @@ __device__ __forceinline__ Desc desc_at(uint8_t* ring, int slot) {
     return d;
 }
 
-template <int BM>
+// DYN: the dynamic tail (p.sched) is compiled in.  A separate instantiation, because the code
+// alone, never taken, made the small decode layers ~2 us slower (M=1: 35.3 vs 33.3 us).
+template <int BM, bool DYN>
 __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_a, GemmArgs p) {
@@ -241,13 +251,14 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
         // its shared-memory stores.
         int nblk = self_route ? 0 : __ldcg(p.num_blocks);
         nblk = max(0, min(nblk, p.B_cap));
-        const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
-        const long long u_lo = units * blockIdx.x / gridDim.x;
-        const long long u_hi = units * (blockIdx.x + 1) / gridDim.x;
-        int nt = static_cast<int>(u_lo % p.NT);
-        int sp = static_cast<int>((u_lo / p.NT) % p.splits);
-        int b = static_cast<int>(u_lo / (static_cast<long long>(p.NT) * p.splits));
-        long long left = u_hi - u_lo;
+        int nt = 0, sp = 0, b = 0;
+        long long left = 0;
+        // unit u's position: tile fastest, then split, then block
+        auto seek = [&](long long u) {
+            nt = static_cast<int>(u % p.NT);
+            sp = static_cast<int>((u / p.NT) % p.splits);
+            b = static_cast<int>(u / (static_cast<long long>(p.NT) * p.splits));
+        };
         int slot = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -322,127 +333,159 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                     sr_off += ej < er ? pj : 0;  // pj > 0 only for an active expert's leader
                 }
                 nblk = min(total / BM, p.B_cap);
-                const long long units_s = static_cast<long long>(nblk) * p.NT * p.splits;
-                const long long lo_s = units_s * blockIdx.x / gridDim.x;
-                nt = static_cast<int>(lo_s % p.NT);
-                sp = static_cast<int>((lo_s / p.NT) % p.splits);
-                b = static_cast<int>(lo_s / (static_cast<long long>(p.NT) * p.splits));
-                left = units_s * (blockIdx.x + 1) / gridDim.x - lo_s;
             }
         }
-        while (left > 0 && ok) {
-            if (self_route && b != cur_b) {
-                if constexpr (BM <= 32) {
-                    // block b belongs to the active expert whose padded run holds slot b*BM
-                    const unsigned own = __ballot_sync(0xFFFFFFFFu, sr_lead && sr_off <= b * BM &&
-                                                                        b * BM < sr_off + sr_pad);
-                    const int src = own ? __ffs(own) - 1 : 0;
-                    const int e_b = __shfl_sync(0xFFFFFFFFu, sr_e, src);
-                    const int off_b = __shfl_sync(0xFFFFFFFFu, sr_off, src);
-                    const int cnt_b = __shfl_sync(0xFFFFFFFFu, sr_cnt, src);
-                    e = own ? e_b : -1;
-                    int row = (lane < BM && e >= 0 && b * BM + lane - off_b < cnt_b) ? b * BM + lane : -1;
-                    if (row >= p.out_rows) {
-                        if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
-                        row = -1;
-                    }
-                    rows[0] = row;
-                }
-                cur_b = b;
-            } else if (b != cur_b) {
-                // the block's expert and its slot rows, loaded together
-                const int e_raw = __ldcg(p.block_expert + b);
-                int rr[(BM + 31) / 32];
-#pragma unroll
-                for (int t = 0; t < (BM + 31) / 32; ++t) {
-                    const int j = t * 32 + lane;
-                    rr[t] = j < BM ? __ldcg(p.sorted_idx + b * BM + j) : -1;
-                }
-                e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
-                if (e >= 0) {
-#pragma unroll
-                    for (int t = 0; t < (BM + 31) / 32; ++t) {
-                        const int slot_j = b * BM + t * 32 + lane;
-                        int row = rr[t] < 0 ? -1 : (p.scatter ? rr[t] : slot_j);
+        // this CTA's static range: an equal share of the units, or, with the dynamic tail, an
+        // equal share of three quarters of them; the rest [dyn_base, units) is handed out
+        const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
+        long long dyn_base = units;
+        if (DYN) {
+            const long long share = units * 3 / (4LL * gridDim.x);
+            dyn_base = share * gridDim.x;
+            seek(share * blockIdx.x);
+            left = share;
+        } else {
+            const long long lo = units * blockIdx.x / gridDim.x;
+            seek(lo);
+            left = units * (blockIdx.x + 1) / gridDim.x - lo;
+        }
+        unsigned long long dyn_pend = 0;  // lane 0: the counter value of the chunk taken ahead
+        bool dyn_started = false;
+        for (;;) {
+            while (left > 0 && ok) {
+                if (self_route && b != cur_b) {
+                    if constexpr (BM <= 32) {
+                        // block b belongs to the active expert whose padded run holds slot b*BM
+                        const unsigned own = __ballot_sync(0xFFFFFFFFu, sr_lead && sr_off <= b * BM &&
+                                                                            b * BM < sr_off + sr_pad);
+                        const int src = own ? __ffs(own) - 1 : 0;
+                        const int e_b = __shfl_sync(0xFFFFFFFFu, sr_e, src);
+                        const int off_b = __shfl_sync(0xFFFFFFFFu, sr_off, src);
+                        const int cnt_b = __shfl_sync(0xFFFFFFFFu, sr_cnt, src);
+                        e = own ? e_b : -1;
+                        int row = (lane < BM && e >= 0 && b * BM + lane - off_b < cnt_b) ? b * BM + lane : -1;
                         if (row >= p.out_rows) {
                             if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
                             row = -1;
                         }
-                        rows[t] = row;
+                        rows[0] = row;
                     }
-                    if (p.red_out) {
-                        // epilogue reduce: the number of kept routes of each row's token
-#pragma unroll
+                    cur_b = b;
+                } else if (b != cur_b) {
+                    // the block's expert and its slot rows, loaded together
+                    const int e_raw = __ldcg(p.block_expert + b);
+                    int rr[(BM + 31) / 32];
+    #pragma unroll
+                    for (int t = 0; t < (BM + 31) / 32; ++t) {
+                        const int j = t * 32 + lane;
+                        rr[t] = j < BM ? __ldcg(p.sorted_idx + b * BM + j) : -1;
+                    }
+                    e = (e_raw >= 0 && e_raw < p.E_local) ? e_raw : -1;
+                    if (e >= 0) {
+    #pragma unroll
                         for (int t = 0; t < (BM + 31) / 32; ++t) {
-                            int cnt = 0;
-                            if (rows[t] >= 0) {
-                                const long long rb = static_cast<long long>(rows[t] / p.red_k) * p.red_k;
-                                for (int j0 = 0; j0 < p.red_k; j0 += 8) {
-                                    int sl[8];
-#pragma unroll
-                                    for (int jj = 0; jj < 8; ++jj)
-                                        sl[jj] = j0 + jj < p.red_k ? __ldcg(p.red_slot + rb + j0 + jj) : -1;
-#pragma unroll
-                                    for (int jj = 0; jj < 8; ++jj) cnt += sl[jj] >= 0 ? 1 : 0;
-                                }
+                            const int slot_j = b * BM + t * 32 + lane;
+                            int row = rr[t] < 0 ? -1 : (p.scatter ? rr[t] : slot_j);
+                            if (row >= p.out_rows) {
+                                if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                                row = -1;
                             }
-                            kept[t] = cnt;
+                            rows[t] = row;
+                        }
+                        if (p.red_out) {
+                            // epilogue reduce: the number of kept routes of each row's token
+    #pragma unroll
+                            for (int t = 0; t < (BM + 31) / 32; ++t) {
+                                int cnt = 0;
+                                if (rows[t] >= 0) {
+                                    const long long rb = static_cast<long long>(rows[t] / p.red_k) * p.red_k;
+                                    for (int j0 = 0; j0 < p.red_k; j0 += 8) {
+                                        int sl[8];
+    #pragma unroll
+                                        for (int jj = 0; jj < 8; ++jj)
+                                            sl[jj] = j0 + jj < p.red_k ? __ldcg(p.red_slot + rb + j0 + jj) : -1;
+    #pragma unroll
+                                        for (int jj = 0; jj < 8; ++jj) cnt += sl[jj] >= 0 ? 1 : 0;
+                                    }
+                                }
+                                kept[t] = cnt;
+                            }
                         }
                     }
+                    cur_b = b;
                 }
-                cur_b = b;
-            }
-            const int run = static_cast<int>(min(static_cast<long long>(p.NT - nt), left));
-            int adv = run;
-            if (e >= 0) {
-                const int kb0 = sp * p.KB / p.splits, kb1 = (sp + 1) * p.KB / p.splits;
-                const int len = kb1 - kb0;
-                const bool whole = len <= C::kCK;
-                const int ntl = whole ? min(run, C::kSwMax / len) : 1;
-                adv = ntl;
-                for (int c0 = kb0; c0 < kb1 && ok; c0 += C::kCK) {
-                    const int nck = min(C::kCK, kb1 - c0);
-                    float sw_v[C::kSwMax / 32];
-                    const int n_sw = ntl * nck;
-#pragma unroll
-                    for (int q = 0; q < C::kSwMax / 32; ++q) {
-                        const int i = q * 32 + lane;
-                        const int t = i / nck, kk = i - t * nck;
-                        sw_v[q] = i < n_sw ? __ldg(p.w_s + (static_cast<long long>(e) * p.NT + nt + t) * p.KB + c0 + kk) : 0.0f;
+                const int run = static_cast<int>(min(static_cast<long long>(p.NT - nt), left));
+                int adv = run;
+                if (e >= 0) {
+                    const int kb0 = sp * p.KB / p.splits, kb1 = (sp + 1) * p.KB / p.splits;
+                    const int len = kb1 - kb0;
+                    const bool whole = len <= C::kCK;
+                    const int ntl = whole ? min(run, C::kSwMax / len) : 1;
+                    adv = ntl;
+                    for (int c0 = kb0; c0 < kb1 && ok; c0 += C::kCK) {
+                        const int nck = min(C::kCK, kb1 - c0);
+                        float sw_v[C::kSwMax / 32];
+                        const int n_sw = ntl * nck;
+    #pragma unroll
+                        for (int q = 0; q < C::kSwMax / 32; ++q) {
+                            const int i = q * 32 + lane;
+                            const int t = i / nck, kk = i - t * nck;
+                            sw_v[q] = i < n_sw ? __ldg(p.w_s + (static_cast<long long>(e) * p.NT + nt + t) * p.KB + c0 + kk) : 0.0f;
+                        }
+                        ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
+                        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                        Desc d = desc_at<BM>(ring, slot);
+                        if (lane == 0) {
+                            d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt; d.hdr[3] = ntl; d.hdr[4] = sp;
+                            d.hdr[5] = c0; d.hdr[6] = nck;
+                            d.hdr[7] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
+                        }
+                        mbar_arrive(dfull + slot);  // the header: the producer and the MMA go ahead
+    #pragma unroll
+                        for (int t = 0; t < (BM + 31) / 32; ++t)
+                            if (t * 32 + lane < BM) { d.rows[t * 32 + lane] = rows[t]; d.kept[t * 32 + lane] = kept[t]; }
+    #pragma unroll
+                        for (int q = 0; q < C::kSwMax / 32; ++q) {
+                            const int i = q * 32 + lane;
+                            if (i < n_sw) d.sw[i] = sw_v[q];
+                        }
+                        if (dep_done) {
+                            fill_sa(slot, b, c0, nck);
+                        } else {
+                            if (npend == 0) pend0 = slot;
+                            ++npend;
+                        }
+                        if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
+                        if (npend == C::kDefer) flush_pending();
                     }
-                    ok = mbar_wait_fast(dempty + slot, ph ^ 1u, abort_flag, p.status);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                    Desc d = desc_at<BM>(ring, slot);
-                    if (lane == 0) {
-                        d.hdr[0] = e; d.hdr[1] = b; d.hdr[2] = nt; d.hdr[3] = ntl; d.hdr[4] = sp;
-                        d.hdr[5] = c0; d.hdr[6] = nck;
-                        d.hdr[7] = (c0 == kb0 ? kFirst : 0) | (c0 + nck == kb1 ? kLast : 0);
-                    }
-                    mbar_arrive(dfull + slot);  // the header: the producer and the MMA go ahead
-#pragma unroll
-                    for (int t = 0; t < (BM + 31) / 32; ++t)
-                        if (t * 32 + lane < BM) { d.rows[t * 32 + lane] = rows[t]; d.kept[t * 32 + lane] = kept[t]; }
-#pragma unroll
-                    for (int q = 0; q < C::kSwMax / 32; ++q) {
-                        const int i = q * 32 + lane;
-                        if (i < n_sw) d.sw[i] = sw_v[q];
-                    }
-                    if (dep_done) {
-                        fill_sa(slot, b, c0, nck);
-                    } else {
-                        if (npend == 0) pend0 = slot;
-                        ++npend;
-                    }
-                    if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
-                    if (npend == C::kDefer) flush_pending();
+                }
+                // advance by adv units (never past the end of this block and split's tile run)
+                nt += adv;
+                left -= adv;
+                if (nt == p.NT) {
+                    nt = 0;
+                    if (++sp == p.splits) { sp = 0; ++b; }
                 }
             }
-            // advance by adv units (never past the end of this block and split's tile run)
-            nt += adv;
-            left -= adv;
-            if (nt == p.NT) {
-                nt = 0;
-                if (++sp == p.splits) { sp = 0; ++b; }
+            if constexpr (!DYN) break;
+            else {
+                if (!ok) break;
+                // Dynamic tail.  Route preparation zeroes the counter: a launch that has not yet waited
+                // for its predecessor (self-routing) does so first.  Each chunk's successor is taken
+                // when the chunk starts, so the atomic's round trip overlaps the chunk's descriptors.
+                if (!dep_done) flush_pending();
+                unsigned long long v = 0;
+                if (!dyn_started) {
+                    if (lane == 0) v = atomicAdd(p.sched, static_cast<unsigned long long>(p.sched_chunk));
+                    dyn_started = true;
+                } else {
+                    v = dyn_pend;
+                }
+                const long long c = dyn_base + static_cast<long long>(__shfl_sync(0xFFFFFFFFu, v, 0));
+                if (c >= units) break;
+                if (lane == 0) dyn_pend = atomicAdd(p.sched, static_cast<unsigned long long>(p.sched_chunk));
+                seek(c);
+                left = min(static_cast<long long>(p.sched_chunk), units - c);
             }
         }
         if (ok) {
@@ -792,18 +835,18 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
     }
 }
 
-template <int BM>
+template <int BM, bool DYN>
 int launch_bm(const CUtensorMap& tw, const CUtensorMap& ta, const GemmArgs& p, long long max_units,
               bool pdl, cudaStream_t stream) {
     using C = Cfg<BM>;
-    if (!ensure_smem(reinterpret_cast<const void*>(k_grouped_gemm<BM>), C::kSmem)) {
+    if (!ensure_smem(reinterpret_cast<const void*>(k_grouped_gemm<BM, DYN>), C::kSmem)) {
         set_error("grouped_gemm: shared-memory limit %d refused", C::kSmem);
         return MOE_ERR_LAUNCH;
     }
     long long grid = std::min<long long>(sm_count(), max_units);
     if (grid <= 0) return MOE_OK;
     Launch L(dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmem, stream, pdl);
-    cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_grouped_gemm<BM>, tw, ta, p);
+    cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_grouped_gemm<BM, DYN>, tw, ta, p);
     if (e != cudaSuccess) { set_error("grouped_gemm launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     return MOE_OK;
 }
@@ -850,7 +893,8 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         const int32_t* num_blocks, int B_cap, int block_m, void* out,
                         moe_dtype out_dtype, int out_rows, int splits, bool pdl,
                         cudaStream_t stream, bool wait_first, const int32_t* self_ids,
-                        const int32_t* self_map, int self_R, int self_E, const EpilogueReduce* red) {
+                        const int32_t* self_map, int self_R, int self_E, const EpilogueReduce* red,
+                        unsigned long long* sched) {
     if (proj != MOE_PROJ_GATE_UP && proj != MOE_PROJ_DOWN) { set_error("grouped_gemm: bad proj"); return MOE_ERR_ARG; }
     if (!a_q || !a_s || !w_q || !w_s || !sorted_idx || !block_expert || !num_blocks || !out) {
         set_error("grouped_gemm: null pointer");
@@ -944,12 +988,25 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
         p.red_k = red->k;
         p.red_M = red->M;
     }
+    if (sched && block_m > 32) {
+        set_error("grouped_gemm: the dynamic tail is built for block_m 16 and 32");
+        return MOE_ERR_ARG;
+    }
+    if (sched) {
+        // dynamic chunks of about 64 KB of weights: a short tail, and few enough descriptors
+        // that the metadata warp keeps ahead of the producer
+        const long long unit_bytes = static_cast<long long>((KB + splits - 1) / splits) * 128 * 128;
+        p.sched = sched;
+        p.sched_chunk = static_cast<int>(std::max(1LL, (kSchedChunkBytes + unit_bytes - 1) / unit_bytes));
+    }
     const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
     switch (block_m) {
-        case 16: return launch_bm<16>(tw, ta, p, max_units, pdl, stream);
-        case 32: return launch_bm<32>(tw, ta, p, max_units, pdl, stream);
-        case 64: return launch_bm<64>(tw, ta, p, max_units, pdl, stream);
-        default: return launch_bm<128>(tw, ta, p, max_units, pdl, stream);
+        case 16: return p.sched ? launch_bm<16, true>(tw, ta, p, max_units, pdl, stream)
+                                : launch_bm<16, false>(tw, ta, p, max_units, pdl, stream);
+        case 32: return p.sched ? launch_bm<32, true>(tw, ta, p, max_units, pdl, stream)
+                                : launch_bm<32, false>(tw, ta, p, max_units, pdl, stream);
+        case 64: return launch_bm<64, false>(tw, ta, p, max_units, pdl, stream);
+        default: return launch_bm<128, false>(tw, ta, p, max_units, pdl, stream);
     }
 }
 

@@ -50,6 +50,8 @@ SIGNATURES = {
     "moe_forward_block_m": (_I, [_I, _I, _I, _I, _I]),
     "moe_blockfp8_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
                                ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "moe_blockfp8_dynamic_tail": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(ctypes.c_int)]),
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_get_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "moe_device_supported": (_I, []),
@@ -340,6 +342,14 @@ def moe_blockfp8_plan(M, k, E, E_local, H, N, block_m=0):
     _check(load().moe_blockfp8_plan(M, k, E, E_local, H, N, block_m, ctypes.byref(bm),
                                     ctypes.byref(bc), ctypes.byref(sp)), "moe_blockfp8_plan")
     return bm.value, bc.value, sp.value
+
+
+def moe_blockfp8_dynamic_tail(M, k, E, E_local, H, N, block_m=0):
+    """(gate_up, down): whether the staged forward's GEMMs take the dynamic tail."""
+    gu, dn = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().moe_blockfp8_dynamic_tail(M, k, E, E_local, H, N, block_m, ctypes.byref(gu),
+                                            ctypes.byref(dn)), "moe_blockfp8_dynamic_tail")
+    return bool(gu.value), bool(dn.value)
 
 
 def moe_blockfp8_forward(x, topk_ids, topk_w, E, expert_map, wgu_q, wgu_s, wd_q, wd_s,

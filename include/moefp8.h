@@ -333,6 +333,16 @@ MOEFP8_API int moe_forward_block_m(int M, int k, int E_local, int H, int N);
 MOEFP8_API int moe_blockfp8_plan(int M, int k, int E, int E_local, int H, int N, int block_m,
                                  int* out_block_m, int* out_B_cap, int* out_splits);
 
+/* Whether the staged forward's gate/up and down GEMMs (*gate_up, *down: 1 or 0) hand out the
+ * last quarter of their work units from a counter in the workspace instead of splitting all of
+ * them statically over the SMs: only when a GEMM's expected active-expert weight stream is long
+ * (at least 8 MB per SM), where the SMs' differing streaming rates would otherwise leave a
+ * tail.  A scheduling choice of this library, no counterpart in the pages; every unit is
+ * computed exactly as in the static split, so the results are the same bit for bit.  Host
+ * only; MOE_OK, or MOE_ERR_ARG for bad sizes or null outputs. */
+MOEFP8_API int moe_blockfp8_dynamic_tail(int M, int k, int E, int E_local, int H, int N,
+                                         int block_m, int* gate_up, int* down);
+
 /* ------------------------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------------------------ */
