@@ -151,10 +151,11 @@ constexpr size_t kSchedBytes = 256;
 
 // A GEMM takes the dynamic tail when its expected weight stream is at least this many bytes per
 // SM.  Measured on GB300 (graph-replayed layer, interleaved A/B): the Zipf prefill shape (about
-// 21 and 10 MB per SM for gate/up and down) went from 778 to 764 us, while at decode sizes
-// (at most ~6 MB per SM) and the expert-parallel shape the atomic round trips and, for the
-// self-routed gate/up GEMM, the earlier dependency wait cost more than the tail saves
-// (decode M=1: 33.4 -> 41.4 us).
+// 21 and 10 MB per SM for gate/up and down) went from 780 to 741 us.  With every GEMM taking
+// it, decode M=64 lost 5 us, M=32 and the expert-parallel shape 2 us, M=256 gained 3.5 us; a
+// threshold of 6 MB (taking the gate/up GEMMs of M=128 and 256) measured the same as 8 MB.
+// The self-routed gate/up GEMM would also have to wait for its predecessor before the tail
+// (decode M=1: 33.4 -> 41.4 us with it).
 constexpr double kDynTailMinBytesPerSm = 8.0 * 1024 * 1024;
 
 // Whether a GEMM of N_out x K weights per expert takes the dynamic tail (see

@@ -90,8 +90,10 @@ struct GemmArgs {
     int sched_chunk;
 };
 
-// Weight bytes of one chunk of the dynamic tail.
-constexpr long long kSchedChunkBytes = 64 * 1024;
+// Weight bytes of one chunk of the dynamic tail.  Measured on the Zipf prefill layer: 32 and
+// 64 KB 760-765 us, 128 KB 741 us, 256 KB 745 us, 512 KB 750 us (its down GEMM's 96 KB units
+// then go two to a chunk and a descriptor).
+constexpr long long kSchedChunkBytes = 128 * 1024;
 
 template <int BM>
 struct Cfg {
@@ -993,8 +995,8 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
         return MOE_ERR_ARG;
     }
     if (sched) {
-        // dynamic chunks of about 64 KB of weights: a short tail, and few enough descriptors
-        // that the metadata warp keeps ahead of the producer
+        // dynamic chunks of about kSchedChunkBytes of weights: a short tail, and few enough
+        // descriptors that the metadata warp keeps ahead of the producer
         const long long unit_bytes = static_cast<long long>((KB + splits - 1) / splits) * 128 * 128;
         p.sched = sched;
         p.sched_chunk = static_cast<int>(std::max(1LL, (kSchedChunkBytes + unit_bytes - 1) / unit_bytes));
