@@ -296,10 +296,16 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
 // Pairs of 128-groups each warp of the input quantisation quantises before the routing wait.
 constexpr int kInputHold = 2;
 
+// PADS: the kernel also writes the -1 pads of sorted_idx that route preparation left out (a
+// separate instantiation: the code alone, never taken, cost the small decode layers ~0.5 us).
+template <bool PADS>
 __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __restrict__ x, int M,
                                                             int H, int k, const int32_t* route_slot,
                                                             int slots, uint8_t* xq, float* xs,
-                                                            int fmt, int* status) {
+                                                            int fmt, int* status,
+                                                            const int32_t* pad_off,
+                                                            const int32_t* pad_cnt,
+                                                            int32_t* pad_sorted, int pad_E) {
     constexpr int kHold = kInputHold;
     const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
     const int G = H / 128;
@@ -351,6 +357,16 @@ __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __re
 #pragma unroll
     for (int i = 0; i < kHold; ++i)
         if (ha[i]) scatter(ht[i], hg[i], hc[i], hs[i]);
+    if constexpr (PADS) {
+        // the -1 pads of sorted_idx that route preparation left out: one warp per expert, the
+        // slots after its count up to the next expert's start, then every slot past the blocks
+        for (long long e = w0; e < pad_E; e += warps) {
+            const int lo = __ldcg(pad_off + e) + __ldcg(pad_cnt + e), hi = __ldcg(pad_off + e + 1);
+            for (int sl = lo + lane; sl < hi; sl += 32) pad_sorted[sl] = -1;
+        }
+        for (long long sl = __ldcg(pad_off + pad_E) + w0 * 32 + lane; sl < slots; sl += warps * 32)
+            pad_sorted[sl] = -1;
+    }
     for (long long pr = w0 + kHold * warps; pr < pairs; pr += warps) {
         int t, g;
         uint2 codes;
@@ -529,7 +545,8 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
 
 int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t* route_slot,
                               int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const int32_t* pad_offset,
+                              const int32_t* pad_count, int32_t* pad_sorted, int pad_E) {
     const long long pairs = (static_cast<long long>(M) * (H / 128) + 1) / 2;
     if (pairs == 0) return MOE_OK;
     // One pair per warp, at most two CTAs per SM, so the next kernel's CTAs fit beside them.
@@ -541,9 +558,13 @@ int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t*
     long long blocks = std::min<long long>((pairs + 7) / 8, sms * 2);
     if (blocks * 8 * kInputHold < pairs) blocks = std::min<long long>((pairs + 15) / 16, sms * 4);
     Launch L(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl);
-    cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_input_quant_tokens, static_cast<const uint16_t*>(x),
-                                       M, H, k, route_slot, slots, xq, xs, static_cast<int>(fmt),
-                                       device_status_ptr());
+    cudaError_t e = pad_sorted
+        ? cudaLaunchKernelEx(&L.cfg, k_input_quant_tokens<true>, static_cast<const uint16_t*>(x), M, H, k,
+                             route_slot, slots, xq, xs, static_cast<int>(fmt), device_status_ptr(),
+                             pad_offset, pad_count, pad_sorted, pad_E)
+        : cudaLaunchKernelEx(&L.cfg, k_input_quant_tokens<false>, static_cast<const uint16_t*>(x), M, H, k,
+                             route_slot, slots, xq, xs, static_cast<int>(fmt), device_status_ptr(),
+                             pad_offset, pad_count, pad_sorted, pad_E);
     if (e != cudaSuccess) { set_error("input quant launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     return MOE_OK;
 }

@@ -43,13 +43,15 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
 // Per-token input quantisation scattered to the route slots (the layer's first stage).
 int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t* route_slot,
                               int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const int32_t* pad_offset = nullptr,
+                              const int32_t* pad_count = nullptr, int32_t* pad_sorted = nullptr,
+                              int pad_E = 0);
 int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int32_t* expert_map,
                          int E_local, int block_m, moe_route_path path, int32_t* sorted_idx,
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
                          int32_t* expert_offset, int32_t* route_slot, void* workspace,
                          size_t ws_bytes, bool pdl, cudaStream_t stream,
-                         uint32_t* zero_ptr = nullptr, int zero_n = 0);
+                         uint32_t* zero_ptr = nullptr, int zero_n = 0, bool skip_pads = false);
 size_t route_workspace_bytes(int R, int E_local, int block_m);
 bool route_single_cta(int R, int E_local, moe_route_path path);
 // The weighted top-k sum done in the down GEMM's epilogue (see GemmArgs in grouped_gemm.cu).
@@ -71,6 +73,8 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
                         unsigned long long* sched = nullptr);
 // Largest route count for which the gate/up GEMM derives its block table itself.
 constexpr int kSelfRouteMaxRoutes = 32;
+// Largest route count route preparation sorts in one warp (AUTO path).
+constexpr int kRouteWarpMaxRoutes = 32;
 int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
                       const int32_t* expert_map, int M, int k, int E, int E_local, int H, void* out,
                       bool pdl, cudaStream_t stream);

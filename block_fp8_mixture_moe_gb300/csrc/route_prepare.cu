@@ -57,6 +57,10 @@ struct RouteArgs {
     uint32_t* zero_ptr;
     int zero_n;
     int compact;  // single CTA with an expert map: compact the kept routes first
+    // The -1 pads of sorted_idx are left to the next kernel (the layer's input quantisation,
+    // spread over every SM): one CTA's scattered pad stores took 1.6 us at 256 experts and
+    // 7 us at 512 on the critical path.  The single-CTA and multi-CTA paths only.
+    int skip_pads;
 };
 
 // Clears the caller's zero region (grid-stride over the launch).
@@ -186,12 +190,14 @@ __device__ void write_metadata(const RouteArgs& p, const int* tot, const int* st
         p.count[e] = tot[e];
         if (p.offset) p.offset[e] = start[e];
         for (int b = start[e] >> p.bm_shift; b < (start[e + 1] >> p.bm_shift); ++b) p.block_expert[b] = e;
-        for (int s = start[e] + tot[e]; s < start[e + 1]; ++s) p.sorted_idx[s] = -1;
+        if (!p.skip_pads)
+            for (int s = start[e] + tot[e]; s < start[e + 1]; ++s) p.sorted_idx[s] = -1;
     }
     for (int b = nb + threadIdx.x; b < p.B_cap; b += blockDim.x) p.block_expert[b] = -1;
-    for (long long s = (static_cast<long long>(nb) << p.bm_shift) + threadIdx.x;
-         s < (static_cast<long long>(p.B_cap) << p.bm_shift); s += blockDim.x)
-        p.sorted_idx[s] = -1;
+    if (!p.skip_pads)
+        for (long long s = (static_cast<long long>(nb) << p.bm_shift) + threadIdx.x;
+             s < (static_cast<long long>(p.B_cap) << p.bm_shift); s += blockDim.x)
+            p.sorted_idx[s] = -1;
     if (threadIdx.x == 0) {
         *p.num_blocks = nb;
         if (p.offset) p.offset[p.E_loc] = start[p.E_loc];
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
 // padded count).  Meanwhile the CTA's other warps write every pad and empty block entry; after
 // the one barrier, each expert's count and padded offset are sums over that table, and the
 // real entries overwrite the pads.
-constexpr int kWarpMaxRoutes = 32;
+constexpr int kWarpMaxRoutes = kRouteWarpMaxRoutes;
 constexpr int kWarpThreads = 256;
 
 // The one-warp sort's table: the active experts of at most 32 routes (local id, route count,
@@ -501,7 +507,7 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
                          int32_t* expert_offset, int32_t* route_slot, void* workspace,
                          size_t ws_bytes, bool pdl, cudaStream_t stream, uint32_t* zero_ptr,
-                         int zero_n) {
+                         int zero_n, bool skip_pads) {
     if (M < 0 || k <= 0 || E <= 0 || E_local <= 0) {
         set_error("moe_route_prepare: need M >= 0, k > 0, E > 0, E_local > 0");
         return MOE_ERR_ARG;
@@ -543,6 +549,7 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
     p.status = device_status_ptr();
     p.zero_ptr = zero_ptr;
     p.zero_n = zero_ptr ? zero_n : 0;
+    p.skip_pads = skip_pads ? 1 : 0;
     if (path == MOE_ROUTE_AUTO && R > 0 && R <= kWarpMaxRoutes) {
         // a handful of routes (decode batches of a few tokens): one warp sorts them
         Launch L(dim3(1), dim3(kWarpThreads), 0, stream, pdl);
