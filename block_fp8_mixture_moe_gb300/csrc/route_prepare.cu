@@ -132,13 +132,19 @@ __device__ __forceinline__ void warp_histogram(const int* loc, int n, int per_wa
                                                uint16_t* row) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int lo = w * per_warp, hi = min(n, lo + per_warp);
-    for (int base = lo; base < hi; base += 32) {
-        const int r = base + lane;
-        const int e = r < hi ? loc[r] : -1;
-        const unsigned m = __match_any_sync(kFull, e);
-        if (e >= 0 && lane == __ffs(m) - 1) row[e] = static_cast<uint16_t>(row[e] + __popc(m));
-        __syncwarp();
+    // One shared-memory atomic per route.  The 16-bit counters are updated through 32-bit
+    // atomics on their word (a warp's count stays below 65536, so no carry reaches the
+    // neighbour).  Grouping equal experts with __match_any_sync first took 3.5 us at 4096 routes
+    // over 512 experts (prefill layer 732.9 -> 730.1 us, decode M=256 254.8 -> 253.1).
+    const uintptr_t rbase = reinterpret_cast<uintptr_t>(row);
+    for (int r = lo + lane; r < hi; r += 32) {
+        const int e = loc[r];
+        if (e >= 0) {
+            const uintptr_t a = rbase + 2u * static_cast<unsigned>(e);
+            atomicAdd(reinterpret_cast<unsigned*>(a & ~static_cast<uintptr_t>(3)), 1u << ((a & 2u) * 8u));
+        }
     }
+    __syncwarp();
 }
 
 // Turns the per-warp histograms [nw][E_loc] into exclusive per-warp starting ranks; stores the
