@@ -50,6 +50,8 @@ struct AQArgs {
     const int32_t* slot_route;
     const int32_t* n_blocks;
     int bm;
+    // nullable: the number of work rows, read on the device (rows is then an upper bound)
+    const int32_t* n_rows;
     int* status;
 };
 
@@ -248,6 +250,10 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
         // back, so its count is read before the wait)
         const long long nb = max(0, __ldcg(p.n_blocks));
         p.rows = static_cast<int>(min(static_cast<long long>(p.rows), nb * p.bm));
+    }
+    if (p.n_rows) {
+        // written by route preparation two or more launches back, so read before the wait
+        p.rows = min(p.rows, max(0, __ldcg(p.n_rows)));
     }
     const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
     long long pair = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
@@ -468,7 +474,8 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
                      const int32_t* row_expert, const int32_t* expert_map, int E,
                      const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
                      float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream,
-                     bool map_early, const int32_t* slot_route, const int32_t* n_blocks, int bm) {
+                     bool map_early, const int32_t* slot_route, const int32_t* n_blocks, int bm,
+                     const int32_t* n_rows) {
     if (!in || !out_q || !out_s) { set_error("silu_mul_quant_fp8: null pointer"); return MOE_ERR_ARG; }
     if (!aligned16(in) || !aligned16(out_q) || (reinterpret_cast<uintptr_t>(out_s) & 3u)) {
         set_error("silu_mul_quant_fp8: in/out_q must be 16-byte aligned, out_s 4-byte aligned");
@@ -524,6 +531,7 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
     p.slot_route = slot_route;
     p.n_blocks = n_blocks;
     p.bm = bm;
+    p.n_rows = n_rows;
     p.status = device_status_ptr();
     bool persistent;
     if (strategy == MOE_QUANT_PER_GROUP) persistent = false;

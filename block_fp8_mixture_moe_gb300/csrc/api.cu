@@ -173,7 +173,7 @@ bool dyn_tail(int M, int k, int E, int E_local, int N_out, int K, int bm) {
 struct Plan {
     int bm, B_cap, slots, R, splits;
     size_t off_sorted, off_bexp, off_nb, off_cnt, off_off, off_rslot, off_rws, off_xq, off_xs,
-        off_gu, off_aq, off_as, off_z, off_sync, off_sched, off_rcnt, total;
+        off_gu, off_aq, off_as, off_z, off_sync, off_sched, off_rcnt, off_kslot, off_nkept, total;
 };
 
 Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int sms) {
@@ -204,6 +204,8 @@ Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int 
     // counters, so that route preparation zeroes both as one range
     P.off_sched = take(kSchedBytes);
     P.off_rcnt = take(sizeof(unsigned) * static_cast<size_t>(M) * (H / 128));
+    P.off_kslot = take(sizeof(int32_t) * P.R);  // slots of the kept routes (compacting route prep)
+    P.off_nkept = take(sizeof(int32_t));
     P.total = o;
     return P;
 }
@@ -378,6 +380,12 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     // it.  Measured on GB300 (interleaved A/B): prefill 733.5 -> 728.3 us, decode M=32 161.7 ->
     // 161.0, smaller sizes unchanged (the one-warp path still writes its own pads).
     const bool defer_pads = P.R > kRouteWarpMaxRoutes;
+    // With an expert map, route preparation's compacting path lists the kept routes' slots, and
+    // the activation kernel walks exactly those rows: at the expert-parallel shape 739 rows
+    // instead of the blocks' 1056 slots, a third of them pads whose loads went for nothing.
+    const bool kept_walk = route_compacts(P.R, E, E_local, expert_map != nullptr);
+    int32_t* kept_slot = reinterpret_cast<int32_t*>(ws + P.off_kslot);
+    int32_t* n_kept = reinterpret_cast<int32_t*>(ws + P.off_nkept);
     const bool dyn_gu = dyn_tail(M, k, E, E_local, 2 * N, H, P.bm);
     const bool dyn_dn = dyn_tail(M, k, E, E_local, H, N, P.bm);
 
@@ -405,7 +413,7 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                               ws + P.off_rws, rws_bytes, false, stream,
                               reinterpret_cast<uint32_t*>(sched),
                               static_cast<int>(kSchedBytes / 4) + (epi_reduce ? M * (H / 128) : 0),
-                              defer_pads);
+                              defer_pads, kept_walk ? kept_slot : nullptr, kept_walk ? n_kept : nullptr);
     if (rc) return rc;
     rc = launch_input_quant_tokens(x, M, H, k, route_slot, P.slots, xq, xs, act_fmt, true, stream,
                                    defer_pads ? offsets : nullptr, counts,
@@ -429,7 +437,11 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     // act-quant walks the routes (through route_slot) or, when the blocks hold fewer slots than
     // there are routes (an expert map that keeps few of them), the slots of the blocks that exist
     const bool slot_rows = expected_blocks(M, k, E, E_local, P.bm) * P.bm < P.R;
-    if (slot_rows)
+    if (kept_walk)
+        rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
+                              nullptr, nullptr, 0, kept_slot, 0, P.slots, aq, as, MOE_QUANT_PERSISTENT,
+                              true, stream, /*map_early=*/true, nullptr, nullptr, 0, n_kept);
+    else if (slot_rows)
         rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.slots, N, clamp_limit, act_fmt,
                               nullptr, nullptr, 0, nullptr, 0, P.slots, aq, as, MOE_QUANT_PERSISTENT,
                               true, stream, false, sorted_idx, num_blocks, P.bm);

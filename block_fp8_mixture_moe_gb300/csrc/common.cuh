@@ -39,7 +39,7 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
                      const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
                      float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream,
                      bool map_early = false, const int32_t* slot_route = nullptr,
-                     const int32_t* n_blocks = nullptr, int bm = 0);
+                     const int32_t* n_blocks = nullptr, int bm = 0, const int32_t* n_rows = nullptr);
 // Per-token input quantisation scattered to the route slots (the layer's first stage).
 int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t* route_slot,
                               int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
@@ -51,7 +51,11 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
                          int32_t* expert_offset, int32_t* route_slot, void* workspace,
                          size_t ws_bytes, bool pdl, cudaStream_t stream,
-                         uint32_t* zero_ptr = nullptr, int zero_n = 0, bool skip_pads = false);
+                         uint32_t* zero_ptr = nullptr, int zero_n = 0, bool skip_pads = false,
+                         int32_t* kept_slot = nullptr, int32_t* n_kept = nullptr);
+// Whether AUTO route preparation takes its compacting single-CTA path (which alone writes the
+// kept-slot list and count).
+bool route_compacts(int R, int E, int E_local, bool map);
 size_t route_workspace_bytes(int R, int E_local, int block_m);
 bool route_single_cta(int R, int E_local, moe_route_path path);
 // The weighted top-k sum done in the down GEMM's epilogue (see GemmArgs in grouped_gemm.cu).

@@ -31,6 +31,8 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kSingleWarps = 32;
 constexpr int kSingleMaxRoutes = 8192;
+// the compacting single-CTA variant when its shared memory fits comfortably
+constexpr size_t kCompactMaxSmem = 200 * 1024;
 constexpr int kSingleMaxExperts = 2048;
 constexpr int kMaxExperts = 4096;
 constexpr size_t kMultiHistBytes = 96 * 1024;  // per-warp histogram budget of a scatter CTA
@@ -61,6 +63,11 @@ struct RouteArgs {
     // spread over every SM): one CTA's scattered pad stores took 1.6 us at 256 experts and
     // 7 us at 512 on the critical path.  The single-CTA and multi-CTA paths only.
     int skip_pads;
+    // With the compaction (single CTA, expert map): the slot of each kept route in route order
+    // and their number, so that the layer's activation kernel walks the kept routes only
+    // (nullable; written only by the compacting path).
+    int32_t* kept_slot;
+    int32_t* n_kept;
 };
 
 // Clears the caller's zero region (grid-stride over the launch).
@@ -200,6 +207,7 @@ __device__ __forceinline__ void warp_scatter(const RouteArgs& p, const int* loc,
             if (chunk_base) slot += chunk_base[e];
             p.sorted_idx[slot] = route;
             if (p.route_slot) p.route_slot[route] = slot;
+            if (ridx && p.kept_slot) p.kept_slot[r] = slot;
         } else if (r < hi && p.route_slot) {
             p.route_slot[route] = -1;
         }
@@ -312,6 +320,7 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
             if (loc[r] >= 0) { kloc[pos] = loc[r]; kidx[pos] = r; ++pos; }
         }
         n = tmp[32];
+        if (threadIdx.x == 0 && p.n_kept) *p.n_kept = n;
         key = kloc;
         ridx = kidx;
         __syncthreads();
@@ -521,6 +530,11 @@ bool route_single_cta(int R, int E_local, moe_route_path path) {
     return R <= kSingleMaxRoutes && E_local <= 512;
 }
 
+bool route_compacts(int R, int E, int E_local, bool map) {
+    return map && R > kWarpMaxRoutes && route_single_cta(R, E_local, MOE_ROUTE_AUTO) &&
+           single_smem_bytes(R, E, E_local, true) <= kCompactMaxSmem;
+}
+
 size_t route_workspace_bytes(int R, int E_local, int block_m) {
     (void)block_m;
     const int chunk = multi_warps(E_local) * 32;
@@ -534,7 +548,7 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
                          int32_t* expert_offset, int32_t* route_slot, void* workspace,
                          size_t ws_bytes, bool pdl, cudaStream_t stream, uint32_t* zero_ptr,
-                         int zero_n, bool skip_pads) {
+                         int zero_n, bool skip_pads, int32_t* kept_slot, int32_t* n_kept) {
     if (M < 0 || k <= 0 || E <= 0 || E_local <= 0) {
         set_error("moe_route_prepare: need M >= 0, k > 0, E > 0, E_local > 0");
         return MOE_ERR_ARG;
@@ -577,6 +591,8 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
     p.zero_ptr = zero_ptr;
     p.zero_n = zero_ptr ? zero_n : 0;
     p.skip_pads = skip_pads ? 1 : 0;
+    p.kept_slot = kept_slot;
+    p.n_kept = n_kept;
     if (path == MOE_ROUTE_AUTO && R > 0 && R <= kWarpMaxRoutes) {
         // a handful of routes (decode batches of a few tokens): one warp sorts them
         Launch L(dim3(1), dim3(kWarpThreads), 0, stream, pdl);
@@ -592,7 +608,7 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
             return MOE_ERR_ARG;
         }
         // with an expert map, the compacting variant when its shared memory fits comfortably
-        p.compact = expert_map && single_smem_bytes(R, E, E_local, true) <= 200 * 1024 ? 1 : 0;
+        p.compact = expert_map && single_smem_bytes(R, E, E_local, true) <= kCompactMaxSmem ? 1 : 0;
         const size_t smem = single_smem_bytes(R, E, E_local, p.compact != 0);
         if (!ensure_smem(reinterpret_cast<const void*>(k_route_single), static_cast<int>(smem))) {
             set_error("route single: shared-memory limit %zu refused", smem);
