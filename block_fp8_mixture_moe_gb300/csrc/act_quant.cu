@@ -417,7 +417,10 @@ __global__ void __launch_bounds__(256) k_silu_and_mul(const uint16_t* in, int ro
 
 template <int ACT, bool F32IN, int KG, bool INL>
 int launch_aq_grid(const AQArgs& p, long long pairs, bool persistent, bool pdl, cudaStream_t stream) {
-    const int threads = 256, wpb = threads / 32;
+    // Few pairs (decode batches): CTAs of two warps, one pair a warp.  Each is small enough in
+    // registers to become resident beside a grouped-GEMM CTA, so the down GEMM's CTAs, launched
+    // early, do not wait for an act-quant CTA to leave their SM.
+    const int threads = persistent && pairs <= 2LL * sm_count() ? 64 : 256, wpb = threads / 32;
     long long blocks = (pairs + wpb - 1) / wpb;
     const size_t smem = persistent && p.map_smem ? static_cast<size_t>(p.E) * 4 : 0;
     if (persistent) {
