@@ -417,10 +417,13 @@ __global__ void __launch_bounds__(256) k_silu_and_mul(const uint16_t* in, int ro
 
 template <int ACT, bool F32IN, int KG, bool INL>
 int launch_aq_grid(const AQArgs& p, long long pairs, bool persistent, bool pdl, cudaStream_t stream) {
-    // Few pairs (decode batches): CTAs of two warps, one pair a warp.  Each is small enough in
-    // registers to become resident beside a grouped-GEMM CTA, so the down GEMM's CTAs, launched
-    // early, do not wait for an act-quant CTA to leave their SM.
-    const int threads = persistent && pairs <= 2LL * sm_count() ? 64 : 256, wpb = threads / 32;
+    // Few pairs (decode batches): one-warp CTAs, one pair each.  A grouped-GEMM CTA (11 warps of
+    // ~144 registers, spread over the SM's four schedulers and their register files) leaves room
+    // beside it for one more warp, not two, so a one-warp CTA becomes resident next to a running
+    // GEMM CTA.  The act-quant is then in place before the gate/up GEMM ends, and no down-GEMM CTA
+    // waits for an act-quant CTA to leave its SM.  Measured on GB300 against two-warp CTAs (which
+    // started only as GEMM CTAs left): decode M=2 to 8 ~1.8 us faster, M=16 and 32 ~0.8 us.
+    const int threads = persistent && pairs <= 2LL * sm_count() ? 32 : 256, wpb = threads / 32;
     long long blocks = (pairs + wpb - 1) / wpb;
     const size_t smem = persistent && p.map_smem ? static_cast<size_t>(p.E) * 4 : 0;
     if (persistent) {
