@@ -189,7 +189,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
     const bool slot_walk = p.slot_route && !p.row_expert && !p.row_map;
     int route = 0;
     if (active) {
-        const int w = static_cast<int>(item / p.G);
+        const int w = static_cast<int>(static_cast<unsigned>(item) / static_cast<unsigned>(p.G));
         g = static_cast<int>(item - static_cast<long long>(w) * p.G);
         if (slot_walk) {
             in_row = row = w;
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     const long long items = static_cast<long long>(p.rows) * p.G;
     auto sel_of = [&](long long pr) -> int {
         const long long item = pr * 2 + (lane >> 4);
-        return (pr < pairs && item < items) ? __ldcg(sel + item / p.G) : -1;
+        return (pr < pairs && item < items) ? __ldcg(sel + static_cast<unsigned>(item) / static_cast<unsigned>(p.G)) : -1;
     };
     // the first pair's selector before the wait, when it is an input or was written two or
     // more launches back; with an expert filter the (caller's) expert map is staged in shared
@@ -456,6 +456,12 @@ template <int ACT, bool F32IN, int KG>
 int launch_aq_kg(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream) {
     const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
     if (pairs == 0) return MOE_OK;
+    // the kernel divides group indices in 32 bits (a 64-bit division is a long software
+    // sequence on the path from the dependency wait to a pair's loads)
+    if (static_cast<long long>(p.rows) * p.G >= (1LL << 31)) {
+        set_error("act_quant: rows * N / 128 must be below 2^31");
+        return MOE_ERR_ARG;
+    }
     if constexpr (ACT != MOE_ACT_IDENTITY) {
         if (pairs <= kInlinePairs) return launch_aq_grid<ACT, F32IN, KG, true>(p, pairs, persistent, pdl, stream);
     }

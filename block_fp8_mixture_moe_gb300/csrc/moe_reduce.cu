@@ -66,12 +66,12 @@ __global__ void __launch_bounds__(kThreads) k_moe_reduce(const uint16_t* __restr
     unsigned keep = 0;
     int t = -1;
     if (it < items) {
-        t = static_cast<int>(it / chunks);
+        t = static_cast<int>(static_cast<unsigned>(it) / static_cast<unsigned>(chunks));
         keep = token_routes(ids, w, map, t, k, E, E_local, lane, &wl);
     }
     grid_dep_wait();  // the expert outputs z are the previous kernel's
     for (; it < items; it += stride) {
-        const int tt = static_cast<int>(it / chunks);
+        const int tt = static_cast<int>(static_cast<unsigned>(it) / static_cast<unsigned>(chunks));
         if (tt != t) {
             t = tt;
             keep = token_routes(ids, w, map, t, k, E, E_local, lane, &wl);
@@ -139,6 +139,8 @@ int launch_moe_reduce(const void* z, const float* topk_w, const int32_t* topk_id
     if (k > kMaxTopk) { set_error("moe_reduce: top-k above %d is not supported", kMaxTopk); return MOE_ERR_ARG; }
     const long long items = static_cast<long long>(M) * ((H + 255) / 256);
     if (items == 0) return MOE_OK;
+    // item indices are divided in 32 bits in the kernel
+    if (items >= (1LL << 31)) { set_error("moe_reduce: M * H / 256 must be below 2^31"); return MOE_ERR_ARG; }
     if (!z || !topk_w || !topk_ids || !out) { set_error("moe_reduce: null pointer"); return MOE_ERR_ARG; }
     if (!aligned16(z) || !aligned16(out)) { set_error("moe_reduce: z and out must be 16-byte aligned"); return MOE_ERR_ARG; }
     // Few items (decode batches of a few tokens): one item per warp in CTAs of two warps, one

@@ -217,7 +217,7 @@ MOEFP8_API int moe_blockfp8_pack_weights(const uint8_t* w_q, int E_local, int N_
  * decode without a filter), PERSISTENT a grid-stride kernel of as many CTAs as are resident at
  * once; AUTO picks
  * PER_GROUP when there is no filter or map and rows*N < 2^20.
- * N multiple of 128; in and out_q 16-byte aligned.
+ * N multiple of 128; rows * N/128 < 2^31; in and out_q 16-byte aligned.
  * ------------------------------------------------------------------------------------------ */
 MOEFP8_API int silu_mul_quant_fp8(moe_act act, const void* in, moe_dtype in_dtype, int in_splits,
                        int in_rows, int rows, int N, float clamp_limit, moe_scale_fmt fmt,
@@ -244,7 +244,7 @@ MOEFP8_API int silu_and_mul_bf16(moe_act act, const void* in, int rows, int N, f
  * entry for which route preparation gave the route no slot).
  *   z [M*k, H] bf16 (route order); topk_w [M, k] f32; topk_ids [M, k] int32;
  *   expert_map nullable [E] (without it E_local must equal E); out [M, H] bf16.  H multiple
- *   of 8, k <= 32; pointers 16-byte aligned.
+ *   of 8, k <= 32, M * ceil(H/256) < 2^31; pointers 16-byte aligned.
  * ------------------------------------------------------------------------------------------ */
 MOEFP8_API int moe_reduce(const void* z, const float* topk_w, const int32_t* topk_ids,
                const int32_t* expert_map, int M, int k, int E, int E_local, int H, void* out,
