@@ -177,6 +177,64 @@ __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, 
     return true;
 }
 
+// The gate and up inputs of one lane, 4 values each, from fp32 split-K partials (the layer's
+// few-item shape below): the same loads in flight together and additions in split order as
+// load_gate_up.
+template <int KG>
+__device__ __forceinline__ void load_gate_up4(const AQArgs& p, long long off_g, long long off_u,
+                                              float* g, float* u) {
+    const float* bg = static_cast<const float*>(p.in) + off_g;
+    const float* bu = static_cast<const float*>(p.in) + off_u;
+    for (int s0 = 0; s0 < p.in_splits; s0 += KG) {
+        float4 cg[KG], cu[KG];
+#pragma unroll
+        for (int t = 0; t < KG; ++t) {
+            if (s0 + t < p.in_splits) {
+                const long long so = static_cast<long long>(s0 + t) * p.split_stride;
+                cg[t] = __ldg(reinterpret_cast<const float4*>(bg + so));
+                cu[t] = __ldg(reinterpret_cast<const float4*>(bu + so));
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < KG; ++t) {
+            if (s0 + t < p.in_splits) {
+                const float vg[4] = {cg[t].x, cg[t].y, cg[t].z, cg[t].w};
+                const float vu[4] = {cu[t].x, cu[t].y, cu[t].z, cu[t].w};
+                if (s0 + t == 0) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) { g[i] = vg[i]; u[i] = vu[i]; }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) { g[i] = __fadd_rn(g[i], vg[i]); u[i] = __fadd_rn(u[i], vu[i]); }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { g[i] = bf16_round_f32(g[i]); u[i] = bf16_round_f32(u[i]); }
+}
+
+// quant_group_codes for a group spread over a whole warp, 4 values a lane (same scale rule and
+// quantiser); the 4 codes of a lane come back in one word, lowest column in the low byte.
+__device__ __forceinline__ void quant_group_codes4(const float* a, bool active, int fmt,
+                                                   uint32_t* codes, float* scale) {
+    float amax = 0.0f;
+    if (active) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(a[i]));
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    if (active) {
+        const float s = group_scale(amax, fmt);
+        const float inv = fmt == MOE_SCALE_UE8M0 ? pow2_reciprocal(s) : 0.0f;
+        const uint32_t c0 = cvt_e4m3x2(quant_div(a[0], s, inv, fmt), quant_div(a[1], s, inv, fmt));
+        const uint32_t c1 = cvt_e4m3x2(quant_div(a[2], s, inv, fmt), quant_div(a[3], s, inv, fmt));
+        *codes = c0 | (c1 << 16);
+        *scale = s;
+    }
+}
+
 template <int ACT, bool F32IN, int KG, bool INL>
 __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int lane, int pre = -2,
                                            const int* smap = nullptr) {
@@ -240,7 +298,58 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
     }
 }
 
-template <int ACT, bool F32IN, bool PERSISTENT, int KG, bool INL>
+// One (row, 128-column group) item with a whole warp, 4 values a lane: the work row and its
+// selector as in quant_pair, SiLU*mul inlined.  Per lane it is half of quant_pair's chain of
+// loads, SiLU and quantisation, which shortens the layer's act-quant where one warp per SM does
+// the work (decode batches); where the SMs are full of warps (expert-parallel and prefill
+// shapes) the per-item overhead over 4 values instead of 8 makes it slower, so the launcher
+// takes it only for few items.
+template <int ACT, int KG>
+__device__ __forceinline__ void quant_item4(const AQArgs& p, long long item, int lane, int pre,
+                                            const int* smap) {
+    bool active = item < static_cast<long long>(p.rows) * p.G;
+    int row = 0, g = 0, in_row = 0;
+    const bool slot_walk = p.slot_route && !p.row_expert && !p.row_map;
+    int route = 0;
+    if (active) {
+        const int w = static_cast<int>(static_cast<unsigned>(item) / static_cast<unsigned>(p.G));
+        g = static_cast<int>(item - static_cast<long long>(w) * p.G);
+        if (slot_walk) {
+            in_row = row = w;
+            if (w >= p.in_rows || w >= p.out_rows) {
+                if (p.status) atomicOr(p.status, MOE_DEV_BAD_INDEX);
+                active = false;
+            } else {
+                route = __ldcg(p.slot_route + w);
+            }
+        } else {
+            active = row_source(p, w, &in_row, &row, pre, smap);
+        }
+    }
+    float a[4];
+    if (active) {
+        const long long col = static_cast<long long>(g) * 128 + lane * 4;
+        const long long rbase = static_cast<long long>(in_row) * p.W;
+        float gv[4], uv[4];
+        load_gate_up4<KG>(p, rbase + col, rbase + p.N + col, gv, uv);
+        if (slot_walk && route < 0) active = false;  // a pad slot
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = silu_mul_bf16<ACT>(gv[i], uv[i], p.L);
+        }
+    }
+    uint32_t codes;
+    float sc;
+    quant_group_codes4(a, active, p.fmt, &codes, &sc);
+    if (active) {
+        const long long o = static_cast<long long>(row) * p.N + static_cast<long long>(g) * 128 + lane * 4;
+        *reinterpret_cast<uint32_t*>(p.out_q + o) = codes;
+        if (lane == 0) p.out_s[static_cast<long long>(row) * p.G + g] = sc;
+    }
+}
+
+// W4: one group per warp (quant_item4) instead of one per half-warp (quant_pair).
+template <int ACT, bool F32IN, bool PERSISTENT, int KG, bool INL, bool W4 = false>
 __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     extern __shared__ int aq_smap[];  // the expert map, when p.map_smem
     const int lane = threadIdx.x & 31;
@@ -255,13 +364,14 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
         // written by route preparation two or more launches back, so read before the wait
         p.rows = min(p.rows, max(0, __ldcg(p.n_rows)));
     }
-    const long long pairs = (static_cast<long long>(p.rows) * p.G + 1) / 2;
+    // a warp's work unit: a pair of groups, or one group with W4
+    const long long items = static_cast<long long>(p.rows) * p.G;
+    const long long pairs = W4 ? items : (items + 1) / 2;
     long long pair = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
     // a row's first selector: its expert id (a caller input) or its row-map entry
     const int32_t* sel = p.row_expert ? p.row_expert : p.row_map;
-    const long long items = static_cast<long long>(p.rows) * p.G;
     auto sel_of = [&](long long pr) -> int {
-        const long long item = pr * 2 + (lane >> 4);
+        const long long item = W4 ? pr : pr * 2 + (lane >> 4);
         return (pr < pairs && item < items) ? __ldcg(sel + static_cast<unsigned>(item) / static_cast<unsigned>(p.G)) : -1;
     };
     // the first pair's selector before the wait, when it is an input or was written two or
@@ -289,7 +399,10 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     if (ahead && cur == -2) cur = sel_of(pair);
     for (; pair < pairs; pair += stride) {
         const int nxt = ahead ? sel_of(pair + stride) : -2;
-        quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, ahead ? cur : -2, smap);
+        if constexpr (W4)
+            quant_item4<ACT, KG>(p, pair, lane, ahead ? cur : -2, smap);
+        else
+            quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, ahead ? cur : -2, smap);
         cur = nxt;
     }
 }
@@ -415,21 +528,22 @@ __global__ void __launch_bounds__(256) k_silu_and_mul(const uint16_t* in, int ro
     }
 }
 
-template <int ACT, bool F32IN, int KG, bool INL>
-int launch_aq_grid(const AQArgs& p, long long pairs, bool persistent, bool pdl, cudaStream_t stream) {
-    // Few pairs (decode batches): one-warp CTAs, one pair each.  A grouped-GEMM CTA (11 warps of
+// `units`: work units of the kernel, group pairs, or groups with W4 (persistent only).
+template <int ACT, bool F32IN, int KG, bool INL, bool W4 = false>
+int launch_aq_grid(const AQArgs& p, long long units, bool persistent, bool pdl, cudaStream_t stream) {
+    // Few units (decode batches): one-warp CTAs, one unit each.  A grouped-GEMM CTA (11 warps of
     // ~144 registers, spread over the SM's four schedulers and their register files) leaves room
     // beside it for one more warp, not two, so a one-warp CTA becomes resident next to a running
     // GEMM CTA.  The act-quant is then in place before the gate/up GEMM ends, and no down-GEMM CTA
     // waits for an act-quant CTA to leave its SM.  Measured on GB300 against two-warp CTAs (which
     // started only as GEMM CTAs left): decode M=2 to 8 ~1.8 us faster, M=16 and 32 ~0.8 us.
-    const int threads = persistent && pairs <= 2LL * sm_count() ? 32 : 256, wpb = threads / 32;
-    long long blocks = (pairs + wpb - 1) / wpb;
+    const int threads = persistent && units <= (W4 ? 4LL : 2LL) * sm_count() ? 32 : 256, wpb = threads / 32;
+    long long blocks = (units + wpb - 1) / wpb;
     const size_t smem = persistent && p.map_smem ? static_cast<size_t>(p.E) * 4 : 0;
     if (persistent) {
         // as many CTAs as are resident at once, so the grid runs in one wave
         int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_act_quant<ACT, F32IN, true, KG, INL>, threads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_act_quant<ACT, F32IN, true, KG, INL, W4>, threads,
                                                           smem) != cudaSuccess || occ < 1)
             occ = 1;
         long long cap = static_cast<long long>(sm_count()) * occ;
@@ -437,8 +551,12 @@ int launch_aq_grid(const AQArgs& p, long long pairs, bool persistent, bool pdl, 
     }
     if (blocks > 0x7FFFFFFFLL) { set_error("act_quant: too many groups"); return MOE_ERR_ARG; }
     Launch L(dim3(static_cast<unsigned>(blocks)), dim3(threads), smem, stream, pdl);
-    cudaError_t e = persistent ? cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, true, KG, INL>, p)
-                               : cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, false, KG, INL>, p);
+    cudaError_t e;
+    if constexpr (W4)
+        e = cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, true, KG, INL, true>, p);
+    else
+        e = persistent ? cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, true, KG, INL>, p)
+                       : cudaLaunchKernelEx(&L.cfg, k_act_quant<ACT, F32IN, false, KG, INL>, p);
     if (e != cudaSuccess) {
         set_error("act_quant launch: %s", cudaGetErrorString(e));
         return MOE_ERR_LAUNCH;
@@ -461,6 +579,15 @@ int launch_aq_kg(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream
     if (static_cast<long long>(p.rows) * p.G >= (1LL << 31)) {
         set_error("act_quant: rows * N / 128 must be below 2^31");
         return MOE_ERR_ARG;
+    }
+    if constexpr (ACT != MOE_ACT_IDENTITY && F32IN && KG <= 4) {
+        // Few groups of split partials (decode batches): one group per warp (quant_item4).
+        // Measured on GB300 against group pairs, graph-replayed layer, interleaved A/B: decode
+        // M=1 33.4 -> 32.7 us, M=16 113.2 -> 112.0, M=32 161.9 -> 160.8.  With 8 splits (M=2 to 8)
+        // it measured no faster, and with many groups (expert-parallel, prefill) 2-2.5 us slower.
+        const long long items = static_cast<long long>(p.rows) * p.G;
+        if (persistent && items <= 4LL * sm_count())
+            return launch_aq_grid<ACT, F32IN, KG, true, true>(p, items, persistent, pdl, stream);
     }
     if constexpr (ACT != MOE_ACT_IDENTITY) {
         if (pairs <= kInlinePairs) return launch_aq_grid<ACT, F32IN, KG, true>(p, pairs, persistent, pdl, stream);
