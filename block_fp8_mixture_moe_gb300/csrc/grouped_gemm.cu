@@ -338,11 +338,18 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
             }
         }
         // this CTA's static range: an equal share of the units, or, with the dynamic tail, an
-        // equal share of three quarters of them; the rest [dyn_base, units) is handed out
+        // equal share of at most three quarters of them in whole blocks; the rest
+        // [dyn_base, units) is handed out.  Whole blocks start every CTA's range at tile 0 of a
+        // block, so at any moment the CTAs stream the same tile index of their blocks, and the
+        // blocks of a hot expert share each weight tile through L2 instead of re-reading it.
+        // Measured on GB300 at the Zipf prefill shape (ncu DRAM bytes, one launch each):
+        // gate/up 3.01 -> 2.84 GB, down 1.49 -> 1.39 GB; the layer 726 -> 711 us.
         const long long units = static_cast<long long>(nblk) * p.NT * p.splits;
         long long dyn_base = units;
         if (DYN) {
-            const long long share = units * 3 / (4LL * gridDim.x);
+            long long share = units * 3 / (4LL * gridDim.x);
+            const long long per_block = static_cast<long long>(p.NT) * p.splits;
+            if (share >= per_block) share -= share % per_block;
             dyn_base = share * gridDim.x;
             seek(share * blockIdx.x);
             left = share;
