@@ -93,7 +93,10 @@ struct GemmArgs {
 // Weight bytes of one chunk of the dynamic tail.  Measured on the Zipf prefill layer: 32 and
 // 64 KB 760-765 us, 128 KB 741 us, 256 KB 745 us, 512 KB 750 us (its down GEMM's 96 KB units
 // then go two to a chunk and a descriptor).
-constexpr long long kSchedChunkBytes = 128 * 1024;
+// Measured on GB300 at the Zipf prefill shape (the down GEMM's 96 KB units; the gate/up GEMM's
+// 512 KB units always go one to a chunk): chunks of 1 / 2 / 3 / 4 / 5 units gave 757 / 712.9 /
+// 713.8 / 710.9 / 720.6 us for the layer, the best at 4 units, which divide its 32-tile blocks.
+constexpr long long kSchedChunkBytes = 384 * 1024;
 
 template <int BM>
 struct Cfg {
@@ -1003,10 +1006,15 @@ int launch_grouped_gemm(moe_proj proj, const uint8_t* a_q, const float* a_s, int
     }
     if (sched) {
         // dynamic chunks of about kSchedChunkBytes of weights: a short tail, and few enough
-        // descriptors that the metadata warp keeps ahead of the producer
+        // descriptors that the metadata warp keeps ahead of the producer.  The chunk's unit count
+        // divides a block's (tiles x splits), so that no chunk straddles two blocks (each block a
+        // chunk touches costs its expert and rows, and a new descriptor run).
         const long long unit_bytes = static_cast<long long>((KB + splits - 1) / splits) * 128 * 128;
+        const long long per_block = static_cast<long long>(N_out / 128) * splits;
+        long long chunk = std::max(1LL, (kSchedChunkBytes + unit_bytes - 1) / unit_bytes);
+        while (chunk > 1 && per_block % chunk != 0) --chunk;
         p.sched = sched;
-        p.sched_chunk = static_cast<int>(std::max(1LL, (kSchedChunkBytes + unit_bytes - 1) / unit_bytes));
+        p.sched_chunk = static_cast<int>(chunk);
     }
     const long long max_units = static_cast<long long>(B_cap) * p.NT * splits;
     switch (block_m) {
