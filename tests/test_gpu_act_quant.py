@@ -126,6 +126,50 @@ def test_fp32_split_partials_input(ops, splits):
     assert (q.cpu().numpy() == rq).all() and (s.cpu().numpy() == rs).all()
 
 
+def _split_sum_bf16(P):
+    """bf16 bits of the split partials summed in split order with fp32 adds (torch)."""
+    acc = torch.from_numpy(P[0].copy())
+    for i in range(1, P.shape[0]):
+        acc = acc + torch.from_numpy(P[i])
+    return acc.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("rows", [40, 700])
+@pytest.mark.parametrize("act,clamp,fmt", [(1, float("inf"), 0), (1, 7.0, 1), (2, 7.0, 0), (2, float("inf"), 1)])
+@pytest.mark.parametrize("splits", [1, 3, 4, 6])
+def test_persistent_split_partials(ops, splits, act, clamp, fmt, rows):
+    """The persistent launch on split-K partials, as the layer runs it.  At most 4 splits with
+    few groups (40 rows of width 256: 80 groups) take one 128-column group per warp, 4 values a
+    lane; 6 splits or 1400 groups take the group pairs.  Both bitwise against the oracle."""
+    N = 256
+    r = np.random.default_rng(1000 * splits + rows + 10 * act + fmt)
+    P = (r.standard_normal((splits, rows, 2 * N)) * 1.5).astype(np.float32)
+    q, s = ops.silu_mul_quant_fp8(act, to_dev(P), N, in_splits=splits, clamp_limit=clamp, fmt=fmt,
+                                  strategy=ops.QUANT_PERSISTENT)
+    rq, rs = oracle.act_quant(act, _split_sum_bf16(P), N, clamp_limit=clamp, fmt=fmt)
+    assert (q.cpu().numpy() == rq).all() and (s.cpu().numpy() == rs).all()
+
+
+@pytest.mark.parametrize("splits", [2, 4, 7])
+def test_persistent_split_partials_row_map(ops, splits):
+    """The layer's route walk on split partials: work row i writes slot row_map[i] from the
+    same slot's partials; dropped routes (-1) and slots no route maps to stay untouched."""
+    N, slots, R = 512, 96, 60
+    r = np.random.default_rng(splits)
+    P = (r.standard_normal((splits, slots, 2 * N)) * 1.5).astype(np.float32)
+    row_map = r.permutation(slots)[:R].astype(np.int32)
+    row_map[[3, 17, 40]] = -1
+    q, s = ops.silu_mul_quant_fp8(1, to_dev(P), N, rows=R, row_map=to_dev(row_map), row_div=0,
+                                  out_rows=slots, in_splits=splits, clamp_limit=7.0, fmt=1,
+                                  strategy=ops.QUANT_PERSISTENT)
+    rq, rs = oracle.act_quant(1, _split_sum_bf16(P), N, clamp_limit=7.0, fmt=1)
+    q, s = q.cpu().numpy(), s.cpu().numpy()
+    kept = np.zeros(slots, dtype=bool)
+    kept[row_map[row_map >= 0]] = True
+    assert (q[kept] == rq[kept]).all() and (s[kept] == rs[kept]).all()
+    assert (q[~kept] == 0).all() and (s[~kept] == 0).all()
+
+
 def test_row_map_gather_and_mask(ops):
     """Slot-order gathering as the layer uses it: work row = route r, output row = slot of r,
     input row = r // k (gather) or the slot itself (mask)."""
