@@ -6,14 +6,14 @@
 // parallel path otherwise; outputs are the sorted route indices and the compact blocks.  The
 // review on that page asks that the local-expert slice and block_m be checked before launch.
 //
-// Single CTA (1024 threads = 32 warps).  Every route's local expert goes to shared memory.
-// Warp w owns a contiguous chunk of routes and counts it into its own row of a per-warp
-// histogram [32][E_local] (uint16): 32 routes at a time, __match_any_sync groups lanes with the
-// same expert and the group's lowest lane adds the group size -- no atomics, so the result is
-// deterministic.  A column scan over the 32 rows turns the histogram into per-warp starting
-// ranks; a block scan over the block_m-padded expert totals gives each expert's first slot.
-// The scatter repeats the warp walk: slot = expert start + warp rank + rank inside the 32-route
-// group, so the order inside an expert is the route order (stable).
+// Single CTA (8, 16 or 32 warps, by route count).  Every route's local expert goes to shared
+// memory.  Warp w owns a contiguous chunk of routes and counts it into its own row of a
+// per-warp histogram [warps][E_local] (uint16), one shared-memory atomic per route (counts do
+// not depend on the atomics' order).  A column scan over the rows turns the histogram into
+// per-warp starting ranks; a block scan over the block_m-padded expert totals gives each
+// expert's first slot.  The scatter walks each warp's chunk again, 32 routes at a time:
+// __match_any_sync groups the lanes of one expert, and slot = expert start + warp rank + rank
+// inside the group, so the order inside an expert is the route order (stable).
 //
 // Multi CTA.  Kernel 1: each CTA histograms one chunk of routes (shared-memory atomics; counts
 // only) into the workspace; the CTA that finishes last (atomic ticket, no waiting) scans the
@@ -240,17 +240,18 @@ __device__ void write_metadata(const RouteArgs& p, const int* tot, const int* st
 }
 
 // Shared memory of the single-CTA kernel: loc[R] | start[E_loc+1] | tot[E_loc] | tmp[33] |
-// wcnt[32][E_loc] (uint16), and with an expert map also smap[E] | kloc[R] | kidx[R].
+// wcnt[warps][E_loc] (uint16), and with an expert map also smap[E] | kloc[R] | kidx[R].
 __host__ __device__ inline size_t single_ints(int R, int E_loc) {
     const size_t ints = static_cast<size_t>(R) + (E_loc + 1) + E_loc + 33;
     return (ints + 3) & ~static_cast<size_t>(3);
 }
-size_t single_smem_bytes(int R, int E, int E_loc, bool map) {
-    const size_t base = single_ints(R, E_loc) * 4 + static_cast<size_t>(kSingleWarps) * E_loc * 2;
+size_t single_smem_bytes(int R, int E, int E_loc, bool map, int warps = kSingleWarps) {
+    const size_t base = single_ints(R, E_loc) * 4 + static_cast<size_t>(warps) * E_loc * 2;
     return map ? ((base + 15) & ~static_cast<size_t>(15)) + (static_cast<size_t>(E) + 2 * R) * 4 : base;
 }
 
-__global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
+template <int W>
+__global__ void __launch_bounds__(W * 32, 1) k_route_single(RouteArgs p) {
     extern __shared__ __align__(16) int sm[];
     int* loc = sm;
     int* start = loc + p.R;
@@ -270,12 +271,12 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
         // expert costs no second dependent global load, and the kept routes are compacted in
         // route order (a block scan) before the sort, which then walks only them.
         int* smap = reinterpret_cast<int*>(
-            (reinterpret_cast<uintptr_t>(wcnt + kSingleWarps * p.E_loc) + 15) & ~static_cast<uintptr_t>(15));
+            (reinterpret_cast<uintptr_t>(wcnt + W * p.E_loc) + 15) & ~static_cast<uintptr_t>(15));
         int* kloc = smap + p.E;
         int* kidx = kloc + p.R;
         for (int i = threadIdx.x; i < p.E; i += blockDim.x) smap[i] = __ldg(p.map + i);
         load_ids_batched(p, loc);
-        for (int i = threadIdx.x; i < kSingleWarps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
+        for (int i = threadIdx.x; i < W * p.E_loc; i += blockDim.x) wcnt[i] = 0;
         __syncthreads();
         for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
             const int id = loc[r];
@@ -326,14 +327,14 @@ __global__ void __launch_bounds__(1024, 1) k_route_single(RouteArgs p) {
         __syncthreads();
     } else {
         for (int r = threadIdx.x; r < p.R; r += blockDim.x) loc[r] = local_of(p, r);
-        for (int i = threadIdx.x; i < kSingleWarps * p.E_loc; i += blockDim.x) wcnt[i] = 0;
+        for (int i = threadIdx.x; i < W * p.E_loc; i += blockDim.x) wcnt[i] = 0;
         __syncthreads();
     }
-    const int per_warp = (n + kSingleWarps - 1) / kSingleWarps;
+    const int per_warp = (n + W - 1) / W;
     uint16_t* row = wcnt + (threadIdx.x >> 5) * p.E_loc;
     warp_histogram(key, n, per_warp, row);
     __syncthreads();
-    column_scan(wcnt, kSingleWarps, p.E_loc, tot);
+    column_scan(wcnt, W, p.E_loc, tot);
     __syncthreads();
     for (int e = threadIdx.x; e < p.E_loc; e += blockDim.x)
         start[e] = ((tot[e] + p.bm - 1) >> p.bm_shift) << p.bm_shift;
@@ -609,13 +610,24 @@ int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int
         }
         // with an expert map, the compacting variant when its shared memory fits comfortably
         p.compact = expert_map && single_smem_bytes(R, E, E_local, true) <= kCompactMaxSmem ? 1 : 0;
-        const size_t smem = single_smem_bytes(R, E, E_local, p.compact != 0);
-        if (!ensure_smem(reinterpret_cast<const void*>(k_route_single), static_cast<int>(smem))) {
+        // Fewer warps for fewer routes: the per-warp histograms, their per-expert column scan
+        // and every CTA barrier shrink with the warp count.  Measured on GB300 (graph-replayed
+        // layer, interleaved A/B) against 32 warps: decode M=8 -0.9 us, M=16 -1.7, M=32 -1.2 with
+        // 8 warps up to 256 routes; M=64 -1.2 with 16 up to 512; 4 warps up to 128 routes were
+        // slower than 8.
+        const int W = R <= 256 ? 8 : R <= 512 ? 16 : kSingleWarps;
+        const size_t smem = single_smem_bytes(R, E, E_local, p.compact != 0, W);
+        const void* kfn = W == 8 ? reinterpret_cast<const void*>(k_route_single<8>)
+                        : W == 16 ? reinterpret_cast<const void*>(k_route_single<16>)
+                                  : reinterpret_cast<const void*>(k_route_single<kSingleWarps>);
+        if (!ensure_smem(kfn, static_cast<int>(smem))) {
             set_error("route single: shared-memory limit %zu refused", smem);
             return MOE_ERR_LAUNCH;
         }
-        Launch L(dim3(1), dim3(1024), smem, stream, pdl);
-        cudaError_t e = cudaLaunchKernelEx(&L.cfg, k_route_single, p);
+        Launch L(dim3(1), dim3(W * 32), smem, stream, pdl);
+        cudaError_t e = W == 8 ? cudaLaunchKernelEx(&L.cfg, k_route_single<8>, p)
+                      : W == 16 ? cudaLaunchKernelEx(&L.cfg, k_route_single<16>, p)
+                                : cudaLaunchKernelEx(&L.cfg, k_route_single<kSingleWarps>, p);
         if (e != cudaSuccess) { set_error("route single launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
         return MOE_OK;
     }
