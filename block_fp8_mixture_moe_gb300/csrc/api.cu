@@ -419,6 +419,10 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
                                    defer_pads ? offsets : nullptr, counts,
                                    defer_pads ? sorted_idx : nullptr, E_local);
     if (rc) return rc;
+    // The gate/up output: fp32 split partials, or with a single split the BF16 value the
+    // act-quant would round it to (the same round-to-nearest-even), at half the bytes written and
+    // read.  Measured on GB300: prefill 710.1 -> 704.1 us, decode M=128 and 256 -0.4 us.
+    const moe_dtype gu_dtype = P.splits == 1 ? MOE_DTYPE_BF16 : MOE_DTYPE_F32;
     // A few routes (decode batches of 1-4 tokens at top-8): the gate/up GEMM sorts them itself
     // from topk_ids, so its weight stream starts while routing and input quantisation still run.
     // Otherwise it waits for the input quantisation before reading route preparation's tables.
@@ -426,27 +430,27 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     if (self_route)
         rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
                                  w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
-                                 MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/false,
+                                 gu_dtype, P.slots, P.splits, true, stream, /*wait_first=*/false,
                                  topk_ids, expert_map, P.R, E, nullptr, dyn_gu ? sched : nullptr);
     else
         rc = launch_grouped_gemm(MOE_PROJ_GATE_UP, xq, xs, P.slots, H, wgu_q, wgu_s, E_local, 2 * N,
                                  w_layout, sorted_idx, block_expert, num_blocks, P.B_cap, P.bm, gu,
-                                 MOE_DTYPE_F32, P.slots, P.splits, true, stream, /*wait_first=*/true,
+                                 gu_dtype, P.slots, P.splits, true, stream, /*wait_first=*/true,
                                  nullptr, nullptr, 0, 0, nullptr, dyn_gu ? sched : nullptr);
     if (rc) return rc;
     // act-quant walks the routes (through route_slot) or, when the blocks hold fewer slots than
     // there are routes (an expert map that keeps few of them), the slots of the blocks that exist
     const bool slot_rows = expected_blocks(M, k, E, E_local, P.bm) * P.bm < P.R;
     if (kept_walk)
-        rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
+        rc = launch_act_quant(act, gu, gu_dtype, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
                               nullptr, nullptr, 0, kept_slot, 0, P.slots, aq, as, MOE_QUANT_PERSISTENT,
                               true, stream, /*map_early=*/true, nullptr, nullptr, 0, n_kept);
     else if (slot_rows)
-        rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.slots, N, clamp_limit, act_fmt,
+        rc = launch_act_quant(act, gu, gu_dtype, P.splits, P.slots, P.slots, N, clamp_limit, act_fmt,
                               nullptr, nullptr, 0, nullptr, 0, P.slots, aq, as, MOE_QUANT_PERSISTENT,
                               true, stream, false, sorted_idx, num_blocks, P.bm);
     else
-        rc = launch_act_quant(act, gu, MOE_DTYPE_F32, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
+        rc = launch_act_quant(act, gu, gu_dtype, P.splits, P.slots, P.R, N, clamp_limit, act_fmt,
                               nullptr, nullptr, 0, route_slot, 0, P.slots, aq, as,
                               MOE_QUANT_PERSISTENT, true, stream, /*map_early=*/true);
     if (rc) return rc;

@@ -305,8 +305,9 @@ MOEFP8_API int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
  *     the outputs of moe_route_prepare;
  *   XQ  E4M3 [slots, H]: the quantised input, row = slot of a kept route;
  *   XS  f32 scales of XQ: STAGED [slots, KB]; FUSED K-block major [KB, slots];
- *   GU  f32 gate/up partial sums: STAGED [S, slots, 2N] (split p covers K-blocks
- *       [p*KB/S, (p+1)*KB/S)); FUSED [pieces, num_blocks * block_m, 2N], piece q of a
+ *   GU  gate/up partial sums: STAGED f32 [S, slots, 2N] (split p covers K-blocks
+ *       [p*KB/S, (p+1)*KB/S)), or with S = 1 the sum rounded to BF16, bf16 [slots, 2N];
+ *       FUSED f32 [pieces, num_blocks * block_m, 2N], piece q of a
  *       128-column tile is its q-th stream-K range (see moe_blockfp8_forward);
  *   AQ  E4M3 [slots, N]: the quantised SiLU*mul activation; AS its scales: STAGED
  *       [slots, GN]; FUSED [GN, slots];

@@ -68,9 +68,12 @@ def test_dynamic_tail_computes_every_unit_as_the_static_split(ops):
 
     xq = _region(ws, lay, "xq", torch.uint8, slots * H).view(slots, H)
     xs = _region(ws, lay, "xs", torch.float32, slots * (H // 128)).view(slots, H // 128)
-    gu_layer = _region(ws, lay, "gu", torch.float32, S * slots * 2 * N).view(S, slots, 2 * N).clone()
+    # one split: the layer keeps the BF16-rounded sum; several: the fp32 partials
+    gu_t, gu_dt = (torch.bfloat16, ops.DTYPE_BF16) if S == 1 else (torch.float32, ops.DTYPE_F32)
+    gu_layer = _region(ws, lay, "gu", gu_t, S * slots * 2 * N).view(S, slots, 2 * N).clone()
     gu_static = ops.moe_blockfp8_grouped_gemm(ops.PROJ_GATE_UP, xq, xs, wgu, L["wgu_s"], route, bm,
-                                              out_dtype=ops.DTYPE_F32, out_rows=slots, splits=S)
+                                              out_dtype=gu_dt, out_rows=slots,
+                                              splits=S).view(S, slots, 2 * N)
     torch.cuda.synchronize()
     assert torch.equal(gu_layer[:, kept_slots], gu_static[:, kept_slots])
 

@@ -38,6 +38,8 @@ CASES = [
     ("decode_m32", dict(wl.CONFIGS["decode"], M=32), 22, dict(act=1, clamp=INF, fmt=0)),
     ("ep_t100", dict(wl.CONFIGS["ep"], M=100), 23, dict(act=1, clamp=7.0, fmt=1)),
     ("gate_upper_m4", dict(wl.CONFIGS["decode"], M=4), 24, dict(act=2, clamp=1.0, fmt=1)),
+    # a single gate/up split: the layer stores the gate/up value in BF16
+    ("decode_m64", dict(wl.CONFIGS["decode"], M=64), 25, dict(act=1, clamp=7.0, fmt=1)),
 ]
 
 
@@ -64,6 +66,10 @@ def _gate_up_sum(host, lay, path, slots_kept, S, slots, N, bm, nblk, KB1):
     """The fp32 gate/up value of each kept slot as the layer's act-quant adds it up: partials
     in split (staged) or stream-K piece (fused) order, fp32 additions, starting from the first."""
     W = 2 * N
+    if path == STAGED and S == 1:
+        # one split: the layer stores the BF16-rounded sum (exact in fp32)
+        g16 = _view(host, lay["gu"], np.uint16, slots * W).reshape(slots, W)[slots_kept]
+        return (g16.astype(np.uint32) << 16).view(np.float32)
     if path == STAGED:
         gu = _view(host, lay["gu"], np.float32, S * slots * W).reshape(S, slots, W)
         acc = gu[0][slots_kept].copy()
