@@ -424,7 +424,8 @@ __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __re
                                                             int fmt, int* status,
                                                             const int32_t* pad_off,
                                                             const int32_t* pad_cnt,
-                                                            int32_t* pad_sorted, int pad_E) {
+                                                            int32_t* pad_sorted, int pad_E,
+                                                            int late_release) {
     constexpr int kHold = kInputHold;
     const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
     const int G = H / 128;
@@ -463,9 +464,10 @@ __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __re
             }
         }
     };
-    // the next launch (the gate/up GEMM) may start at once: it waits for this one before it reads
-    // anything, so its set-up overlaps this kernel
-    grid_dep_launch();
+    // The next launch (the gate/up GEMM) is released at once, or with late_release only after
+    // this kernel's routing wait: route preparation is then complete, and the GEMM reads its
+    // tables as soon as it starts, waiting for this kernel only before its activation tiles.
+    if (!late_release) grid_dep_launch();
     uint2 hc[kHold];
     float hs[kHold];
     int ht[kHold], hg[kHold];
@@ -473,6 +475,7 @@ __global__ void __launch_bounds__(256) k_input_quant_tokens(const uint16_t* __re
 #pragma unroll
     for (int i = 0; i < kHold; ++i) ha[i] = quant(w0 + i * warps, ht[i], hg[i], hc[i], hs[i]);
     grid_dep_wait();
+    if (late_release) grid_dep_launch();
 #pragma unroll
     for (int i = 0; i < kHold; ++i)
         if (ha[i]) scatter(ht[i], hg[i], hc[i], hs[i]);
@@ -693,7 +696,8 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
 int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t* route_slot,
                               int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
                               cudaStream_t stream, const int32_t* pad_offset,
-                              const int32_t* pad_count, int32_t* pad_sorted, int pad_E) {
+                              const int32_t* pad_count, int32_t* pad_sorted, int pad_E,
+                              bool late_release) {
     const long long pairs = (static_cast<long long>(M) * (H / 128) + 1) / 2;
     if (pairs == 0) return MOE_OK;
     // One pair per warp, at most two CTAs per SM, so the next kernel's CTAs fit beside them.
@@ -708,10 +712,10 @@ int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t*
     cudaError_t e = pad_sorted
         ? cudaLaunchKernelEx(&L.cfg, k_input_quant_tokens<true>, static_cast<const uint16_t*>(x), M, H, k,
                              route_slot, slots, xq, xs, static_cast<int>(fmt), device_status_ptr(),
-                             pad_offset, pad_count, pad_sorted, pad_E)
+                             pad_offset, pad_count, pad_sorted, pad_E, late_release ? 1 : 0)
         : cudaLaunchKernelEx(&L.cfg, k_input_quant_tokens<false>, static_cast<const uint16_t*>(x), M, H, k,
                              route_slot, slots, xq, xs, static_cast<int>(fmt), device_status_ptr(),
-                             pad_offset, pad_count, pad_sorted, pad_E);
+                             pad_offset, pad_count, pad_sorted, pad_E, late_release ? 1 : 0);
     if (e != cudaSuccess) { set_error("input quant launch: %s", cudaGetErrorString(e)); return MOE_ERR_LAUNCH; }
     return MOE_OK;
 }

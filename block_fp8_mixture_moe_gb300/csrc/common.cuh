@@ -45,7 +45,7 @@ int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t*
                               int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
                               cudaStream_t stream, const int32_t* pad_offset = nullptr,
                               const int32_t* pad_count = nullptr, int32_t* pad_sorted = nullptr,
-                              int pad_E = 0);
+                              int pad_E = 0, bool late_release = false);
 int launch_route_prepare(const int32_t* topk_ids, int M, int k, int E, const int32_t* expert_map,
                          int E_local, int block_m, moe_route_path path, int32_t* sorted_idx,
                          int32_t* block_expert, int32_t* num_blocks, int32_t* expert_count,
