@@ -53,6 +53,8 @@ struct AQArgs {
     // nullable: the number of work rows, read on the device (rows is then an upper bound)
     const int32_t* n_rows;
     int* status;
+    // release the next launch before this kernel's dependency wait (see launch_act_quant)
+    int early_release;
 };
 
 // Loads 8 consecutive inputs as fp32 values of their BF16 materialisation.
@@ -385,8 +387,9 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
         __syncthreads();
         smap = aq_smap;
     }
+    if (p.early_release) grid_dep_launch();
     grid_dep_wait();
-    grid_dep_launch();
+    if (!p.early_release) grid_dep_launch();
     if (!PERSISTENT) {
         if (pair < pairs) quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, pre);
         return;
@@ -617,7 +620,7 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
                      const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
                      float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream,
                      bool map_early, const int32_t* slot_route, const int32_t* n_blocks, int bm,
-                     const int32_t* n_rows) {
+                     const int32_t* n_rows, bool early_release) {
     if (!in || !out_q || !out_s) { set_error("silu_mul_quant_fp8: null pointer"); return MOE_ERR_ARG; }
     if (!aligned16(in) || !aligned16(out_q) || (reinterpret_cast<uintptr_t>(out_s) & 3u)) {
         set_error("silu_mul_quant_fp8: in/out_q must be 16-byte aligned, out_s 4-byte aligned");
@@ -674,6 +677,7 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
     p.n_blocks = n_blocks;
     p.bm = bm;
     p.n_rows = n_rows;
+    p.early_release = early_release ? 1 : 0;
     p.status = device_status_ptr();
     bool persistent;
     if (strategy == MOE_QUANT_PER_GROUP) persistent = false;

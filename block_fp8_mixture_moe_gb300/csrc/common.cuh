@@ -39,7 +39,8 @@ int launch_act_quant(moe_act act, const void* in, moe_dtype in_dtype, int in_spl
                      const int32_t* row_map, int row_div, int out_rows, uint8_t* out_q,
                      float* out_s, moe_quant_strategy strategy, bool pdl, cudaStream_t stream,
                      bool map_early = false, const int32_t* slot_route = nullptr,
-                     const int32_t* n_blocks = nullptr, int bm = 0, const int32_t* n_rows = nullptr);
+                     const int32_t* n_blocks = nullptr, int bm = 0, const int32_t* n_rows = nullptr,
+                     bool early_release = false);
 // Per-token input quantisation scattered to the route slots (the layer's first stage).
 int launch_input_quant_tokens(const void* x, int M, int H, int k, const int32_t* route_slot,
                               int slots, uint8_t* xq, float* xs, moe_scale_fmt fmt, bool pdl,
