@@ -151,19 +151,23 @@ constexpr size_t kSchedBytes = 256;
 
 // A GEMM takes the dynamic tail when its expected weight stream is at least this many bytes per
 // SM.  Measured on GB300 (graph-replayed layer, interleaved A/B): the Zipf prefill shape (about
-// 21 and 10 MB per SM for gate/up and down) went from 780 to 741 us.  With every GEMM taking
-// it, decode M=64 lost 5 us, M=32 and the expert-parallel shape 2 us, M=256 gained 3.5 us; a
-// threshold of 6 MB (taking the gate/up GEMMs of M=128 and 256) measured the same as 8 MB.
-// The self-routed gate/up GEMM would also have to wait for its predecessor before the tail
-// (decode M=1: 33.4 -> 41.4 us with it).
+// 21 and 10 MB per SM for gate/up and down, block_m 32) went from 780 to 741 us.  Before the
+// tail's chunks were taken late (kDynLookahead in the GEMM), every decode and expert-parallel
+// GEMM lost with it; the self-routed gate/up GEMM would also have to wait for its predecessor
+// before the tail (decode M=1: 33.4 -> 41.4 us with it).
 constexpr double kDynTailMinBytesPerSm = 8.0 * 1024 * 1024;
+// With late chunks, block_m 16 (the decode GEMMs' 16-token blocks) from 2.5 MiB per SM: both
+// GEMMs at decode M=64 -3.4 us, M=128 -8.6, M=256 -7.2; the gate/up GEMM of M=32 (3.8 MiB)
+// unchanged, of M=16 (2.35 MiB) +4 us with it, so it stays below the threshold.
+constexpr double kDynTailMinBytesPerSmBm16 = 2.5 * 1024 * 1024;
 
 // Whether a GEMM of N_out x K weights per expert takes the dynamic tail (see
 // kDynTailMinBytesPerSm): its expected active-expert weight bytes per SM.
 bool dyn_tail(int M, int k, int E, int E_local, int N_out, int K, int bm) {
     if (bm > 32) return false;  // built for the plan's block sizes, 16 and 32
     const double bytes = expected_blocks(M, k, E, E_local, bm) * (N_out / 128) * (K / 128) * 128.0 * 128.0;
-    return bytes / std::max(1, sm_count()) >= kDynTailMinBytesPerSm;
+    const double min_bytes = bm <= 16 ? kDynTailMinBytesPerSmBm16 : kDynTailMinBytesPerSm;
+    return bytes / std::max(1, sm_count()) >= min_bytes;
 }
 
 // One workspace layout serves both forward paths: the token-scale and partial-sum regions are

@@ -97,6 +97,10 @@ struct GemmArgs {
 // 512 KB units always go one to a chunk): chunks of 1 / 2 / 3 / 4 / 5 units gave 757 / 712.9 /
 // 713.8 / 710.9 / 720.6 us for the layer, the best at 4 units, which divide its 32-tile blocks.
 constexpr long long kSchedChunkBytes = 384 * 1024;
+// descriptors of a CTA's queue still unconsumed when it takes its next dynamic chunk: at most
+// kDynLookahead - 1.  Measured at the prefill shape: 2 / 3 / 4 gave 702.5 / 701.8 / 701.7 us
+// against 703.6 us when chunks were taken as soon as the ring had room.
+constexpr int kDynLookahead = 3;
 
 template <int BM>
 struct Cfg {
@@ -364,8 +368,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
             seek(lo);
             left = units * (blockIdx.x + 1) / gridDim.x - lo;
         }
-        unsigned long long dyn_pend = 0;  // lane 0: the counter value of the chunk taken ahead
-        bool dyn_started = false;
+        long long npub = 0;  // descriptors published
         for (;;) {
             while (left > 0 && ok) {
                 if (self_route && b != cur_b) {
@@ -471,6 +474,7 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                             ++npend;
                         }
                         if (++slot == C::kRing) { slot = 0; ph ^= 1u; }
+                        ++npub;
                         if (npend == C::kDefer) flush_pending();
                     }
                 }
@@ -489,16 +493,20 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                 // for its predecessor (self-routing) does so first.  Each chunk's successor is taken
                 // when the chunk starts, so the atomic's round trip overlaps the chunk's descriptors.
                 if (!dep_done) flush_pending();
-                unsigned long long v = 0;
-                if (!dyn_started) {
-                    if (lane == 0) v = atomicAdd(p.sched, static_cast<unsigned long long>(p.sched_chunk));
-                    dyn_started = true;
-                } else {
-                    v = dyn_pend;
+                // A chunk is taken only once the descriptor kDynLookahead back has been consumed,
+                // so that chunks go out near the end of each CTA's queued work.  Taken as soon as
+                // the ring had room, every chunk went out within the first ~35 us at decode M=32
+                // (the ring holds 8 descriptors, a CTA ~9 units) and nothing was balanced.
+                if (npub >= kDynLookahead) {
+                    const int j = slot >= kDynLookahead ? slot - kDynLookahead : slot - kDynLookahead + C::kRing;
+                    const uint32_t pj = slot >= kDynLookahead ? ph : ph ^ 1u;
+                    ok = mbar_wait_fast(dempty + j, pj, abort_flag, p.status);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 }
+                unsigned long long v = 0;
+                if (lane == 0) v = atomicAdd(p.sched, static_cast<unsigned long long>(p.sched_chunk));
                 const long long c = dyn_base + static_cast<long long>(__shfl_sync(0xFFFFFFFFu, v, 0));
                 if (c >= units) break;
-                if (lane == 0) dyn_pend = atomicAdd(p.sched, static_cast<unsigned long long>(p.sched_chunk));
                 seek(c);
                 left = min(static_cast<long long>(p.sched_chunk), units - c);
             }

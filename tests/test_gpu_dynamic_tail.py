@@ -30,8 +30,10 @@ def test_plan_takes_the_dynamic_tail_only_on_long_streams(ops):
     p = wl.CONFIGS["prefill"]
     assert ops.moe_blockfp8_dynamic_tail(p["M"], p["k"], p["E"], p["E_local"], p["H"], p["N"]) == (True, True)
     d = wl.CONFIGS["decode"]
-    for M in (1, 32, 256):
-        assert ops.moe_blockfp8_dynamic_tail(M, d["k"], d["E"], d["E_local"], d["H"], d["N"]) == (False, False)
+    # block_m 16 from 2.5 MB of weights per SM: the gate/up GEMM from M=32, the down GEMM from 64
+    for M, want in ((1, (False, False)), (16, (False, False)), (32, (True, False)),
+                    (64, (True, True)), (256, (True, True))):
+        assert ops.moe_blockfp8_dynamic_tail(M, d["k"], d["E"], d["E_local"], d["H"], d["N"]) == want
     e = wl.CONFIGS["ep"]
     assert ops.moe_blockfp8_dynamic_tail(1024, e["k"], e["E"], e["E_local"], e["H"], e["N"]) == (False, False)
     with pytest.raises(ops.MoeError):
