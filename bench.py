@@ -400,7 +400,9 @@ def run_ours(args):
                     "weights": args.weights, "peak_source": peak_src}
     else:
         # the dominant kernel of the staged layer: the gate/up grouped GEMM, timed alone
-        roofline = {"bound": "hbm", "kernel": f"k_grouped_gemm<{bm}> (gate/up, split-K {splits})",
+        roofline = {"bound": "hbm",
+                    "kernel": f"k_grouped_gemm<{bm}> (gate/up, split-K {splits}; timed alone through "
+                              f"moe_blockfp8_grouped_gemm, static unit split)",
                     "achieved": round(gemm_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(gemm_achieved / hbm_peak, 4), "traffic": recorded_traffic("staged"),
                     "algorithmic_bytes": int(gu_mean_bytes),
