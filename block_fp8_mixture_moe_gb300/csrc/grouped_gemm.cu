@@ -98,9 +98,10 @@ struct GemmArgs {
 // 713.8 / 710.9 / 720.6 us for the layer, the best at 4 units, which divide its 32-tile blocks.
 constexpr long long kSchedChunkBytes = 384 * 1024;
 // descriptors of a CTA's queue still unconsumed when it takes its next dynamic chunk: at most
-// kDynLookahead - 1.  Measured at the prefill shape: 2 / 3 / 4 gave 702.5 / 701.8 / 701.7 us
-// against 703.6 us when chunks were taken as soon as the ring had room.
-constexpr int kDynLookahead = 3;
+// kDynLookahead(BM) - 1.  Measured at the prefill shape (block_m 32): 2 / 3 / 4 gave 702.5 /
+// 701.8 / 701.7 us against 703.6 us when chunks were taken as soon as the ring had room; at
+// decode (block_m 16) 2 against 3: M=32 -0.3 us, M=64 -0.5, M=256 -0.6.
+__host__ __device__ constexpr int kDynLookahead(int bm) { return bm <= 16 ? 2 : 3; }
 
 template <int BM>
 struct Cfg {
@@ -493,13 +494,14 @@ __global__ void __launch_bounds__(Cfg<BM>::kThreads, 1)
                 // for its predecessor (self-routing) does so first.  Each chunk's successor is taken
                 // when the chunk starts, so the atomic's round trip overlaps the chunk's descriptors.
                 if (!dep_done) flush_pending();
-                // A chunk is taken only once the descriptor kDynLookahead back has been consumed,
+                // A chunk is taken only once the descriptor kDynLookahead(BM) back has been consumed,
                 // so that chunks go out near the end of each CTA's queued work.  Taken as soon as
                 // the ring had room, every chunk went out within the first ~35 us at decode M=32
                 // (the ring holds 8 descriptors, a CTA ~9 units) and nothing was balanced.
-                if (npub >= kDynLookahead) {
-                    const int j = slot >= kDynLookahead ? slot - kDynLookahead : slot - kDynLookahead + C::kRing;
-                    const uint32_t pj = slot >= kDynLookahead ? ph : ph ^ 1u;
+                constexpr int kLa = kDynLookahead(BM);
+                if (npub >= kLa) {
+                    const int j = slot >= kLa ? slot - kLa : slot - kLa + C::kRing;
+                    const uint32_t pj = slot >= kLa ? ph : ph ^ 1u;
                     ok = mbar_wait_fast(dempty + j, pj, abort_flag, p.status);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 }
