@@ -126,15 +126,17 @@ double expected_blocks(int M, int k, int E, int E_local, int bm) {
 }
 
 // Split-K of the gate/up GEMM: the smallest split whose round-robin schedule is within a few
-// percent of the best achievable balance over the SMs.  At most 8 splits: the activation
-// kernel then sums a row's partials with one round trip to memory (its loads of 8 splits are in
-// flight together), and on GB300 more splits measured no faster at any decode size.
+// percent of the best achievable balance over the SMs.  At most 4 splits: the activation kernel
+// then takes its one-group-per-warp form and releases the down GEMM early, and with one split
+// the GEMM stores BF16.  Measured on GB300 against at most 8 (graph-replayed layer, interleaved
+// A/B, three rounds): decode M=2 (7 -> 2 splits) -0.3 us, M=4 (6 -> 1) -1.15, M=8 (7 -> 3)
+// -2.35.  Above 8 splits nothing measured faster at any decode size.
 int gate_up_splits(int M, int k, int E, int E_local, int H, int N, int bm, int sms) {
     const int KB = H / 128;
     const double units1 = expected_blocks(M, k, E, E_local, bm) * (2 * N / 128);
     int best = 1;
     double best_cost = 1e300;
-    const int smax = std::min(KB, 8);
+    const int smax = std::min(KB, 4);
     for (int s = 1; s <= smax; ++s) {
         const double units = units1 * s;
         const double waves = std::ceil(units / sms);
