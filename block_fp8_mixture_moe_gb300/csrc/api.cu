@@ -189,6 +189,13 @@ Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int 
     P.B_cap = (P.R + P.bm - 1) / P.bm + std::min(E_local, P.R);
     P.slots = P.B_cap * P.bm;
     P.splits = gate_up_splits(M, k, E, E_local, H, N, P.bm, sms);
+    // With the dynamic tail on the gate/up GEMM at block_m 16, one split leaves units of a whole
+    // K range (896 KB at H=7168, ~19 us of one SM's stream), too coarse for the tail to even out
+    // the SMs' end times; two halve them.  Above ~1024 routes the extra fp32 partials cost more.
+    // Measured on GB300 (interleaved A/B, three rounds): decode M=64 -2.1 us, M=96 and 128 -0.1
+    // to -0.4; M=256 +1.0 with two splits; three or four splits slower at every decode size.
+    if (P.splits == 1 && P.bm <= 16 && P.R <= 1024 && H >= 256 && dyn_tail(M, k, E, E_local, 2 * N, H, P.bm))
+        P.splits = 2;
     size_t o = 0;
     auto take = [&o](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
     P.off_sorted = take(sizeof(int32_t) * P.slots);
