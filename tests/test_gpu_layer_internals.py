@@ -37,8 +37,9 @@ CASES = [
     ("decode_m1", dict(wl.CONFIGS["decode"], M=1), 21, dict(act=1, clamp=INF, fmt=0)),
     ("decode_m32", dict(wl.CONFIGS["decode"], M=32), 22, dict(act=1, clamp=INF, fmt=0)),
     ("ep_t100", dict(wl.CONFIGS["ep"], M=100), 23, dict(act=1, clamp=7.0, fmt=1)),
+    # M=4 takes a single gate/up split: the layer stores the gate/up value in BF16
     ("gate_upper_m4", dict(wl.CONFIGS["decode"], M=4), 24, dict(act=2, clamp=1.0, fmt=1)),
-    # a single gate/up split: the layer stores the gate/up value in BF16
+    # two gate/up splits under the gate/up GEMM's dynamic tail
     ("decode_m64", dict(wl.CONFIGS["decode"], M=64), 25, dict(act=1, clamp=7.0, fmt=1)),
 ]
 
