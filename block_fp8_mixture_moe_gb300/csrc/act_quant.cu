@@ -589,8 +589,9 @@ int launch_aq_kg(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream
     if constexpr (ACT != MOE_ACT_IDENTITY && F32IN && KG <= 4) {
         // Few groups of split partials (decode batches): one group per warp (quant_item4).
         // Measured on GB300 against group pairs, graph-replayed layer, interleaved A/B: decode
-        // M=1 33.4 -> 32.7 us, M=16 113.2 -> 112.0, M=32 161.9 -> 160.8.  With 8 splits (M=2 to 8)
-        // it measured no faster, and with many groups (expert-parallel, prefill) 2-2.5 us slower.
+        // M=1 33.4 -> 32.7 us, M=16 113.2 -> 112.0, M=32 161.9 -> 160.8.  With 8 splits (M=2 to 8,
+        // which took 6 to 8 before the layer capped the split count at 4) it measured no faster,
+        // and with many groups (expert-parallel, prefill) 2-2.5 us slower.
         const long long items = static_cast<long long>(p.rows) * p.G;
         if (persistent && items <= 4LL * sm_count())
             return launch_aq_grid<ACT, F32IN, KG, true, true>(p, items, persistent, pdl, stream);
