@@ -179,12 +179,19 @@ __device__ __forceinline__ bool row_source(const AQArgs& p, int w, int* in_row, 
     return true;
 }
 
-// The gate and up inputs of one lane, 4 values each, from fp32 split-K partials (the layer's
-// few-item shape below): the same loads in flight together and additions in split order as
-// load_gate_up.
-template <int KG>
+// The gate and up inputs of one lane, 4 values each (the layer's few-item shape below): BF16
+// (one 8-byte load per operand), or fp32 split-K partials with the same loads in flight
+// together and additions in split order as load_gate_up.
+template <bool F32IN, int KG>
 __device__ __forceinline__ void load_gate_up4(const AQArgs& p, long long off_g, long long off_u,
                                               float* g, float* u) {
+    if constexpr (!F32IN) {
+        const uint2 wg = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.in) + off_g));
+        const uint2 wu = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.in) + off_u));
+        g[0] = bf16_lo(wg.x); g[1] = bf16_hi(wg.x); g[2] = bf16_lo(wg.y); g[3] = bf16_hi(wg.y);
+        u[0] = bf16_lo(wu.x); u[1] = bf16_hi(wu.x); u[2] = bf16_lo(wu.y); u[3] = bf16_hi(wu.y);
+        return;
+    }
     const float* bg = static_cast<const float*>(p.in) + off_g;
     const float* bu = static_cast<const float*>(p.in) + off_u;
     for (int s0 = 0; s0 < p.in_splits; s0 += KG) {
@@ -306,7 +313,7 @@ __device__ __forceinline__ void quant_pair(const AQArgs& p, long long pair, int 
 // the work (decode batches); where the SMs are full of warps (expert-parallel and prefill
 // shapes) the per-item overhead over 4 values instead of 8 makes it slower, so the launcher
 // takes it only for few items.
-template <int ACT, int KG>
+template <int ACT, bool F32IN, int KG>
 __device__ __forceinline__ void quant_item4(const AQArgs& p, long long item, int lane, int pre,
                                             const int* smap) {
     bool active = item < static_cast<long long>(p.rows) * p.G;
@@ -333,7 +340,7 @@ __device__ __forceinline__ void quant_item4(const AQArgs& p, long long item, int
         const long long col = static_cast<long long>(g) * 128 + lane * 4;
         const long long rbase = static_cast<long long>(in_row) * p.W;
         float gv[4], uv[4];
-        load_gate_up4<KG>(p, rbase + col, rbase + p.N + col, gv, uv);
+        load_gate_up4<F32IN, KG>(p, rbase + col, rbase + p.N + col, gv, uv);
         if (slot_walk && route < 0) active = false;  // a pad slot
         if (active) {
 #pragma unroll
@@ -403,7 +410,7 @@ __global__ void __launch_bounds__(256) k_act_quant(AQArgs p) {
     for (; pair < pairs; pair += stride) {
         const int nxt = ahead ? sel_of(pair + stride) : -2;
         if constexpr (W4)
-            quant_item4<ACT, KG>(p, pair, lane, ahead ? cur : -2, smap);
+            quant_item4<ACT, F32IN, KG>(p, pair, lane, ahead ? cur : -2, smap);
         else
             quant_pair<ACT, F32IN, KG, INL>(p, pair, lane, ahead ? cur : -2, smap);
         cur = nxt;
@@ -586,12 +593,14 @@ int launch_aq_kg(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream
         set_error("act_quant: rows * N / 128 must be below 2^31");
         return MOE_ERR_ARG;
     }
-    if constexpr (ACT != MOE_ACT_IDENTITY && F32IN && KG <= 4) {
-        // Few groups of split partials (decode batches): one group per warp (quant_item4).
-        // Measured on GB300 against group pairs, graph-replayed layer, interleaved A/B: decode
+    if constexpr (ACT != MOE_ACT_IDENTITY && KG <= 4) {
+        // Few groups (decode batches), of split partials or of the BF16 value of one split: one
+        // group per warp (quant_item4).  Measured on GB300 against group pairs (split partials),
+        // graph-replayed layer, interleaved A/B: decode
         // M=1 33.4 -> 32.7 us, M=16 113.2 -> 112.0, M=32 161.9 -> 160.8.  With 8 splits (M=2 to 8,
         // which took 6 to 8 before the layer capped the split count at 4) it measured no faster,
-        // and with many groups (expert-parallel, prefill) 2-2.5 us slower.
+        // and with many groups (expert-parallel, prefill) 2-2.5 us slower.  On the BF16 value of
+        // one split (decode M=4, 5 and 10): M=4 -0.3 us, M=5 -1.0, M=10 -0.9.
         const long long items = static_cast<long long>(p.rows) * p.G;
         if (persistent && items <= 4LL * sm_count())
             return launch_aq_grid<ACT, F32IN, KG, true, true>(p, items, persistent, pdl, stream);
