@@ -601,9 +601,10 @@ int launch_aq_kg(const AQArgs& p, bool persistent, bool pdl, cudaStream_t stream
         // which took 6 to 8 before the layer capped the split count at 4) it measured no faster,
         // and with many groups (expert-parallel, prefill) 2-2.5 us slower.  On the BF16 value of
         // one split (decode M=4, 5 and 10): M=4 -0.3 us, M=5 -1.0, M=10 -0.9.  Up to 8 groups
-        // per SM instead of 4: M=48 -0.7 us, M=64 -0.55.
+        // per SM instead of 4: M=48 -0.7 us, M=64 -0.55; up to 16 instead of 8: M=96 -0.55,
+        // M=128 -0.3.
         const long long items = static_cast<long long>(p.rows) * p.G;
-        if (persistent && items <= 8LL * sm_count())
+        if (persistent && items <= 16LL * sm_count())
             return launch_aq_grid<ACT, F32IN, KG, true, true>(p, items, persistent, pdl, stream);
     }
     if constexpr (ACT != MOE_ACT_IDENTITY) {

@@ -134,13 +134,14 @@ def _split_sum_bf16(P):
     return acc.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("rows", [40, 700])
+@pytest.mark.parametrize("rows", [40, 700, 1400])
 @pytest.mark.parametrize("act,clamp,fmt", [(1, float("inf"), 0), (1, 7.0, 1), (2, 7.0, 0), (2, float("inf"), 1)])
 @pytest.mark.parametrize("splits", [1, 3, 4, 6])
 def test_persistent_split_partials(ops, splits, act, clamp, fmt, rows):
     """The persistent launch on split-K partials, as the layer runs it.  At most 4 splits with
-    few groups (40 rows of width 256: 80 groups) take one 128-column group per warp, 4 values a
-    lane; 6 splits or 1400 groups take the group pairs.  Both bitwise against the oracle."""
+    at most 16 groups per SM (40 or 700 rows of width 256: 80 or 1400 groups) take one
+    128-column group per warp, 4 values a lane; 6 splits or 2800 groups take the group pairs.
+    Both bitwise against the oracle."""
     N = 256
     r = np.random.default_rng(1000 * splits + rows + 10 * act + fmt)
     P = (r.standard_normal((splits, rows, 2 * N)) * 1.5).astype(np.float32)
