@@ -165,11 +165,11 @@ constexpr double kDynTailMinBytesPerSmBm16 = 2.5 * 1024 * 1024;
 
 // Whether a GEMM of N_out x K weights per expert takes the dynamic tail (see
 // kDynTailMinBytesPerSm): its expected active-expert weight bytes per SM.
-bool dyn_tail(int M, int k, int E, int E_local, int N_out, int K, int bm) {
+bool dyn_tail(int M, int k, int E, int E_local, int N_out, int K, int bm, int sms) {
     if (bm > 32) return false;  // built for the plan's block sizes, 16 and 32
     const double bytes = expected_blocks(M, k, E, E_local, bm) * (N_out / 128) * (K / 128) * 128.0 * 128.0;
     const double min_bytes = bm <= 16 ? kDynTailMinBytesPerSmBm16 : kDynTailMinBytesPerSm;
-    return bytes / std::max(1, sm_count()) >= min_bytes;
+    return bytes / std::max(1, sms) >= min_bytes;
 }
 
 // One workspace layout serves both forward paths: the token-scale and partial-sum regions are
@@ -194,7 +194,8 @@ Plan make_plan(int M, int k, int E, int E_local, int H, int N, int block_m, int 
     // the SMs' end times; two halve them.  Above ~1024 routes the extra fp32 partials cost more.
     // Measured on GB300 (interleaved A/B, three rounds): decode M=64 -2.1 us, M=96 and 128 -0.1
     // to -0.4; M=256 +1.0 with two splits; three or four splits slower at every decode size.
-    if (P.splits == 1 && P.bm <= 16 && P.R <= 1024 && H >= 256 && dyn_tail(M, k, E, E_local, 2 * N, H, P.bm))
+    if (P.splits == 1 && P.bm <= 16 && P.R <= 1024 && H >= 256 &&
+        dyn_tail(M, k, E, E_local, 2 * N, H, P.bm, sms))
         P.splits = 2;
     size_t o = 0;
     auto take = [&o](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
@@ -275,34 +276,40 @@ extern "C" int moe_forward_block_m(int M, int k, int E_local, int H, int N) {
     return forward_block_m(M, k, E_local, H, N);
 }
 
-extern "C" int moe_blockfp8_plan(int M, int k, int E, int E_local, int H, int N, int block_m,
-                                 int* out_block_m, int* out_B_cap, int* out_splits) {
+extern "C" int moe_blockfp8_plan_for_sms(int M, int k, int E, int E_local, int H, int N,
+                                         int block_m, int sms, int* out_block_m, int* out_B_cap,
+                                         int* out_splits, int* out_dyn_gate_up,
+                                         int* out_dyn_down) {
     clear_error();
-    if (M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0 || H % 128 || N % 128 ||
-        (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)) {
-        set_error("moe_blockfp8_plan: bad sizes");
+    if (sms <= 0 || M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0 || H % 128 ||
+        N % 128 || (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)) {
+        set_error("moe_blockfp8_plan: bad sizes or SM count");
         return MOE_ERR_ARG;
     }
-    const Plan P = make_plan(M, k, E, E_local, H, N, block_m, sm_count());
+    const Plan P = make_plan(M, k, E, E_local, H, N, block_m, sms);
     if (out_block_m) *out_block_m = P.bm;
     if (out_B_cap) *out_B_cap = P.B_cap;
     if (out_splits) *out_splits = P.splits;
+    if (out_dyn_gate_up) *out_dyn_gate_up = dyn_tail(M, k, E, E_local, 2 * N, H, P.bm, sms) ? 1 : 0;
+    if (out_dyn_down) *out_dyn_down = dyn_tail(M, k, E, E_local, H, N, P.bm, sms) ? 1 : 0;
     return MOE_OK;
+}
+
+extern "C" int moe_blockfp8_plan(int M, int k, int E, int E_local, int H, int N, int block_m,
+                                 int* out_block_m, int* out_B_cap, int* out_splits) {
+    return moe_blockfp8_plan_for_sms(M, k, E, E_local, H, N, block_m, sm_count(), out_block_m,
+                                     out_B_cap, out_splits, nullptr, nullptr);
 }
 
 extern "C" int moe_blockfp8_dynamic_tail(int M, int k, int E, int E_local, int H, int N, int block_m,
                                          int* gate_up, int* down) {
-    clear_error();
-    if (!gate_up || !down || M < 0 || k <= 0 || E <= 0 || E_local <= 0 || H <= 0 || N <= 0 ||
-        H % 128 || N % 128 ||
-        (block_m != 0 && block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)) {
-        set_error("moe_blockfp8_dynamic_tail: bad sizes or null outputs");
+    if (!gate_up || !down) {
+        clear_error();
+        set_error("moe_blockfp8_dynamic_tail: null outputs");
         return MOE_ERR_ARG;
     }
-    const int bm = block_m > 0 ? block_m : forward_block_m(M, k, E_local, H, N);
-    *gate_up = dyn_tail(M, k, E, E_local, 2 * N, H, bm) ? 1 : 0;
-    *down = dyn_tail(M, k, E, E_local, H, N, bm) ? 1 : 0;
-    return MOE_OK;
+    return moe_blockfp8_plan_for_sms(M, k, E, E_local, H, N, block_m, sm_count(), nullptr, nullptr,
+                                     nullptr, gate_up, down);
 }
 
 extern "C" size_t moe_blockfp8_workspace_bytes(int M, int k, int E, int E_local, int H, int N,
@@ -399,8 +406,8 @@ extern "C" int moe_blockfp8_forward(const void* x, const int32_t* topk_ids, cons
     const bool kept_walk = route_compacts(P.R, E, E_local, expert_map != nullptr);
     int32_t* kept_slot = reinterpret_cast<int32_t*>(ws + P.off_kslot);
     int32_t* n_kept = reinterpret_cast<int32_t*>(ws + P.off_nkept);
-    const bool dyn_gu = dyn_tail(M, k, E, E_local, 2 * N, H, P.bm);
-    const bool dyn_dn = dyn_tail(M, k, E, E_local, H, N, P.bm);
+    const bool dyn_gu = dyn_tail(M, k, E, E_local, 2 * N, H, P.bm, sm_count());
+    const bool dyn_dn = dyn_tail(M, k, E, E_local, H, N, P.bm, sm_count());
 
     int rc;
     if (fused) {

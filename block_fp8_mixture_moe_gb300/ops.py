@@ -52,6 +52,7 @@ SIGNATURES = {
                                ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "moe_blockfp8_dynamic_tail": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(ctypes.c_int)]),
+    "moe_blockfp8_plan_for_sms": (_I, [_I, _I, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(ctypes.c_int)] * 5),
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_get_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "moe_device_supported": (_I, []),
@@ -350,6 +351,17 @@ def moe_blockfp8_dynamic_tail(M, k, E, E_local, H, N, block_m=0):
     _check(load().moe_blockfp8_dynamic_tail(M, k, E, E_local, H, N, block_m, ctypes.byref(gu),
                                             ctypes.byref(dn)), "moe_blockfp8_dynamic_tail")
     return bool(gu.value), bool(dn.value)
+
+
+def moe_blockfp8_plan_for_sms(M, k, E, E_local, H, N, sms, block_m=0):
+    """(block_m, B_cap, splits, dynamic tail on the gate/up GEMM, on the down GEMM) for a device
+    with `sms` SMs; host only, no GPU needed."""
+    out = [ctypes.c_int(0) for _ in range(5)]
+    _check(load().moe_blockfp8_plan_for_sms(M, k, E, E_local, H, N, block_m, sms,
+                                            *[ctypes.byref(o) for o in out]),
+           "moe_blockfp8_plan_for_sms")
+    bm, bc, sp, gu, dn = (o.value for o in out)
+    return bm, bc, sp, bool(gu), bool(dn)
 
 
 def moe_blockfp8_forward(x, topk_ids, topk_w, E, expert_map, wgu_q, wgu_s, wd_q, wd_s,

@@ -337,12 +337,23 @@ MOEFP8_API int moe_blockfp8_plan(int M, int k, int E, int E_local, int H, int N,
 /* Whether the staged forward's gate/up and down GEMMs (*gate_up, *down: 1 or 0) hand out the
  * last quarter of their work units from a counter in the workspace instead of splitting all of
  * them statically over the SMs: only when a GEMM's expected active-expert weight stream is long
- * (at least 8 MB per SM), where the SMs' differing streaming rates would otherwise leave a
- * tail.  A scheduling choice of this library, no counterpart in the pages; every unit is
- * computed exactly as in the static split, so the results are the same bit for bit.  Host
- * only; MOE_OK, or MOE_ERR_ARG for bad sizes or null outputs. */
+ * (at least 8 MB per SM, 2.5 MiB per SM at block_m 16), where the SMs' differing streaming
+ * rates would otherwise leave a tail.  A scheduling choice of this library, no counterpart in
+ * the pages; every unit is computed exactly as in the static split, so the results are the
+ * same bit for bit.  Host only; MOE_OK, or MOE_ERR_ARG for bad sizes or null outputs. */
 MOEFP8_API int moe_blockfp8_dynamic_tail(int M, int k, int E, int E_local, int H, int N,
                                          int block_m, int* gate_up, int* down);
+
+/* The plan of moe_blockfp8_plan and moe_blockfp8_dynamic_tail for a device with `sms` SMs
+ * instead of the current device (152 on a GB300): block_m, block capacity, gate/up split
+ * count and the two dynamic-tail flags (1 or 0).  Any output pointer may be null.  It lets a
+ * host without that device compute the plan, and tests check the plan's rules without a GPU.
+ * A scheduling choice of this library, no counterpart in the pages.  Host only; MOE_OK, or
+ * MOE_ERR_ARG for bad sizes or sms <= 0. */
+MOEFP8_API int moe_blockfp8_plan_for_sms(int M, int k, int E, int E_local, int H, int N,
+                                         int block_m, int sms, int* out_block_m, int* out_B_cap,
+                                         int* out_splits, int* out_dyn_gate_up,
+                                         int* out_dyn_down);
 
 /* ------------------------------------------------------------------------------------------
  * Diagnostics.

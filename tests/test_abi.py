@@ -77,6 +77,34 @@ def test_pure_host_helpers(lib_path):
     assert L.moe_forward_block_m(1, 8, 256, 7168, 256) in (16, 32, 64, 128)
 
 
+def test_layer_plan_on_152_sms(lib_path):
+    """The layer plan for a GB300 (152 SMs), computed on the host: 16-token blocks up to M=256,
+    32 above; the gate/up split-K count (at most 4, two under the dynamic tail up to 1024
+    routes); and which GEMMs hand out their last units dynamically.  The table is the plan the
+    forward takes on the bench's decode, expert-parallel and prefill shapes."""
+    from block_fp8_mixture_moe_gb300 import ops
+    ops.load(lib_path)
+    import oracle
+    plan = lambda M, k, E, El, H, N: ops.moe_blockfp8_plan_for_sms(M, k, E, El, H, N, 152)
+    decode = {1: (4, False, False), 2: (2, False, False), 4: (1, False, False),
+              8: (3, False, False), 16: (4, False, False), 32: (2, True, False),
+              64: (2, True, True), 128: (2, True, True), 256: (1, True, True)}
+    for M, (splits, gu, dn) in decode.items():
+        bm, bc, sp, dgu, ddn = plan(M, 8, 256, 256, 7168, 256)
+        assert (bm, sp, dgu, ddn) == (16, splits, gu, dn), M
+        assert bc == oracle.block_capacity(M * 8, 256, 16)
+    assert plan(1024, 6, 256, 32, 2048, 2048)[0::2] == (32, 1, False)   # expert-parallel T=1024
+    assert plan(100, 6, 256, 32, 2048, 2048)[0::2] == (16, 2, False)    # T=100
+    assert plan(512, 8, 512, 512, 4096, 768)[0::2] == (32, 1, True)      # Zipf prefill
+    assert plan(512, 8, 512, 512, 4096, 768)[4] is True
+    for M in (1, 3, 7, 33, 300, 2048):
+        sp = plan(M, 8, 256, 256, 7168, 256)[2]
+        assert 1 <= sp <= 4
+    assert plan(4, 2, 16, 16, 128, 128)[2] == 1                          # one K-block: one split
+    with pytest.raises(ops.MoeError):
+        ops.moe_blockfp8_plan_for_sms(1, 8, 256, 256, 7168, 256, 0)
+
+
 def test_calls_without_a_gpu_fail_cleanly(lib_path):
     """On a machine without an sm_103 device every launch entry point refuses with
     MOE_ERR_UNSUPPORTED and launches nothing."""
