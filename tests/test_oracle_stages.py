@@ -244,6 +244,34 @@ def test_gemm_block_scaled_matches_float64_matmul(orc):
     assert (np.abs(ours - ref) <= step).all()
 
 
+def test_gemm_power_of_two_scales_is_exact(orc):
+    """Power-of-two (UE8M0-style) scales and E4M3 operands of magnitude >= 2^-3 (or zero): every
+    product and partial sum of the whole block-scaled GEMM is exact in double (a span of under
+    48 bits), so the result is the float64 matmul of the dequantised operands, in any order,
+    rounded once to BF16 (the nearest-BF16 rounding of double pinned in the codec tests)."""
+    r = np.random.default_rng(3)
+    R, K, N_out, E_loc = 9, 512, 256, 3
+    vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    ok = np.flatnonzero(np.isfinite(vals) & ((np.abs(vals) >= 0.125) | (vals == 0))).astype(np.uint8)
+    aq = r.choice(ok, (R, K))
+    wq = r.choice(ok, (E_loc, N_out, K))
+    a_s = np.ldexp(1.0, r.integers(-8, -3, (R, K // 128))).astype(np.float32)
+    w_s = np.ldexp(1.0, r.integers(-12, -7, (E_loc, N_out // 128, K // 128))).astype(np.float32)
+    rexp = r.integers(0, E_loc, R).astype(np.int32)
+    rows = r.permutation(R).astype(np.int32)
+    out = orc.route_gemm(aq, a_s, wq, w_s, rows, rexp)
+    A = vals[aq] * np.repeat(a_s.astype(np.float64), 128, axis=1)
+    W = vals[wq] * np.repeat(np.repeat(w_s.astype(np.float64), 128, axis=1), 128, axis=2)
+    ref = np.stack([W[rexp[i]] @ A[rows[i]] for i in range(R)])
+    assert (out == orc.bf16_round_double(ref)).all()
+    # the same operands with one weight block's scale doubled change that block's rows
+    w_s2 = w_s.copy()
+    w_s2[0, 0, 0] *= 2
+    out2 = orc.route_gemm(aq, a_s, wq, w_s2, rows, rexp)
+    hit = rexp == 0
+    assert (out2[~hit] == out[~hit]).all() and (out2[hit][:, :128] != out[hit][:, :128]).any()
+
+
 def test_gemm_skips_dropped_routes(orc):
     r = np.random.default_rng(2)
     aq = r.integers(0, 0x70, (4, 128)).astype(np.uint8)
