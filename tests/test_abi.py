@@ -122,6 +122,17 @@ def test_calls_without_a_gpu_fail_cleanly(lib_path):
     rc = L.moe_reduce(None, None, None, None, 1, 1, 1, 1, 8, None, None)
     assert rc == ops.MOE_ERR_UNSUPPORTED
     assert L.moe_last_error_string()
+    # every other launching entry point too (sizes 1, null pointers, zero floats): the device
+    # check comes before anything is read or launched
+    launching = ["moe_route_prepare", "moe_route_prepare_noalloc", "moe_blockfp8_grouped_gemm",
+                 "silu_mul_quant_fp8", "silu_and_mul_bf16", "moe_blockfp8_forward",
+                 "moe_blockfp8_pack_weights"]
+    for name in launching:
+        _, argtypes = ops.SIGNATURES[name]
+        args = [0.0 if a in (ctypes.c_float, ctypes.c_double) else
+                1 if a in (ctypes.c_int, ctypes.c_size_t, ctypes.c_ulonglong) else None
+                for a in argtypes]
+        assert getattr(L, name)(*args) == ops.MOE_ERR_UNSUPPORTED, name
 
 
 def test_forward_refuses_pageable_host_activations(lib_path):
